@@ -1,0 +1,488 @@
+"""Benchmark of the EAGLE draft-tree verify round on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one full round over one batch: eagle_build_tree -> eagle_tree_attention (all layers)
+-> eagle_tree_verify, through the C ABI, inputs resident in HBM.  Consecutive steps rotate over
+several independent input sets whose combined size is far above the 129 MB L2, so no step reads
+what the previous one left in L2.  Timing: CUDA events on the launching stream around exactly K
+steps, a barrier and a device synchronize on both sides, max over ranks; rank 0 prints one JSON
+line.  With N > 1 (torchrun) every rank runs its own replica of the workload (weak scaling; the
+round has no cross-sequence exchange).
+
+--impl reference times the fp64 CPU oracle on this machine's host cores on the same workload,
+metric and unit (each step a bounded sample of the round, extrapolated to rounds/s).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import datagen  # noqa: E402
+
+METRIC = "tree-verify rounds/s (build+attn+sample) at 8B shape; tree-attn HBM GB/s vs peak"
+UNIT = "rounds/s"
+
+
+def _peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def _workload_desc(wl) -> str:
+    ctx = f"ctx={wl.ctx}" if wl.ctx_min == wl.ctx else f"ctx=U[{wl.ctx_min},{wl.ctx}]"
+    return (f"{wl.name}: B={wl.batch} V={wl.vocab} D={wl.depth} k={wl.topk} m={wl.keep} L={wl.layers} "
+            f"Hq={wl.heads_q} Hkv={wl.heads_kv} d={wl.head_dim} {ctx} {wl.kv_dtype} KV, T={wl.temperature}")
+
+
+# ---------------------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------- our arm
+
+class Round:
+    """Device buffers and pre-marshalled C-ABI arguments of one input set."""
+
+    def __init__(self, eg, wl, seed, dev, ws, outs, temperature):
+        self.wl = wl
+        B, R, V, n = wl.batch, wl.rows, wl.vocab, wl.nodes
+        self.draft = datagen.draft_logits(B, R, V, seed, dev)
+        self.root = datagen.root_tokens(B, V, seed, dev)
+        self.attn = datagen.attention_inputs(wl, seed, dev)
+        self.u = datagen.uniforms(B, n, seed, dev)
+        # the target logits follow the tree of this round (built once here, outside timing)
+        tree = eg.build_tree(self.draft, self.root, depth=wl.depth, topk=wl.topk, keep=wl.keep, ws=ws)
+        self.target = datagen.target_logits(self.draft, tree["node_row"], datagen.noise_sigmas(wl, seed), seed)
+        torch.cuda.synchronize()
+        P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+        self.tcfg = eg.TreeCfg(B, V, wl.depth, wl.topk, wl.keep, 1.0)
+        dt = eg.EAGLE_DTYPE_F32 if wl.kv_dtype == "f32" else eg.EAGLE_DTYPE_BF16
+        self.acfg = eg.AttnCfg(B, wl.layers, n, wl.heads_q, wl.heads_kv, wl.head_dim, wl.max_seq, dt, 0.0)
+        self.vcfg = eg.VerifyCfg(B, V, wl.depth, wl.topk, wl.keep, float(temperature))
+        a = self.attn
+        self.build_args = (ctypes.byref(self.tcfg), P(self.draft), P(self.root), P(outs["tokens"]),
+                           P(outs["parents"]), P(outs["depths"]), P(outs["node_row"]), P(outs["mask"]),
+                           P(outs["node_logv"]))
+        self.attn_args = (ctypes.byref(self.acfg), P(a["q"]), P(a["k_cache"]), P(a["v_cache"]), P(a["ctx_len"]),
+                          P(a["k_tree"]), P(a["v_tree"]), P(outs["mask"]), P(outs["attn_out"]))
+        self.verify_args = (ctypes.byref(self.vcfg), P(self.target), P(self.draft), P(outs["tokens"]),
+                            P(outs["parents"]), P(outs["node_row"]), P(self.u), P(outs["out_tokens"]),
+                            P(outs["out_len"]), P(outs["out_path"]), None)
+
+    def bytes_per_set(self) -> int:
+        ts = [self.draft, self.root, self.u, self.target] + [v for v in self.attn.values()]
+        return sum(t.numel() * t.element_size() for t in ts)
+
+
+def run_ours(args, rank, world, dev) -> dict | None:
+    import eagle_draft_tree_gb300 as eg
+
+    lib = eg.load()
+    wl = datagen.WORKLOADS[args.workload]
+    T = wl.temperature if args.temperature is None else args.temperature
+    B, n, D = wl.batch, wl.nodes, wl.depth
+    ws = eg.Workspace(device=dev)
+    need = max(lib.eagle_build_tree_workspace_size(ctypes.byref(eg.TreeCfg(B, wl.vocab, D, wl.topk, wl.keep, 1.0))),
+               lib.eagle_tree_attention_workspace_size(ctypes.byref(eg.AttnCfg(
+                   B, wl.layers, n, wl.heads_q, wl.heads_kv, wl.head_dim, wl.max_seq,
+                   0 if wl.kv_dtype == "f32" else 1, 0.0))),
+               lib.eagle_tree_verify_workspace_size(ctypes.byref(eg.VerifyCfg(B, wl.vocab, D, wl.topk, wl.keep, T))))
+    ws.reserve(need)
+    outs = {k: torch.empty((B, n), dtype=torch.int32, device=dev) for k in ("tokens", "parents", "depths", "node_row")}
+    outs["mask"] = torch.empty((B, n), dtype=torch.int64, device=dev)
+    outs["node_logv"] = torch.empty((B, n), dtype=torch.float32, device=dev)
+    outs["out_tokens"] = torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    outs["out_len"] = torch.empty((B,), dtype=torch.int32, device=dev)
+    outs["out_path"] = torch.empty((B, D), dtype=torch.int32, device=dev)
+    kvdt = torch.float32 if wl.kv_dtype == "f32" else torch.bfloat16
+    outs["attn_out"] = torch.empty((wl.layers, B, n, wl.heads_q, wl.head_dim), dtype=kvdt, device=dev)
+
+    sets = [Round(eg, wl, 1000 * rank + 17 * s + args.seed, dev, ws, outs, T) for s in range(args.sets)]
+    set_bytes = sets[0].bytes_per_set()
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    wsp, wsn = ws.ptr, ctypes.c_size_t(ws.nbytes)
+    launches = [0]
+
+    def step(rd: Round, ev: tuple | None = None):
+        st = lib.eagle_build_tree(*rd.build_args, wsp, wsn, sptr)
+        c = lib.eagle_last_launch_count()
+        if ev is not None:
+            ev[0].record(stream)
+        st |= lib.eagle_tree_attention(*rd.attn_args, wsp, wsn, sptr)
+        c += lib.eagle_last_launch_count()
+        if ev is not None:
+            ev[1].record(stream)
+        st |= lib.eagle_tree_verify(*rd.verify_args, wsp, wsn, sptr)
+        c += lib.eagle_last_launch_count()
+        if st != 0:
+            raise RuntimeError(f"C-ABI call failed with status {st}")
+        launches[0] += c
+
+    for i in range(args.warmup):
+        step(sets[i % len(sets)])
+    torch.cuda.synchronize(dev)
+    if ws.status(stream) != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    K = args.steps
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    launches[0] = 0
+    e0.record(stream)
+    for i in range(K):
+        step(sets[i % len(sets)], attn_ev[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
+    gpu_launches = launches[0]
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    if ws.status(stream) != 0:
+        raise RuntimeError("device status not OK after the timed steps")
+
+    # mean committed length (synthetic inputs; not comparable to the pages' acceptance lengths)
+    lens = []
+    for rd in sets:
+        step(rd)
+        lens.append(outs["out_len"].double().mean().item())
+    mean_len = statistics.mean(lens)
+
+    # end to end: per-round inputs from pinned host memory, the three calls, results back to host
+    e2e = run_e2e(eg, lib, wl, sets[0], outs, ws, stream, dev, min(K, args.e2e_steps), world)
+
+    bytes_ = datagen.bytes_of(wl, ctx_total=float(sets[0].attn["ctx_len"].sum().item()))
+    peaks = _peaks()
+    attn_bytes = bytes_["attention"]
+    achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
+    value = world * K / (ms * 1e-3)
+    metric_bytes = bytes_["metric"]
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": _workload_desc(wl), "temperature": T, "parallelism": f"replicas x{world}",
+                   "l2": f"{len(sets)} rotating input sets of {set_bytes / 1e6:.0f} MB each (> 129 MB L2)",
+                   "dtype_detail": "bf16 K/V/Q/O with fp32 softmax and accumulation; fp32 logits"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": _traffic(attn_bytes),
+                     "kernel": "tree_attn_bf16_kernel" if wl.kv_dtype == "bf16" else "tree_attn_f32_kernel",
+                     "algorithmic_bytes": attn_bytes, "avg_launch_ms": attn_ms,
+                     "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)"},
+        "end_to_end_hbm": {"metric_bytes": metric_bytes, "exact_bytes": bytes_["exact"],
+                           "gbs": metric_bytes / (ms / K * 1e-3) / 1e9,
+                           "frac": metric_bytes / (ms / K * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "mean_committed": mean_len,
+    }
+    return res
+
+
+def run_e2e(eg, lib, wl, rd: Round, outs, ws, stream, dev, steps, world) -> dict:
+    """The same round through the public calls with host inputs: every step copies the round's
+    inputs (logits, uniforms, root tokens, q and the tree's K/V, context lengths) from pinned host
+    memory and reads the committed tokens back.  The KV cache is decoder state resident on the
+    device, as in any serving stack."""
+    host = {}
+    names = [("draft", rd.draft), ("target", rd.target), ("u", rd.u), ("root", rd.root),
+             ("q", rd.attn["q"]), ("k_tree", rd.attn["k_tree"]), ("v_tree", rd.attn["v_tree"]),
+             ("ctx_len", rd.attn["ctx_len"])]
+    for k, t in names:
+        host[k] = t.detach().cpu().pin_memory()
+    dst = dict(names)
+    out_h = torch.empty(outs["out_tokens"].shape, dtype=torch.int32).pin_memory()
+    len_h = torch.empty(outs["out_len"].shape, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * 4 + len_h.numel() * 4
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    wsp, wsn = ws.ptr, ctypes.c_size_t(ws.nbytes)
+
+    def one():
+        for k, _ in names:
+            dst[k].copy_(host[k], non_blocking=True)
+        st = lib.eagle_build_tree(*rd.build_args, wsp, wsn, sptr)
+        st |= lib.eagle_tree_attention(*rd.attn_args, wsp, wsn, sptr)
+        st |= lib.eagle_tree_verify(*rd.verify_args, wsp, wsn, sptr)
+        if st:
+            raise RuntimeError(f"C-ABI call failed with status {st}")
+        out_h.copy_(outs["out_tokens"], non_blocking=True)
+        len_h.copy_(outs["out_len"], non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * steps / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def _traffic(attn_bytes: float):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was taken on the
+    current attention kernel source (else null)."""
+    path = os.path.join(ROOT, "profiles", "tree_attention_llama31_8b.md")
+    src = os.path.join(ROOT, "eagle_draft_tree_gb300", "csrc", "tree_attention.cu")
+    if not os.path.exists(path):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    fields = {}
+    for line in open(path):
+        if line.startswith("- ") and ":" in line:
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source sha256[:16]") != h:
+        return None
+    try:
+        return float(fields["dram bytes per launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------------- CPU oracle
+
+class OracleRound:
+    """The fp64 oracle on one round of a workload, split into timeable items: the build of every
+    sequence's tree, the verification of every sequence, and the L*B*Hkv attention units (one
+    unit = all query heads of one KV head, every node, the sequence's full context)."""
+
+    def __init__(self, wl, seed, nthreads):
+        import oracle
+
+        self.oracle = oracle
+        self.wl, self.nthreads = wl, nthreads
+        B, R, V, n = wl.batch, wl.rows, wl.vocab, wl.nodes
+        draft = datagen.draft_logits(B, R, V, seed)
+        self.draft_np, self.root_np = draft.numpy(), datagen.root_tokens(B, V, seed).numpy()
+        self.tree = oracle.build_tree(self.draft_np, self.root_np, wl.depth, wl.topk, wl.keep, nthreads=nthreads)
+        target = datagen.target_logits(draft, torch.from_numpy(self.tree["node_row"]),
+                                       datagen.noise_sigmas(wl, seed), seed)
+        self.tgt_np = target.numpy()
+        self.u_np = datagen.uniforms(B, n, seed).numpy()
+        one = wl.with_(layers=1, batch=1, heads_q=wl.group, heads_kv=1)
+        inp = datagen.attention_inputs(one, seed)
+        ctx = int(datagen.ctx_lens(wl, seed)[0])
+        inp["ctx_len"] = torch.tensor([ctx], dtype=torch.int32)
+        self.attn = [datagen.to_numpy(inp[k]) for k in ("q", "k_cache", "v_cache", "ctx_len", "k_tree", "v_tree")]
+        self.mask = self.tree["mask"][:1]
+        self.units = wl.layers * wl.batch * wl.heads_kv
+        # mean context of the workload over the one timed unit's context
+        self.ctx_scale = ((wl.ctx + wl.ctx_min) / 2 / ctx) if wl.ctx_min != wl.ctx else 1.0
+        self.times = {"build": [], "verify": [], "attn": []}
+
+    def item(self, i: int) -> None:
+        """Run and time item i of the rotation build, verify, attention unit, attention unit ..."""
+        kind = "build" if i % (self.units + 2) == 0 else ("verify" if i % (self.units + 2) == 1 else "attn")
+        wl, o = self.wl, self.oracle
+        t0 = time.perf_counter()
+        if kind == "build":
+            o.build_tree(self.draft_np, self.root_np, wl.depth, wl.topk, wl.keep, nthreads=self.nthreads)
+        elif kind == "verify":
+            o.tree_verify(self.tgt_np, self.draft_np, self.tree["tokens"], self.tree["parents"],
+                          self.tree["node_row"], self.u_np, wl.temperature, wl.depth + 1, nthreads=self.nthreads)
+        else:
+            o.tree_attention(*self.attn, self.mask, nthreads=self.nthreads)
+        self.times[kind].append(time.perf_counter() - t0)
+
+    def round_seconds(self) -> float:
+        t = {k: statistics.mean(v) for k, v in self.times.items()}
+        return t["build"] + t["verify"] + t["attn"] * self.units * self.ctx_scale
+
+    def summary(self) -> dict:
+        t = {k: statistics.mean(v) for k, v in self.times.items()}
+        return {"build_s": round(t["build"], 4), "verify_s": round(t["verify"], 4),
+                "attn_unit_s": round(t["attn"], 5), "attn_units_per_round": self.units,
+                "attn_units_timed": len(self.times["attn"]), "round_s": round(self.round_seconds(), 3)}
+
+
+def cpu_baseline(wl, seed, budget_s: float = 20.0) -> dict:
+    nthreads = os.cpu_count() or 1
+    orc = OracleRound(wl, seed, nthreads)
+    t0 = time.perf_counter()
+    i = 0
+    while i < 3 or (time.perf_counter() - t0 < budget_s and i < orc.units + 2):
+        orc.item(i)
+        i += 1
+    return {"value": 1.0 / orc.round_seconds(), "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": (f"one round's build and verify of every sequence plus {len(orc.times['attn'])} of "
+                       f"{orc.units} attention units (layer x KV head; all nodes and query heads of the group; "
+                       f"full context), attention extrapolated linearly in units; fp64 C oracle, OpenMP on "
+                       f"{nthreads} threads"),
+            "seconds": orc.summary()}
+
+
+def run_reference(args, rank, world) -> dict | None:
+    """Reference arm: the fp64 CPU oracle as it stands, on the host cores, same workload/metric.
+    Each step is one item of the round (build, verify, or one attention unit) in rotation; the
+    round time is the sum of the item means scaled by their counts per round."""
+    if rank != 0:
+        return None
+    wl = datagen.WORKLOADS[args.workload]
+    nthreads = os.cpu_count() or 1
+    orc = OracleRound(wl, args.seed, nthreads)
+    for i in range(args.warmup):
+        orc.item(i)
+    warm = {k: list(v) for k, v in orc.times.items()}
+    orc.times = {k: [] for k in orc.times}
+    t0 = time.perf_counter()
+    for i in range(args.warmup, args.warmup + args.steps):
+        orc.item(i)
+    wall = time.perf_counter() - t0
+    for k in orc.times:  # an item kind the timed steps did not reach keeps its warm-up timing
+        if not orc.times[k]:
+            orc.times[k] = warm[k]
+    value = 1.0 / orc.round_seconds()
+    sample = (f"each step one item of a round in rotation (build of all trees, verify of all sequences, or one of "
+              f"{orc.units} attention units); round time = item means x counts; fp64 C oracle, OpenMP {nthreads} "
+              f"threads")
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": _workload_desc(wl), "temperature": wl.temperature},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle", "sample": sample,
+                             "seconds": orc.summary()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama31_8b", choices=list(datagen.WORKLOADS))
+    ap.add_argument("--temperature", type=float, default=None)
+    ap.add_argument("--sets", type=int, default=4)
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the library has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    res = run_ours(args, rank, world, dev)
+    if rank == 0:
+        wl = datagen.WORKLOADS[args.workload]
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(wl, args.seed)
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+// capi.cu -- the extern "C" entry points of libeagle: argument validation on the host, then the
+// kernel launches of build_tree.cu, tree_attention.cu and verify.cu.  No entry point allocates
+// memory or synchronises the stream (except eagle_get_device_status, which exists to read back).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace eagle {
+
+size_t build_tree_workspace_bytes(const eagle_tree_cfg &c);
+eagle_status build_tree_launch(const eagle_tree_cfg &c, const float *draft, const int32_t *root, int32_t *tokens,
+                               int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask,
+                               float *node_logv, void *ws, cudaStream_t stream);
+size_t tree_attention_workspace_bytes(const eagle_attn_cfg &c);
+eagle_status tree_attention_launch(const eagle_attn_cfg &c, const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *ctx_len, const void *k_tree, const void *v_tree,
+                                   const uint64_t *mask, void *out, void *ws, cudaStream_t stream);
+size_t tree_verify_workspace_bytes(const eagle_verify_cfg &c);
+eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, const float *draft,
+                                const int32_t *tokens, const int32_t *parents, const int32_t *node_row,
+                                const float *uniforms, int32_t *out_tokens, int32_t *out_len, int32_t *out_path,
+                                float *out_ratio, void *ws, cudaStream_t stream);
+size_t verify_max_vocab();
+
+static thread_local int32_t t_launches = 0;
+void note_launch() { ++t_launches; }
+void reset_launches() { t_launches = 0; }
+
+namespace {
+
+bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+// 0 = ok, else an eagle status
+int check_tree(const eagle_tree_cfg *c) {
+    if (!c) return EAGLE_ERR_INVALID_ARG;
+    if (c->batch < 1 || c->vocab < 1 || c->depth < 1 || c->topk < 1 || c->keep < 1) return EAGLE_ERR_INVALID_ARG;
+    if (!(c->tree_temp > 0.f)) return EAGLE_ERR_INVALID_ARG;
+    if (c->topk > c->vocab) return EAGLE_ERR_INVALID_ARG;
+    if (c->topk > 16) return EAGLE_ERR_UNSUPPORTED;
+    if (c->depth > 64) return EAGLE_ERR_UNSUPPORTED;
+    const long P = long(c->topk) + long(c->depth - 1) * c->topk * c->topk;
+    if (c->keep > P) return EAGLE_ERR_INVALID_ARG;
+    if (P > 1024) return EAGLE_ERR_UNSUPPORTED;
+    if (c->keep + 1 > 64) return EAGLE_ERR_UNSUPPORTED;
+    return 0;
+}
+
+int check_attn(const eagle_attn_cfg *c) {
+    if (!c) return EAGLE_ERR_INVALID_ARG;
+    if (c->batch < 1 || c->layers < 1 || c->nodes < 1 || c->heads_q < 1 || c->heads_kv < 1 || c->head_dim < 1 ||
+        c->max_seq < 0)
+        return EAGLE_ERR_INVALID_ARG;
+    if (c->dtype != EAGLE_DTYPE_BF16 && c->dtype != EAGLE_DTYPE_F32) return EAGLE_ERR_INVALID_ARG;
+    if (!(c->scale >= 0.f)) return EAGLE_ERR_INVALID_ARG;
+    if (c->heads_q % c->heads_kv) return EAGLE_ERR_UNSUPPORTED;
+    if (c->head_dim != 64 && c->head_dim != 128) return EAGLE_ERR_UNSUPPORTED;
+    if (c->nodes > 64) return EAGLE_ERR_UNSUPPORTED;
+    const long rows = long(c->heads_q / c->heads_kv) * c->nodes;
+    const long grid = long(c->layers) * c->batch * c->heads_kv * ((rows + 63) / 64);
+    if (grid > 0x7fffffffL) return EAGLE_ERR_UNSUPPORTED;
+    return 0;
+}
+
+int check_verify(const eagle_verify_cfg *c) {
+    if (!c) return EAGLE_ERR_INVALID_ARG;
+    if (c->batch < 1 || c->vocab < 1 || c->depth < 1 || c->topk < 1 || c->keep < 1) return EAGLE_ERR_INVALID_ARG;
+    if (!(c->temperature >= 0.f)) return EAGLE_ERR_INVALID_ARG;
+    if (c->keep + 1 > 64) return EAGLE_ERR_UNSUPPORTED;
+    if (c->batch > 65535) return EAGLE_ERR_UNSUPPORTED;
+    if (size_t(c->vocab) > verify_max_vocab()) return EAGLE_ERR_UNSUPPORTED;
+    return 0;
+}
+
+}  // namespace
+}  // namespace eagle
+
+using namespace eagle;
+
+extern "C" {
+
+size_t eagle_build_tree_workspace_size(const eagle_tree_cfg *cfg) {
+    if (check_tree(cfg)) return 0;
+    return build_tree_workspace_bytes(*cfg);
+}
+
+eagle_status eagle_build_tree(const eagle_tree_cfg *cfg, const float *draft_logits, const int32_t *root_token,
+                              int32_t *tokens, int32_t *parents, int32_t *depths, int32_t *node_row,
+                              uint64_t *mask, float *node_logv, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    reset_launches();
+    if (int e = check_tree(cfg)) return e;
+    if (!draft_logits || !root_token || !tokens || !parents || !depths || !node_row || !mask || !ws)
+        return EAGLE_ERR_INVALID_ARG;
+    if (!aligned256(ws) || ws_bytes < build_tree_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
+    return build_tree_launch(*cfg, draft_logits, root_token, tokens, parents, depths, node_row, mask, node_logv, ws,
+                             stream);
+}
+
+size_t eagle_tree_attention_workspace_size(const eagle_attn_cfg *cfg) {
+    if (check_attn(cfg)) return 0;
+    return tree_attention_workspace_bytes(*cfg);
+}
+
+eagle_status eagle_tree_attention(const eagle_attn_cfg *cfg, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *ctx_len, const void *k_tree,
+                                  const void *v_tree, const uint64_t *mask, void *out, void *ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+    reset_launches();
+    if (int e = check_attn(cfg)) return e;
+    if (!q || !k_cache || !v_cache || !ctx_len || !k_tree || !v_tree || !mask || !out || !ws)
+        return EAGLE_ERR_INVALID_ARG;
+    if (!aligned256(ws) || ws_bytes < tree_attention_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
+    // 16-byte alignment of every K/V/Q/O row start (d elements of 2 or 4 bytes)
+    const uintptr_t any = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+                          reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(k_tree) |
+                          reinterpret_cast<uintptr_t>(v_tree) | reinterpret_cast<uintptr_t>(out);
+    if (any & 15u) return EAGLE_ERR_INVALID_ARG;
+    return tree_attention_launch(*cfg, q, k_cache, v_cache, ctx_len, k_tree, v_tree, mask, out, ws, stream);
+}
+
+size_t eagle_tree_verify_workspace_size(const eagle_verify_cfg *cfg) {
+    if (check_verify(cfg)) return 0;
+    return tree_verify_workspace_bytes(*cfg);
+}
+
+eagle_status eagle_tree_verify(const eagle_verify_cfg *cfg, const float *target_logits, const float *draft_logits,
+                               const int32_t *tokens, const int32_t *parents, const int32_t *node_row,
+                               const float *uniforms, int32_t *out_tokens, int32_t *out_len, int32_t *out_path,
+                               float *out_ratio, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    reset_launches();
+    if (int e = check_verify(cfg)) return e;
+    if (!target_logits || !draft_logits || !tokens || !parents || !node_row || !uniforms || !out_tokens ||
+        !out_len || !out_path || !ws)
+        return EAGLE_ERR_INVALID_ARG;
+    if (!aligned256(ws) || ws_bytes < tree_verify_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
+    return tree_verify_launch(*cfg, target_logits, draft_logits, tokens, parents, node_row, uniforms, out_tokens,
+                              out_len, out_path, out_ratio, ws, stream);
+}
+
+eagle_status eagle_workspace_init(void *ws, size_t bytes, cudaStream_t stream) {
+    if (!ws || bytes < kWsHeader) return EAGLE_ERR_INVALID_ARG;
+    return cudaMemsetAsync(ws, 0, bytes, stream) == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
+}
+
+eagle_status eagle_get_device_status(void *ws, cudaStream_t stream, int32_t *out) {
+    if (!ws || !out) return EAGLE_ERR_INVALID_ARG;
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return EAGLE_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, sizeof v, stream) != cudaSuccess) return EAGLE_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return EAGLE_ERR_CUDA;
+    *out = v;
+    return EAGLE_OK;
+}
+
+const char *eagle_status_string(eagle_status s) {
+    switch (s) {
+        case EAGLE_OK: return "ok";
+        case EAGLE_ERR_INVALID_ARG: return "invalid argument";
+        case EAGLE_ERR_UNSUPPORTED: return "unsupported size";
+        case EAGLE_ERR_CUDA: return "CUDA launch error";
+        case EAGLE_ERR_TIMEOUT: return "device wait timed out";
+        case EAGLE_ERR_DEVICE_INPUT: return "bad device-side input";
+        default: return "unknown status";
+    }
+}
+
+int32_t eagle_last_launch_count(void) { return t_launches; }
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+"""The C-ABI library builds, loads without a GPU, exports every symbol include/eagle.h declares,
+and rejects bad arguments on the host before touching the device (no compute call here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import eagle_draft_tree_gb300 as eg
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "eagle.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(eagle_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = eg.load()
+    names = declared_functions()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), name
+    # the binding knows every declared symbol's signature
+    assert set(names) == set(eg._SIGS)
+
+
+def test_status_strings():
+    lib = eg.load()
+    for s in range(6):
+        assert lib.eagle_status_string(s).decode()
+    assert lib.eagle_status_string(99).decode() == "unknown status"
+
+
+def _tree(**kw):
+    base = dict(batch=1, vocab=1000, depth=3, topk=4, keep=10, tree_temp=1.0)
+    base.update(kw)
+    return eg.TreeCfg(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), None),
+    (dict(batch=0), eg.EAGLE_ERR_INVALID_ARG),
+    (dict(topk=17), eg.EAGLE_ERR_UNSUPPORTED),
+    (dict(depth=8, topk=10, keep=64), eg.EAGLE_ERR_UNSUPPORTED),
+    (dict(keep=1000), eg.EAGLE_ERR_INVALID_ARG),
+    (dict(tree_temp=0.0), eg.EAGLE_ERR_INVALID_ARG),
+    (dict(topk=5, vocab=4), eg.EAGLE_ERR_INVALID_ARG),
+    (dict(depth=40, topk=16, keep=60), eg.EAGLE_ERR_UNSUPPORTED),
+])
+def test_build_tree_host_validation(kw, code):
+    lib = eg.load()
+    cfg = _tree(**kw)
+    size = lib.eagle_build_tree_workspace_size(ctypes.byref(cfg))
+    if code is None:
+        assert size >= 256
+        # null pointers are caught before any launch
+        st = lib.eagle_build_tree(ctypes.byref(cfg), None, None, None, None, None, None, None, None, None, 0, None)
+        assert st == eg.EAGLE_ERR_INVALID_ARG
+    else:
+        assert size == 0
+        st = lib.eagle_build_tree(ctypes.byref(cfg), *([None] * 9), 0, None)
+        assert st == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), None),
+    (dict(heads_q=6, heads_kv=4), eg.EAGLE_ERR_UNSUPPORTED),
+    (dict(head_dim=96), eg.EAGLE_ERR_UNSUPPORTED),
+    (dict(nodes=65), eg.EAGLE_ERR_UNSUPPORTED),
+    (dict(dtype=7), eg.EAGLE_ERR_INVALID_ARG),
+    (dict(max_seq=-1), eg.EAGLE_ERR_INVALID_ARG),
+])
+def test_attention_host_validation(kw, code):
+    lib = eg.load()
+    base = dict(batch=1, layers=2, nodes=11, heads_q=4, heads_kv=2, head_dim=64, max_seq=128, dtype=1, scale=0.0)
+    base.update(kw)
+    cfg = eg.AttnCfg(**base)
+    size = lib.eagle_tree_attention_workspace_size(ctypes.byref(cfg))
+    st = lib.eagle_tree_attention(ctypes.byref(cfg), *([None] * 9), 0, None)
+    if code is None:
+        assert size >= 256 and st == eg.EAGLE_ERR_INVALID_ARG
+    else:
+        assert size == 0 and st == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), None),
+    (dict(temperature=-1.0), eg.EAGLE_ERR_INVALID_ARG),
+    (dict(keep=70), eg.EAGLE_ERR_UNSUPPORTED),
+    (dict(vocab=10_000_000), eg.EAGLE_ERR_UNSUPPORTED),
+])
+def test_verify_host_validation(kw, code):
+    lib = eg.load()
+    base = dict(batch=2, vocab=1000, depth=3, topk=4, keep=10, temperature=1.0)
+    base.update(kw)
+    cfg = eg.VerifyCfg(**base)
+    size = lib.eagle_tree_verify_workspace_size(ctypes.byref(cfg))
+    st = lib.eagle_tree_verify(ctypes.byref(cfg), *([None] * 11), 0, None)
+    if code is None:
+        assert size >= 256 and st == eg.EAGLE_ERR_INVALID_ARG
+    else:
+        assert size == 0 and st == code
+
+
+def test_workspace_too_small_rejected():
+    lib = eg.load()
+    cfg = _tree()
+    fake = ctypes.c_void_p(256 * 1024)  # never dereferenced: the size check fails first
+    st = lib.eagle_build_tree(ctypes.byref(cfg), fake, fake, fake, fake, fake, fake, fake, None, fake, 16, None)
+    assert st == eg.EAGLE_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros((1, 9, 1000), dtype=torch.float32)
+    r = torch.zeros((1,), dtype=torch.int32)
+    with pytest.raises((ValueError, RuntimeError, AssertionError)):
+        eg.build_tree(x, r, depth=3, topk=4, keep=10, ws=object())

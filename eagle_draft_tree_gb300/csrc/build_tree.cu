@@ -219,7 +219,9 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
-        const double lse = double(M) * a.inv_t + log(S);
+        double lse = 0.0;
+        if (lane == 0) lse = double(M) * a.inv_t + log(S);
+        lse = __shfl_sync(0xffffffffu, lse, 0);
         // top-k of the union of the split lists: pass j takes the largest key below pass j-1's
         const int ncand = a.splits * KMAX;
         const uint64_t *cand = a.part_keys + base * KMAX;

@@ -53,8 +53,9 @@ struct VerifyArgs {
     int32_t *out_tokens, *out_len, *out_path;
     int32_t *status;
     int B, n, V, R, D, slice;
-    float inv_t;  // 1/T (T > 0)
-    float c;      // log2(e)/T
+    float inv_t;    // 1/T (T > 0)
+    double inv_td;  // 1/T in double (for the gathered per-child probabilities)
+    float c;        // log2(e)/T
     int greedy;
 };
 
@@ -94,7 +95,6 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kPrepThreads)
     verify_prep_kernel(VerifyArgs a) {
     extern __shared__ __align__(16) float sm[];  // [slice] target, then [slice] draft
     __shared__ float s_scratch[kPrepThreads / 32];
-    __shared__ float s_scratch2[kPrepThreads / 32];
     __shared__ unsigned long long s_xchg[2][4];  // per-pass partials exchanged across the cluster (bit patterns)
     __shared__ int s_kids[kMaxKids];
     __shared__ int s_nk;
@@ -230,19 +230,30 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kPrepThreads)
         const unsigned long long mine[4] = {dbl(M0), dbl(S0), dbl(M1), dbl(S1)};
         exchange(mine, 4);
     }
-    // row-wide max and log of the scaled sum, identical in every CTA of the cluster
-    float Mp = -INFINITY, Mq = -INFINITY;
-    for (int r = 0; r < kCl; ++r) {
-        Mp = fmaxf(Mp, float(all(r, 0)));
-        Mq = fmaxf(Mq, float(all(r, 2)));
+    // row-wide max and log of the scaled sum (one thread computes, every CTA of the cluster gets
+    // the same values because it reduces the same partials in the same order)
+    __shared__ float s_M[2];
+    __shared__ double s_lnS[2];
+    if (tid == 0) {
+        float Mp = -INFINITY, Mq = -INFINITY;
+        for (int r = 0; r < kCl; ++r) {
+            Mp = fmaxf(Mp, float(all(r, 0)));
+            Mq = fmaxf(Mq, float(all(r, 2)));
+        }
+        double Sp = 0.0, Sq = 0.0;
+        for (int r = 0; r < kCl; ++r) {
+            const float m0 = float(all(r, 0)), m1 = float(all(r, 2));
+            if (m0 != -INFINITY) Sp += all(r, 1) * double(exp2f((m0 - Mp) * c));
+            if (m1 != -INFINITY) Sq += all(r, 3) * double(exp2f((m1 - Mq) * c));
+        }
+        s_M[0] = Mp;
+        s_M[1] = Mq;
+        s_lnS[0] = log(Sp);
+        s_lnS[1] = has_q ? log(Sq) : 0.0;
     }
-    double Sp = 0.0, Sq = 0.0;
-    for (int r = 0; r < kCl; ++r) {
-        const float m0 = float(all(r, 0)), m1 = float(all(r, 2));
-        if (m0 != -INFINITY) Sp += all(r, 1) * double(exp2f((m0 - Mp) * c));
-        if (m1 != -INFINITY) Sq += all(r, 3) * double(exp2f((m1 - Mq) * c));
-    }
-    const double lnSp = log(Sp), lnSq = has_q ? log(Sq) : 0.0;
+    __syncthreads();
+    const float Mp = s_M[0], Mq = s_M[1];
+    const double lnSp = s_lnS[0], lnSq = s_lnS[1];
     const float lp_hi = float(lnSp), lp_lo = float(lnSp - double(lp_hi));
     const float lq_hi = float(lnSq), lq_lo = float(lnSq - double(lq_hi));
     const float inv_t = a.inv_t;
@@ -262,14 +273,15 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kPrepThreads)
     for (int j = 0; j < J; ++j) {
         const int child = s_kids[j];
         if (tid == 0 && rank == 0) {
+            // the accept ratio of child j in double: p0(t) - c_j q(t) cancels when the two are close
             const int t = tok[child];
             float r = NAN;
             if (has_q && t >= 0 && t < V) {
-                const float p0 = p_of(__ldg(xrow + t));
-                const float q0 = q_of(__ldg(yrow + t));
-                const float num = j == 0 ? p0 : fmaxf(fmaf(-float(cj), q0, p0), 0.f);
-                const float den = float(Sj) * q0;
-                r = den > 0.f ? num / den : INFINITY;
+                const double p0 = exp((double(__ldg(xrow + t)) - double(Mp)) * a.inv_td - lnSp);
+                const double q0 = exp((double(__ldg(yrow + t)) - double(Mq)) * a.inv_td - lnSq);
+                const double num = j == 0 ? p0 : fmax(p0 - cj * q0, 0.0);
+                const double den = Sj * q0;
+                r = den > 0.0 ? float(num / den) : INFINITY;
             }
             a.ratio[size_t(b) * n + child] = r;
             if (a.out_ratio) a.out_ratio[size_t(b) * n + child] = r;
@@ -284,7 +296,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kPrepThreads)
         const unsigned long long mine[1] = {dbl(double(part))};
         exchange(mine, 1);
         double Sn = 0.0;
-        for (int r = 0; r < kCl; ++r) Sn += all(r, 0);
+        for (int r = 0; r < kCl; ++r) Sn += all(r, 0);  // few double adds, same order everywhere
         if (Sn > 0.0) {  // otherwise the adjusted distribution keeps p_j
             cj = cn;
             Sj = Sn;
@@ -480,6 +492,7 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
     a.slice = slice;
     a.greedy = c.temperature <= 0.f;
     a.inv_t = a.greedy ? 1.f : 1.f / c.temperature;
+    a.inv_td = a.greedy ? 1.0 : 1.0 / double(c.temperature);
     a.c = kLog2e * a.inv_t;
     const size_t smem = a.greedy ? 0 : size_t(2) * slice * sizeof(float);
     static size_t attr = 0;

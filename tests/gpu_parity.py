@@ -5,8 +5,10 @@ Tolerances (GPU vs fp64 oracle):
   * tree indices, masks, committed tokens/paths: bit-exact.  A build difference is excused only
     when the oracle's smallest relative key gap at a selection boundary is < 1e-6; a verify
     difference only when the oracle's smallest |u - decision value| on its walk is < 1e-5.
-  * node_logv: 1e-5 relative.  out_ratio: 1e-5 relative + 1e-6 absolute (ratios that come out of a
-    cancellation p0 - c q are tiny and carry an absolute error).
+  * node_logv: 1e-5 relative.  out_ratio: 1e-5 relative to max(1, ratio).  The ratio is compared
+    with a uniform, so its natural error scale is absolute below 1 (the same 1e-5 that excuses a
+    decision); after j rejections it is (p0 - c_j q)/(S_j q), and the fp32 error of c_j (~1e-7) is
+    amplified by the cancellation p0 - c_j q on small ratios.
   * attention: max-abs 2e-2 (bf16 K/V) or 1e-4 (fp32).
 """
 from __future__ import annotations
@@ -61,7 +63,7 @@ def oracle_tree_tensors(o: dict, device) -> dict:
     return t
 
 
-def compare_verify(g: dict, o: dict, log: list | None = None, ratio_rtol=1e-5, ratio_atol=1e-6):
+def compare_verify(g: dict, o: dict, log: list | None = None, ratio_rtol=1e-5, ratio_atol=1e-5):
     excused = []
     B = o["out_len"].shape[0]
     for b in range(B):

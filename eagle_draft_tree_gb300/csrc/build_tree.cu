@@ -7,40 +7,34 @@
 // "Tree Attention Mask" (flattened sequence, ancestors-only visibility).
 //
 // Two kernels:
-//   row_topk_kernel   one HBM pass over every draft row: online log-sum-exp of x/T and the row's
-//                     top-k logits (value desc, token asc).  A row is split across several CTAs
-//                     so that the grid covers the GPU even at batch 1; each CTA leaves a partial
-//                     (max, scaled sum, its top-KMAX keys) in the workspace.
-//   tree_select_kernel one CTA per sequence: merges the partials, computes the log-confidences
-//                     in fp64, runs the per-depth frontier selection, the global rerank (bitonic
-//                     sort of the <= 1024-entry pool) and writes the flattened tree.
+//   row_topk_kernel    one HBM pass over every draft row.  A row is cut into `splits` slices
+//                      handled by the CTAs of one thread-block cluster; each CTA keeps an online
+//                      log-sum-exp of x/T and a top-KMAX list (per-warp sorted lists that only
+//                      see values above a block-shared threshold), then rank 0 merges the
+//                      cluster's lists and sums through distributed shared memory and writes the
+//                      row's k children (token, fp64 log-confidence).
+//   tree_select_kernel one CTA per sequence: per-depth frontier selection (rank of a 64-bit
+//                      composite key), expansion, the global rerank (8-pass radix select of the
+//                      m-th largest key over the <= 1024-entry pool), flatten, masks.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "common.cuh"
 
+namespace cg = cooperative_groups;
+
 namespace eagle {
 
 namespace {
 
-constexpr int kRowThreads = 256;
-constexpr int kSelThreads = 512;
+constexpr int kRowThreads = 512;
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kRowVals = 16;  // values per thread per batch (4 float4 in registers)
+constexpr int kSelThreads = 256;
 constexpr int kMaxPool = 1024;
-
-template <int KMAX>
-__device__ __forceinline__ void list_insert(uint64_t (&list)[KMAX], uint64_t key) {
-    if (key <= list[KMAX - 1]) return;
-    list[KMAX - 1] = key;
-#pragma unroll
-    for (int j = KMAX - 1; j > 0; --j) {
-        if (list[j] > list[j - 1]) {
-            uint64_t t = list[j];
-            list[j] = list[j - 1];
-            list[j - 1] = t;
-        }
-    }
-}
+constexpr int kMaxSplits = 8;  // portable cluster size
 
 // Merge (m_a, s_a) and (m_b, s_b) where s = sum 2^((x - m) c).
 __device__ __forceinline__ void ms_merge(float &m, float &s, float mo, float so, float c) {
@@ -52,216 +46,273 @@ __device__ __forceinline__ void ms_merge(float &m, float &s, float mo, float so,
     s = a + b;
 }
 
-template <int KMAX>
-__global__ void __launch_bounds__(kRowThreads) row_topk_kernel(const float *__restrict__ x, int V, int R, int splits,
-                                                                 int chunk, float c, uint64_t *__restrict__ part_keys,
-                                                                 float2 *__restrict__ part_ms) {
-    __shared__ uint64_t s_lists[kRowThreads][KMAX + 1];  // +1 breaks bank alignment
-    __shared__ uint64_t s_warp[kRowThreads / 32][KMAX];
-    __shared__ float2 s_ms[kRowThreads / 32];
+struct RowArgs {
+    const float *x;     // [B][R][V]
+    int32_t *row_tok;   // [B][R][k]  children tokens
+    double *row_lc;     // [B][R][k]  children log-confidences
+    int V, R, k, chunk;
+    float c;            // log2(e) / tree_temp
+    double inv_t;       // 1 / tree_temp
+};
 
-    const int split = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x;
-    const float *row = x + (size_t(b) * R + r) * size_t(V);
-    const int lo = split * chunk;
-    const int hi = min(V, lo + chunk);
+// KMAX-th largest key of the warp's 32 lane keys (bitonic sort across lanes, descending).
+template <int KMAX>
+__device__ __forceinline__ uint64_t warp_kth_key(uint64_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const uint64_t o = shfl_xor_u64(v, stride);
+            const bool up = (lane & size) == 0;         // this pair sorts descending when up
+            const bool lower = (lane & stride) == 0;    // this lane holds the earlier position
+            const bool keep_max = (up == lower);
+            v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+        }
+    }
+    return __shfl_sync(0xffffffffu, v, KMAX - 1);
+}
+
+// Fold `count` descending 16-key lists (zero padded) stored in buf[0][0..count) into buf[?][0]
+// with a tree of warp bitonic merges; returns the buffer index holding the result.  Called by the
+// whole CTA (block barriers inside).
+__device__ __forceinline__ int tree_merge16(uint64_t (*buf)[kRowWarps][16], int count) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int cur = 0;
+    while (count > 1) {
+        const int pairs = count >> 1;
+        if (warp < pairs) {
+            const uint64_t v = lane < 16 ? buf[cur][2 * warp][lane] : buf[cur][2 * warp + 1][31 - lane];
+            const uint64_t w = warp_bitonic_merge32(v);
+            if (lane < 16) buf[cur ^ 1][warp][lane] = w;
+        } else if (warp == pairs && (count & 1)) {
+            if (lane < 16) buf[cur ^ 1][warp][lane] = buf[cur][2 * warp][lane];  // odd list carried over
+        }
+        __syncthreads();
+        count = pairs + (count & 1);
+        cur ^= 1;
+    }
+    return cur;
+}
+
+__global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
+    __shared__ uint64_t s_lists[2][kRowWarps][16];
+    __shared__ float2 s_ms[kRowWarps];
+    __shared__ uint64_t s_blk[16];  // this CTA's list, read by the cluster's rank 0
+    __shared__ float2 s_blkms;
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int split = int(cluster.block_rank());
+    const int splits = int(cluster.num_blocks());
+    const int r = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *row = a.x + (size_t(b) * a.R + r) * size_t(a.V);
+    const int lo = split * a.chunk;
+    const int hi = min(a.V, lo + a.chunk);
+    const float c = a.c;
+    const bool vec = ((a.V & 3) == 0) && ((reinterpret_cast<uintptr_t>(row) & 15) == 0) && ((lo & 3) == 0);
 
     float m = -INFINITY, s = 0.f;
-    uint64_t list[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) list[j] = 0;
+    WarpTopK<16> top;
+    uint64_t seed = 0;  // per-warp lower bound of the warp's top-16, from its first batch
+    bool seeded = false;
 
-    auto consume = [&](float v, int t) {
-        if (v > m) {
-            s = s * exp2f((m - v) * c) + 1.f;
-            m = v;
-        } else {
-            s += exp2f((v - m) * c);
+    // One batch: kRowVals values per thread.  Statistics in registers, then the top-16 offer:
+    // a value can only be in the warp's top-16 if its key reaches both the warp's current 16th
+    // key and the seed (the 16th largest lane maximum of the first batch: 16 distinct values at
+    // or above it are known).
+    auto batch = [&](const float (&x)[kRowVals], const int (&tk)[kRowVals]) {
+        float mx = x[0];
+        int tmx = tk[0];
+#pragma unroll
+        for (int j = 1; j < kRowVals; ++j)
+            if (x[j] > mx) {
+                mx = x[j];
+                tmx = tk[j];
+            }
+        if (mx > m) {
+            s = (m == -INFINITY) ? 0.f : s * fast_exp2((m - mx) * c);
+            m = mx;
         }
-        list_insert<KMAX>(list, topk_key(v, uint32_t(t)));
-    };
-
-    const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(row) & 15) == 0);
-    if (vec) {
-        const float4 *row4 = reinterpret_cast<const float4 *>(row);
-        const int lo4 = lo >> 2, hi4 = hi >> 2;
-        int i = lo4 + tid;
-        for (; i + 3 * kRowThreads < hi4; i += 4 * kRowThreads) {
-            float4 a0 = __ldg(row4 + i);
-            float4 a1 = __ldg(row4 + i + kRowThreads);
-            float4 a2 = __ldg(row4 + i + 2 * kRowThreads);
-            float4 a3 = __ldg(row4 + i + 3 * kRowThreads);
-            const float4 av[4] = {a0, a1, a2, a3};
+        if (m != -INFINITY) {
+            const float mc = m * c;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                int t = 4 * (i + u * kRowThreads);
-                consume(av[u].x, t);
-                consume(av[u].y, t + 1);
-                consume(av[u].z, t + 2);
-                consume(av[u].w, t + 3);
+            for (int j = 0; j < kRowVals; ++j) s += fast_exp2(fmaf(x[j], c, -mc));
+        }
+        if (!seeded) {
+            seed = warp_kth_key<16>(mx == -INFINITY ? 0ull : topk_key(mx, uint32_t(tmx)));
+            seeded = true;
+        }
+        const uint64_t bound = seed > top.thr ? seed : top.thr;
+        const float bval = bound == 0 ? -INFINITY : topk_key_value(bound);
+#pragma unroll
+        for (int j = 0; j < kRowVals; ++j) {
+            const bool cand = x[j] >= bval && x[j] != -INFINITY;
+            if (__any_sync(0xffffffffu, cand)) {
+                const uint64_t key = cand ? topk_key(x[j], uint32_t(tk[j])) : 0ull;
+                top.insert(key >= bound ? key : 0ull);
             }
         }
-        for (; i < hi4; i += kRowThreads) {
-            float4 a = __ldg(row4 + i);
-            int t = 4 * i;
-            consume(a.x, t);
-            consume(a.y, t + 1);
-            consume(a.z, t + 2);
-            consume(a.w, t + 3);
+    };
+
+    constexpr int kBatch = kRowThreads * kRowVals;
+    const int nb = (hi - lo + kBatch - 1) / kBatch;  // same for every thread of the CTA
+    if (vec) {
+        const float4 *row4 = reinterpret_cast<const float4 *>(row);
+        float4 nxt[kRowVals / 4];
+        auto load = [&](int bi, float4 (&dst)[kRowVals / 4]) {
+#pragma unroll
+            for (int j = 0; j < kRowVals / 4; ++j) {
+                const int i4 = ((lo + bi * kBatch) >> 2) + tid + j * kRowThreads;
+                dst[j] = 4 * i4 < hi ? __ldg(row4 + i4) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+        };
+        if (nb > 0) load(0, nxt);
+        for (int bi = 0; bi < nb; ++bi) {
+            float x[kRowVals];
+            int tk[kRowVals];
+#pragma unroll
+            for (int j = 0; j < kRowVals / 4; ++j) {
+                const int i4 = ((lo + bi * kBatch) >> 2) + tid + j * kRowThreads;
+                x[4 * j] = nxt[j].x;
+                x[4 * j + 1] = nxt[j].y;
+                x[4 * j + 2] = nxt[j].z;
+                x[4 * j + 3] = nxt[j].w;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) tk[4 * j + e] = 4 * i4 + e;
+            }
+            if (bi + 1 < nb) load(bi + 1, nxt);  // next batch in flight while this one is consumed
+            batch(x, tk);
         }
     } else {
-        for (int t = lo + tid; t < hi; t += kRowThreads) consume(__ldg(row + t), t);
+        for (int bi = 0; bi < nb; ++bi) {
+            float x[kRowVals];
+            int tk[kRowVals];
+#pragma unroll
+            for (int j = 0; j < kRowVals; ++j) {
+                const int t = lo + bi * kBatch + tid + j * kRowThreads;
+                x[j] = t < hi ? __ldg(row + t) : -INFINITY;
+                tk[j] = t;
+            }
+            batch(x, tk);
+        }
     }
 
-    // (max, sum) across the block
+    // block: (max, sum) and the merged list
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         float mo = __shfl_xor_sync(0xffffffffu, m, off);
         float so = __shfl_xor_sync(0xffffffffu, s, off);
         ms_merge(m, s, mo, so, c);
     }
-    const int warp = tid >> 5, lane = tid & 31;
     if (lane == 0) s_ms[warp] = make_float2(m, s);
-
-    // top-KMAX across the block: lanes -> warp lists -> block list
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) s_lists[tid][j] = list[j];
-    __syncwarp();
-    {
-        int ptr = 0;
-        for (int j = 0; j < KMAX; ++j) {
-            uint64_t mine = ptr < KMAX ? s_lists[tid][ptr] : 0;
-            uint64_t best = warp_max_u64(mine);
-            if (best != 0 && mine == best) ++ptr;
-            if (lane == 0) s_warp[warp][j] = best;
-        }
-    }
+    if (lane < 16) s_lists[0][warp][lane] = top.key;
     __syncthreads();
+    const int cur = tree_merge16(s_lists, kRowWarps);
+    if (tid < 16) s_blk[tid] = s_lists[cur][0][tid];
     if (warp == 0) {
-        float mm = lane < kRowThreads / 32 ? s_ms[lane].x : -INFINITY;
-        float ss = lane < kRowThreads / 32 ? s_ms[lane].y : 0.f;
+        float mm = lane < kRowWarps ? s_ms[lane].x : -INFINITY;
+        float ss = lane < kRowWarps ? s_ms[lane].y : 0.f;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             float mo = __shfl_xor_sync(0xffffffffu, mm, off);
             float so = __shfl_xor_sync(0xffffffffu, ss, off);
             ms_merge(mm, ss, mo, so, c);
         }
-        const size_t slot = (size_t(b) * R + r) * splits + split;
-        int ptr = 0;
-        for (int j = 0; j < KMAX; ++j) {
-            uint64_t mine = (lane < kRowThreads / 32 && ptr < KMAX) ? s_warp[lane][ptr] : 0;
-            uint64_t best = warp_max_u64(mine);
-            if (best != 0 && mine == best) ++ptr;
-            if (lane == 0) part_keys[slot * KMAX + j] = best;
-        }
-        if (lane == 0) part_ms[slot] = make_float2(mm, ss);
+        if (lane == 0) s_blkms = make_float2(mm, ss);
     }
+    cluster.sync();
+
+    // cluster rank 0: merge the slices' lists and sums, write the row's children
+    if (split == 0) {
+        for (int t = tid; t < splits * 16; t += kRowThreads)
+            s_lists[0][t / 16][t % 16] = cluster.map_shared_rank(&s_blk[0], t / 16)[t % 16];
+        __syncthreads();
+        const int cur2 = tree_merge16(s_lists, splits);
+        if (warp == 0) {
+            float2 ms = make_float2(-INFINITY, 0.f);
+            if (lane < splits) ms = *cluster.map_shared_rank(&s_blkms, lane);
+            float M = ms.x;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+            double S = ms.x == -INFINITY ? 0.0 : double(ms.y) * double(exp2f((ms.x - M) * c));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
+            double lse = 0.0;
+            if (lane == 0) lse = double(M) * a.inv_t + log(S);
+            lse = __shfl_sync(0xffffffffu, lse, 0);
+            if (lane < a.k) {
+                const size_t o = (size_t(b) * a.R + r) * a.k + lane;
+                const uint64_t key = s_lists[cur2][0][lane];
+                a.row_tok[o] = int32_t(topk_key_token(key));
+                a.row_lc[o] = double(topk_key_value(key)) * a.inv_t - lse;
+            }
+        }
+    }
+    cluster.sync();  // peers' shared memory stays alive until rank 0 has read it
 }
 
-struct PoolEntry {
-    double logv;
-    int idx;  // creation index (pool position)
-    int pad;
-};
-
-// a comes strictly before b in (logv desc, creation asc)
-__device__ __forceinline__ bool entry_before(const PoolEntry &a, const PoolEntry &b) {
-    return a.logv > b.logv || (a.logv == b.logv && a.idx < b.idx);
+// Composite selection key: larger = better.  High 54 bits: orderable log V (the low 10 bits of
+// the double dropped); low 10 bits: 1023 - creation index (earlier creation wins a tie).
+__device__ __forceinline__ uint64_t pool_key(double logv, int creation) {
+    return (double_order_key(logv) & ~uint64_t(1023)) | uint64_t(1023 - creation);
 }
 
 struct SelectArgs {
-    const uint64_t *part_keys;
-    const float2 *part_ms;
+    const int32_t *row_tok;
+    const double *row_lc;
     const int32_t *root_token;
     int32_t *tokens, *parents, *depths, *node_row;
     uint64_t *mask;
     float *node_logv;
     int32_t *status;
-    int V, D, k, m, R, splits;
-    float c;        // log2(e) / tree_temp
-    double inv_t;   // 1 / tree_temp
+    int V, D, k, m, R;
 };
 
-template <int KMAX>
 __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ double s_lc[kMaxPool];     // [R*k] child log-confidences (R*k = P <= 1024)
+    __shared__ int s_ctok[kMaxPool];      // [R*k] child tokens
+    __shared__ double s_logv[kMaxPool];   // pool: log V
+    __shared__ uint64_t s_key[kMaxPool];  // pool: composite key
+    __shared__ int s_par[kMaxPool];       // pool: parent pool index (-1: the root)
+    __shared__ int s_row[kMaxPool];       // pool: draft row that expanded it, or -1
+    __shared__ int s_flat[kMaxPool];      // pool: flattened node index, or -1
+    __shared__ int s_ptok[kMaxPool];      // pool: token
+    __shared__ unsigned char s_dep[kMaxPool];
+    __shared__ int s_slot[16];
+    __shared__ int s_hist[256];
+    __shared__ uint64_t s_prefix;
+    __shared__ int s_remaining;
+    __shared__ int s_wsum[kMaxPool / 32];
+
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = a.k, R = a.R, D = a.D, m = a.m;
-    const int P = k + (D - 1) * k * k;
-    int NP = 1;
-    while (NP < P) NP <<= 1;
 
-    // shared layout
-    double *s_lc = reinterpret_cast<double *>(smem_raw);                 // [R*k] child log-confidence
-    PoolEntry *s_sort = reinterpret_cast<PoolEntry *>(s_lc + kMaxPool);  // [NP <= kMaxPool]
-    double *s_logv = reinterpret_cast<double *>(s_sort + kMaxPool);      // [P]
-    int *s_tok = reinterpret_cast<int *>(s_logv + kMaxPool);             // [R*k] child token
-    int *s_ptok = s_tok + kMaxPool;                                      // [P] token
-    int *s_par = s_ptok + kMaxPool;                                      // [P] parent pool idx
-    int *s_row = s_par + kMaxPool;                                       // [P] expanding row or -1
-    int *s_dep = s_row + kMaxPool;                                       // [P] depth
-    int *s_flat = s_dep + kMaxPool;                                      // [P] flattened index or -1
-    int *s_slot = s_flat + kMaxPool;                                     // [k] frontier slot -> pool idx
-    int *s_wsum = s_slot + 16;                                           // [32] scan scratch
-
-    // 1. merge the row partials: lse in fp64 and the top-k children
-    for (int r = warp; r < R; r += kSelThreads / 32) {
-        const size_t base = (size_t(b) * R + r) * a.splits;
-        float M = -INFINITY;
-        for (int s = lane; s < a.splits; s += 32) M = fmaxf(M, a.part_ms[base + s].x);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        double S = 0.0;
-        for (int s = lane; s < a.splits; s += 32) {
-            float2 ms = a.part_ms[base + s];
-            if (ms.x != -INFINITY) S += double(ms.y) * double(exp2f((ms.x - M) * a.c));
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
-        double lse = 0.0;
-        if (lane == 0) lse = double(M) * a.inv_t + log(S);
-        lse = __shfl_sync(0xffffffffu, lse, 0);
-        // top-k of the union of the split lists: pass j takes the largest key below pass j-1's
-        const int ncand = a.splits * KMAX;
-        const uint64_t *cand = a.part_keys + base * KMAX;
-        uint64_t prev = ~uint64_t(0);
-        for (int j = 0; j < k; ++j) {
-            uint64_t best = 0;
-            for (int i = lane; i < ncand; i += 32) {
-                uint64_t key = cand[i];
-                if (key < prev && key > best) best = key;
-            }
-            best = warp_max_u64(best);
-            prev = best;
-            if (lane == 0) {
-                s_tok[r * k + j] = int(topk_key_token(best));
-                s_lc[r * k + j] = double(topk_key_value(best)) * a.inv_t - lse;
-            }
-        }
+    // the rows' children (written by row_topk_kernel)
+    for (int i = tid; i < R * k; i += kSelThreads) {
+        s_lc[i] = a.row_lc[size_t(b) * R * k + i];
+        s_ctok[i] = a.row_tok[size_t(b) * R * k + i];
     }
     __syncthreads();
-
-    // 2. depth 1: the root's children (row 0)
+    // depth 1: the root's children (row 0)
     for (int i = tid; i < k; i += kSelThreads) {
         s_logv[i] = s_lc[i];
-        s_ptok[i] = s_tok[i];
+        s_key[i] = pool_key(s_lc[i], i);
+        s_ptok[i] = s_ctok[i];
         s_par[i] = -1;
         s_row[i] = -1;
         s_dep[i] = 1;
     }
     __syncthreads();
 
-    // 3. depths 2..D: expand the top-k frontier of the previous depth
+    // depths 2..D: the k best nodes of the previous depth are expanded; frontier slot = rank
     int lb = 0, cnt = k, np = k;
     for (int f = 1; f <= D - 1; ++f) {
         for (int e = lb + tid; e < lb + cnt; e += kSelThreads) {
-            const double v = s_logv[e];
+            const uint64_t v = s_key[e];
             int rank = 0;
-            for (int o = lb; o < lb + cnt; ++o) {
-                const double w = s_logv[o];
-                rank += (w > v) || (w == v && o < e);
-            }
+            for (int o = lb; o < lb + cnt; ++o) rank += s_key[o] > v;
             if (rank < k) {
                 s_slot[rank] = e;
                 s_row[e] = 1 + (f - 1) * k + rank;
@@ -270,15 +321,17 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         __syncthreads();
         const int nf = cnt < k ? cnt : k;
         for (int i = tid; i < nf * k; i += kSelThreads) {
-            const int s = i / k, r = i % k;
-            const int par = s_slot[s];
-            const int rr = 1 + (f - 1) * k + s;
+            const int sl = i / k, ch = i % k;
+            const int par = s_slot[sl];
+            const int rr = 1 + (f - 1) * k + sl;
             const int e = np + i;
-            s_logv[e] = s_logv[par] + s_lc[rr * k + r];
-            s_ptok[e] = s_tok[rr * k + r];
+            const double lv = s_logv[par] + s_lc[rr * k + ch];
+            s_logv[e] = lv;
+            s_key[e] = pool_key(lv, e);
+            s_ptok[e] = s_ctok[rr * k + ch];
             s_par[e] = par;
             s_row[e] = -1;
-            s_dep[e] = f + 1;
+            s_dep[e] = (unsigned char)(f + 1);
         }
         __syncthreads();
         lb = np;
@@ -286,70 +339,83 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         np += nf * k;
     }
 
-    // 4. rerank: bitonic sort of the pool by (logv desc, creation asc)
-    for (int i = tid; i < NP; i += kSelThreads) {
-        PoolEntry pe;
-        pe.logv = i < np ? s_logv[i] : -INFINITY;
-        pe.idx = i;
-        pe.pad = 0;
-        s_sort[i] = pe;
-        s_flat[i] = -1;
+    // rerank: radix-select the m-th largest composite key (keys are unique)
+    if (tid == 0) {
+        s_prefix = 0;
+        s_remaining = m;
     }
     __syncthreads();
-    for (int kk = 2; kk <= NP; kk <<= 1) {
-        for (int j = kk >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < NP; i += kSelThreads) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    PoolEntry x0 = s_sort[i], x1 = s_sort[ixj];
-                    const bool first_half = (i & kk) == 0;
-                    // first_half: ascending position = better first
-                    const bool swap = first_half ? entry_before(x1, x0) : entry_before(x0, x1);
-                    if (swap) {
-                        s_sort[i] = x1;
-                        s_sort[ixj] = x0;
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
-    // kept flags live in s_flat (1 = kept) until the scan below
-    for (int i = tid; i < m; i += kSelThreads) s_flat[s_sort[i].idx] = 1;
-    __syncthreads();
-
-    // 5. flatten: flat index = 1 + number of kept entries created earlier
-    {
-        const int nchunks = (np + 31) / 32;
-        for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
-            const int e = ch * 32 + lane;
-            const bool kept = e < np && s_flat[e] == 1;
-            const unsigned bal = __ballot_sync(0xffffffffu, kept);
-            if (lane == 0) s_wsum[ch] = __popc(bal);
+    uint64_t hmask = 0;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        s_hist[tid] = 0;  // kSelThreads == 256 buckets
+        __syncthreads();
+        const uint64_t prefix = s_prefix;
+        for (int e = tid; e < np; e += kSelThreads) {
+            const uint64_t key = s_key[e];
+            if ((key & hmask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255], 1);
         }
         __syncthreads();
         if (warp == 0) {
-            int v = lane < nchunks ? s_wsum[lane] : 0;
-            int incl = v;
+            // buckets from the top: lane l owns buckets 255-8l .. 248-8l
+            int cntl = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) cntl += s_hist[255 - 8 * lane - q];
+            int incl = cntl;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                int o = __shfl_up_sync(0xffffffffu, incl, off);
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
                 if (lane >= off) incl += o;
             }
-            if (lane < nchunks) s_wsum[lane] = incl - v;  // exclusive
+            const int need = s_remaining;
+            const int excl = incl - cntl;
+            if (excl < need && need <= incl) {
+                int acc = excl;
+                for (int q = 0; q < 8; ++q) {
+                    const int bucket = 255 - 8 * lane - q;
+                    const int h = s_hist[bucket];
+                    if (acc + h >= need) {
+                        s_prefix = prefix | (uint64_t(bucket) << shift);
+                        s_remaining = need - acc;
+                        break;
+                    }
+                    acc += h;
+                }
+            }
         }
-        __syncthreads();
-        for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
-            const int e = ch * 32 + lane;
-            const bool kept = e < np && s_flat[e] == 1;
-            const unsigned bal = __ballot_sync(0xffffffffu, kept);
-            const int before = __popc(bal & ((1u << lane) - 1u));
-            if (e < np) s_flat[e] = kept ? 1 + s_wsum[ch] + before : -1;
-        }
+        hmask |= uint64_t(255) << shift;
         __syncthreads();
     }
+    const uint64_t thr = s_prefix;  // the m-th largest key itself
 
-    // 6. outputs
+    // flatten: flat index = 1 + number of kept entries created earlier (ballots over creation order)
+    const int nchunks = (np + 31) / 32;
+    for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
+        const int e = ch * 32 + lane;
+        const bool kept = e < np && s_key[e] >= thr;
+        const unsigned bal = __ballot_sync(0xffffffffu, kept);
+        if (lane == 0) s_wsum[ch] = __popc(bal);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int v = lane < nchunks ? s_wsum[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane < nchunks) s_wsum[lane] = incl - v;
+    }
+    __syncthreads();
+    for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
+        const int e = ch * 32 + lane;
+        const bool kept = e < np && s_key[e] >= thr;
+        const unsigned bal = __ballot_sync(0xffffffffu, kept);
+        if (e < np) s_flat[e] = kept ? 1 + s_wsum[ch] + __popc(bal & ((1u << lane) - 1u)) : -1;
+    }
+    __syncthreads();
+
+    // outputs
     const int n = m + 1;
     int32_t *tokens = a.tokens + size_t(b) * n;
     int32_t *parents = a.parents + size_t(b) * n;
@@ -357,7 +423,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     int32_t *node_row = a.node_row + size_t(b) * n;
     uint64_t *mask = a.mask + size_t(b) * n;
     if (tid == 0) {
-        int32_t rt = a.root_token[b];
+        const int32_t rt = a.root_token[b];
         if (rt < 0 || rt >= a.V) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
         tokens[0] = rt;
         parents[0] = -1;
@@ -392,34 +458,19 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     }
 }
 
-constexpr size_t select_smem_bytes() {
-    return size_t(kMaxPool) * sizeof(double)       // s_lc
-           + size_t(kMaxPool) * sizeof(PoolEntry)  // s_sort
-           + size_t(kMaxPool) * sizeof(double)     // s_logv
-           + size_t(kMaxPool) * sizeof(int) * 6    // s_tok .. s_flat
-           + 16 * sizeof(int) + 32 * sizeof(int);
-}
-
 int kmax_for(int k) { return k <= 4 ? 4 : (k <= 8 ? 8 : 16); }
 
+// One wave of CTAs: rows are split over a cluster only while the grid stays within the SM count
+// (each CTA streams its slice with loads of the next batch in flight).
 int splits_for(const eagle_tree_cfg &c) {
     const int R = 1 + (c.depth - 1) * c.topk;
     const long rows = long(c.batch) * R;
-    const int want = int((4L * 152 + rows - 1) / rows);
-    const int cap = c.vocab / 2048 > 1 ? c.vocab / 2048 : 1;
-    int s = want < cap ? want : cap;
-    if (s > 32) s = 32;
-    return s < 1 ? 1 : s;
-}
-
-template <int KMAX>
-cudaError_t launch_select_attr() {
-    static bool done = false;  // set once per process; the attribute is per function
-    if (done) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(tree_select_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(select_smem_bytes()));
-    if (e == cudaSuccess) done = true;
-    return e;
+    long sp = 152 / rows;
+    const long per = long(kRowThreads) * kRowVals;
+    const long useful = (c.vocab + per - 1) / per;  // no empty CTAs
+    if (sp > useful) sp = useful;
+    if (sp > kMaxSplits) sp = kMaxSplits;
+    return sp < 1 ? 1 : int(sp);
 }
 
 template <int KMAX>
@@ -430,36 +481,49 @@ eagle_status launch_build(const eagle_tree_cfg &c, const float *draft, const int
     const int splits = splits_for(c);
     int chunk = (c.vocab + splits - 1) / splits;
     chunk = (chunk + 3) & ~3;
-    int32_t *status = reinterpret_cast<int32_t *>(ws);
-    uint64_t *part_keys = reinterpret_cast<uint64_t *>(ws + kWsHeader);
-    const size_t nslots = size_t(c.batch) * R * splits;
-    float2 *part_ms = reinterpret_cast<float2 *>(ws + kWsHeader + align_up(nslots * KMAX * sizeof(uint64_t), 256));
-    const float cexp = kLog2e / c.tree_temp;
+    RowArgs ra;
+    ra.x = draft;
+    ra.row_tok = reinterpret_cast<int32_t *>(ws + kWsHeader);
+    ra.row_lc = reinterpret_cast<double *>(ws + kWsHeader + align_up(size_t(c.batch) * R * c.topk * 4, 256));
+    ra.V = c.vocab;
+    ra.R = R;
+    ra.k = c.topk;
+    ra.chunk = chunk;
+    ra.c = kLog2e / c.tree_temp;
+    ra.inv_t = 1.0 / double(c.tree_temp);
 
-    if (launch_select_attr<KMAX>() != cudaSuccess) return EAGLE_ERR_CUDA;
-    dim3 g1(splits, R, c.batch);
-    row_topk_kernel<KMAX><<<g1, kRowThreads, 0, stream>>>(draft, c.vocab, R, splits, chunk, cexp, part_keys, part_ms);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, R, c.batch);
+    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, row_topk_kernel, ra) != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();
-    SelectArgs a;
-    a.part_keys = part_keys;
-    a.part_ms = part_ms;
-    a.root_token = root;
-    a.tokens = tokens;
-    a.parents = parents;
-    a.depths = depths;
-    a.node_row = node_row;
-    a.mask = mask;
-    a.node_logv = node_logv;
-    a.status = status;
-    a.V = c.vocab;
-    a.D = c.depth;
-    a.k = c.topk;
-    a.m = c.keep;
-    a.R = R;
-    a.splits = splits;
-    a.c = cexp;
-    a.inv_t = 1.0 / double(c.tree_temp);
-    tree_select_kernel<KMAX><<<c.batch, kSelThreads, select_smem_bytes(), stream>>>(a);
+
+    SelectArgs sa;
+    sa.row_tok = ra.row_tok;
+    sa.row_lc = ra.row_lc;
+    sa.root_token = root;
+    sa.tokens = tokens;
+    sa.parents = parents;
+    sa.depths = depths;
+    sa.node_row = node_row;
+    sa.mask = mask;
+    sa.node_logv = node_logv;
+    sa.status = reinterpret_cast<int32_t *>(ws);
+    sa.V = c.vocab;
+    sa.D = c.depth;
+    sa.k = c.topk;
+    sa.m = c.keep;
+    sa.R = R;
+    tree_select_kernel<<<c.batch, kSelThreads, 0, stream>>>(sa);
     note_launch();
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
@@ -468,10 +532,8 @@ eagle_status launch_build(const eagle_tree_cfg &c, const float *draft, const int
 
 size_t build_tree_workspace_bytes(const eagle_tree_cfg &c) {
     const int R = 1 + (c.depth - 1) * c.topk;
-    const int splits = splits_for(c);
-    const size_t nslots = size_t(c.batch) * R * splits;
-    const int kmax = kmax_for(c.topk);
-    return kWsHeader + align_up(nslots * kmax * sizeof(uint64_t), 256) + align_up(nslots * sizeof(float2), 256);
+    const size_t ent = size_t(c.batch) * R * c.topk;
+    return kWsHeader + align_up(ent * 4, 256) + align_up(ent * 8, 256);
 }
 
 eagle_status build_tree_launch(const eagle_tree_cfg &c, const float *draft, const int32_t *root, int32_t *tokens,

@@ -50,11 +50,95 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
     return v;
 }
 
+// Warp-wide sorted top-KMAX list: lane j < KMAX holds the j-th largest key seen (0 = empty).
+// insert() offers one key per lane; only keys above the current KMAX-th key enter, one at a time
+// (the list is shifted down by one lane at the insertion point).  Keys must be unique.
+template <int KMAX>
+struct WarpTopK {
+    uint64_t key = 0;  // this lane's slot (lanes >= KMAX keep 0)
+    uint64_t thr = 0;  // current KMAX-th key, identical on every lane
+
+    __device__ __forceinline__ void insert(uint64_t cand) {
+        const int lane = threadIdx.x & 31;
+        unsigned pend = __ballot_sync(0xffffffffu, cand > thr);
+        while (pend) {
+            const int src = __ffs(pend) - 1;
+            pend &= pend - 1;
+            const uint64_t c = __shfl_sync(0xffffffffu, cand, src);  // (2 x 32-bit shuffles)
+            if (c <= thr) continue;
+            const unsigned above = __ballot_sync(0xffffffffu, lane < KMAX && key > c);
+            const int pos = __popc(above);
+            const uint64_t up = __shfl_up_sync(0xffffffffu, key, 1);
+            if (lane < KMAX && lane >= pos) key = (lane == pos) ? c : up;
+            thr = __shfl_sync(0xffffffffu, key, KMAX - 1);
+        }
+    }
+};
+
+// Merge two descending 16-key lists held by one warp: lanes 0..15 pass list A's key `lane`,
+// lanes 16..31 pass list B's key `31 - lane` (B reversed, so the 32 lanes form a bitonic
+// sequence).  Returns the merged descending sequence; lanes 0..15 hold the top 16.
+__device__ __forceinline__ uint64_t warp_bitonic_merge32(uint64_t v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const uint64_t o = shfl_xor_u64(v, stride);
+        const bool lower = (lane & stride) == 0;
+        v = lower ? (o > v ? o : v) : (o < v ? o : v);
+    }
+    return v;
+}
+
+// Orderable 64-bit image of a double (integer order = numeric order; -0 folded onto +0).
+__device__ __forceinline__ uint64_t double_order_key(double d) {
+    const uint64_t u = static_cast<uint64_t>(__double_as_longlong(d + 0.0));
+    return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+
 // 2^x on the SFU (approximate, relative error about 2^-22; used inside softmax loops).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// ---- mbarrier + bulk copy (global -> own shared memory), with bounded waits ----
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(count));
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
+}
+// One bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) into this CTA's shared
+// memory; completion is counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(d),
+                 "l"(src), "r"(bytes), "r"(b)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for phase `parity` of `bar` at most `limit` polls; false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit = 1u << 24) {
+    for (uint32_t it = 0; it < limit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
 }
 
 constexpr float kLog2e = 1.4426950408889634f;

@@ -18,11 +18,13 @@
 // were rejected) can be computed for all nodes at once, in parallel, and the sequential walk over
 // the tree reduces to comparisons of uniforms with precomputed ratios.
 //
-//   verify_prep_kernel  one 8-CTA cluster per (sequence, node): each CTA holds 1/8 of the
-//                       node's target row (and of its draft row when it has children) in shared
-//                       memory; log-sum-exp, the S_j passes and the inverse-CDF scan are reduced
-//                       across the cluster through distributed shared memory.
-//   verify_walk_kernel  one warp per sequence: validates the tree and walks it.
+//   verify_prep_kernel  one cluster of CL CTAs (8, or 16 for vocabularies above 131072) per
+//                       (sequence, node).  Each thread holds 32 consecutive tokens of the node's
+//                       target row (and of its draft row when the node has children) in
+//                       registers; log-sum-exp, the S_j passes and the inverse-CDF scan are
+//                       register loops whose partials are reduced across the cluster through
+//                       distributed shared memory (one cluster barrier per pass).
+//   verify_walk_kernel  one CTA per sequence: validates the tree and walks it.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -36,8 +38,9 @@ namespace eagle {
 
 namespace {
 
-constexpr int kCl = 8;            // CTAs per cluster (one node's row split 8 ways)
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 512;
+constexpr int kWarpsPrep = kPrepThreads / 32;
+constexpr int kE = 32;  // tokens per thread and row
 constexpr int kMaxKids = 64;
 
 struct VerifyArgs {
@@ -59,19 +62,6 @@ struct VerifyArgs {
     int greedy;
 };
 
-__device__ __forceinline__ float block_sum(float v, float *scratch) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    __syncthreads();
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    float r = 0.f;
-#pragma unroll
-    for (int w = 0; w < kPrepThreads / 32; ++w) r += scratch[w];
-    return r;
-}
-
 __device__ __forceinline__ void ms_merge(float &m, float &s, float mo, float so, float c) {
     const float M = fmaxf(m, mo);
     if (M == -INFINITY) return;
@@ -81,136 +71,148 @@ __device__ __forceinline__ void ms_merge(float &m, float &s, float mo, float so,
     s = x + y;
 }
 
-// add one element x to a running (max m, scaled sum s)
-__device__ __forceinline__ void ms_add(float &m, float &s, float x, float c) {
-    if (x > m) {
-        s = s * exp2f((m - x) * c) + 1.f;
-        m = x;
+// Load this thread's kE consecutive values of a row slice into registers (-inf past the end).
+__device__ __forceinline__ void load_run(float (&v)[kE], const float *src, int t0, int cnt, bool vec) {
+    if (vec) {
+#pragma unroll
+        for (int j = 0; j < kE / 4; ++j) {
+            const int idx = t0 + 4 * j;
+            const float4 w = idx < cnt ? __ldg(reinterpret_cast<const float4 *>(src + idx))
+                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            v[4 * j] = w.x;
+            v[4 * j + 1] = w.y;
+            v[4 * j + 2] = w.z;
+            v[4 * j + 3] = w.w;
+        }
     } else {
-        s += exp2f((x - m) * c);
+#pragma unroll
+        for (int j = 0; j < kE; ++j) v[j] = t0 + j < cnt ? __ldg(src + t0 + j) : -INFINITY;
     }
 }
 
-__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kPrepThreads)
-    verify_prep_kernel(VerifyArgs a) {
-    extern __shared__ __align__(16) float sm[];  // [slice] target, then [slice] draft
-    __shared__ float s_scratch[kPrepThreads / 32];
-    __shared__ unsigned long long s_xchg[2][4];  // per-pass partials exchanged across the cluster (bit patterns)
+template <int CL>
+__global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs a) {
+    constexpr int kParts = CL * kWarpsPrep;
+    // per-warp partials published to the cluster, double-buffered by pass parity
+    __shared__ float4 s_part[2][kWarpsPrep];
+    __shared__ double s_tot;
+    __shared__ double s_rank[CL];  // final pass: per-rank totals
+    __shared__ int s_rlast[CL];    // final pass: per-rank last positive index
     __shared__ int s_kids[kMaxKids];
-    __shared__ int s_nk;
+    __shared__ float s_xk[kMaxKids], s_yk[kMaxKids];
+    __shared__ double s_cj[kMaxKids + 1], s_Sj[kMaxKids + 1];
+    __shared__ int s_nk, s_claim;
+    __shared__ float s_M[2];
+    __shared__ double s_lnS[2];
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = int(cluster.block_rank());
     const int i = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = a.n, V = a.V;
     const int lo = rank * a.slice;
     const int hi = min(V, lo + a.slice);
     const int cnt = hi > lo ? hi - lo : 0;
+    const int t0 = tid * kE;  // this thread's run, relative to lo
 
     const int32_t *par = a.parents + size_t(b) * n;
     const int32_t *tok = a.tokens + size_t(b) * n;
-    if (tid == 0) {
+    // children of node i, in ascending index (warp 0: ballots over the <= 64 nodes)
+    if (warp == 0) {
         int nk = 0;
-        for (int j = i + 1; j < n; ++j)
-            if (par[j] == i && nk < kMaxKids) s_kids[nk++] = j;
-        s_nk = nk;
+        for (int j0 = i + 1; j0 < n; j0 += 32) {
+            const int j = j0 + lane;
+            const bool kid = j < n && par[j] == i;
+            const unsigned bal = __ballot_sync(0xffffffffu, kid);
+            if (kid) s_kids[nk + __popc(bal & ((1u << lane) - 1u))] = j;
+            nk += __popc(bal);
+        }
+        if (lane == 0) s_nk = nk;
     }
     __syncthreads();
     const int J = s_nk;
     const float *xrow = a.target + (size_t(b) * n + i) * V;
-    int row = J > 0 ? a.node_row[size_t(b) * n + i] : -1;
-    const bool has_q = J > 0 && row >= 0 && row < a.R;
+    const int row = J > 0 ? a.node_row[size_t(b) * n + i] : -1;
+    const bool has_q = J > 0 && row >= 0 && row < a.R && !a.greedy;
     const float *yrow = has_q ? a.draft + (size_t(b) * a.R + row) * V : nullptr;
+    const bool vec = ((V & 3) == 0) && ((lo & 3) == 0) && ((reinterpret_cast<uintptr_t>(xrow) & 15) == 0) &&
+                     (!has_q || (reinterpret_cast<uintptr_t>(yrow) & 15) == 0);
     int pass = 0;
 
-    // exchange: every CTA publishes `vals` (up to 4 doubles) and reads all ranks' in rank order
-    __shared__ unsigned long long s_all[kCl][4];
-    auto exchange = [&](const unsigned long long *vals, int nv) {
+    // Publish each warp's float4 (from lane 0), make it visible to the cluster; warp 0 then
+    // fetches all kParts partials (part = rank * kWarpsPrep + warp).
+    auto publish = [&](float4 v) {
         const int slot = pass & 1;
-        if (tid < nv) s_xchg[slot][tid] = vals[tid];
+        if (lane == 0) s_part[slot][warp] = v;
         cluster.sync();
-        if (tid < kCl * nv) {
-            const int r = tid / nv, v = tid % nv;
-            unsigned long long *remote = cluster.map_shared_rank(&s_xchg[slot][0], r);
-            s_all[r][v] = remote[v];
-        }
-        __syncthreads();
         ++pass;
+        return slot;
     };
-    auto dbl = [](double x) { return static_cast<unsigned long long>(__double_as_longlong(x)); };
-    auto all = [&](int r, int v) { return __longlong_as_double(static_cast<long long>(s_all[r][v])); };
+    auto fetch = [&](int slot, int part) -> float4 {
+        const float4 *remote = cluster.map_shared_rank(&s_part[slot][0], part / kWarpsPrep);
+        return remote[part % kWarpsPrep];
+    };
+
+    float xp[kE], xq[kE];
+    load_run(xp, xrow + lo, t0, cnt, vec);
+    if (has_q) load_run(xq, yrow + lo, t0, cnt, vec);
+    if (rank == 0 && tid < J) {  // the children's logits, for their accept ratios
+        const int t = tok[s_kids[tid]];
+        const bool ok = has_q && t >= 0 && t < V;
+        s_xk[tid] = ok ? __ldg(xrow + t) : 0.f;
+        s_yk[tid] = ok ? __ldg(yrow + t) : 0.f;
+    }
 
     if (a.greedy) {
-        // argmax of the target row (ties to the lower id)
+        // argmax of the target row (ties to the lower id): thread, warp, cluster
         uint64_t best = 0;
-        for (int t = lo + tid; t < hi; t += kPrepThreads) {
-            const uint64_t key = topk_key(__ldg(xrow + t), uint32_t(t));
+#pragma unroll
+        for (int j = 0; j < kE; ++j) {
+            const uint64_t key = xp[j] == -INFINITY ? 0ull : topk_key(xp[j], uint32_t(lo + t0 + j));
             best = key > best ? key : best;
         }
         best = warp_max_u64(best);
-        __shared__ uint64_t s_best[kPrepThreads / 32];
-        if ((tid & 31) == 0) s_best[tid >> 5] = best;
-        __syncthreads();
-        if (tid < 32) {
-            uint64_t v = tid < kPrepThreads / 32 ? s_best[tid] : 0;
-            v = warp_max_u64(v);
-            if (tid == 0) s_best[0] = v;
-        }
-        __syncthreads();
-        const unsigned long long mine[1] = {s_best[0]};
-        exchange(mine, 1);
-        if (rank == 0 && tid == 0) {
+        const int slot = publish(make_float4(__uint_as_float(uint32_t(best)), __uint_as_float(uint32_t(best >> 32)),
+                                             0.f, 0.f));
+        if (warp == 0) {
             uint64_t g = 0;
-            for (int r = 0; r < kCl; ++r) {
-                const uint64_t v = s_all[r][0];
-                g = v > g ? v : g;
+#pragma unroll
+            for (int h = 0; h < kParts / 32; ++h) {
+                const float4 v = fetch(slot, lane + 32 * h);
+                const uint64_t key = (uint64_t(__float_as_uint(v.y)) << 32) | __float_as_uint(v.x);
+                g = key > g ? key : g;
             }
-            a.final_tok[size_t(b) * n + i] = int32_t(topk_key_token(g));
-            for (int j = 0; j < J; ++j) a.ratio[size_t(b) * n + s_kids[j]] = NAN;
-            if (a.out_ratio) {
-                for (int j = 0; j < J; ++j) a.out_ratio[size_t(b) * n + s_kids[j]] = NAN;
-                if (i == 0) a.out_ratio[size_t(b) * n] = NAN;
+            g = warp_max_u64(g);
+            if (rank == 0 && lane == 0) a.final_tok[size_t(b) * n + i] = int32_t(topk_key_token(g));
+        }
+        if (rank == 0) {
+            for (int j = tid; j < J; j += kPrepThreads) {
+                a.ratio[size_t(b) * n + s_kids[j]] = NAN;
+                if (a.out_ratio) a.out_ratio[size_t(b) * n + s_kids[j]] = NAN;
             }
+            if (i == 0 && tid == 0 && a.out_ratio) a.out_ratio[size_t(b) * n] = NAN;
         }
         cluster.sync();
         return;
     }
 
-    float *sp = sm;
-    float *sq = sm + a.slice;
     const float c = a.c;
-
-    // pass A: stage the row slices and their (max, scaled sum)
-    float mp = -INFINITY, spp = 0.f, mq = -INFINITY, sqq = 0.f;
-    const bool vec = ((V & 3) == 0) && ((lo & 3) == 0);
-    if (vec) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(xrow + lo);
-        const float4 *y4 = has_q ? reinterpret_cast<const float4 *>(yrow + lo) : nullptr;
-        for (int t = tid; t < cnt / 4; t += kPrepThreads) {
-            const float4 v = __ldg(x4 + t);
-            reinterpret_cast<float4 *>(sp)[t] = v;
-            const float vv[4] = {v.x, v.y, v.z, v.w};
+    // row statistics: max, then the scaled sum of exponentials, per thread / warp / cluster
+    float mp = -INFINITY, mq = -INFINITY, spp = 0.f, sqq = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) ms_add(mp, spp, vv[e], c);
-            if (has_q) {
-                const float4 w = __ldg(y4 + t);
-                reinterpret_cast<float4 *>(sq)[t] = w;
-                const float ww[4] = {w.x, w.y, w.z, w.w};
+    for (int j = 0; j < kE; ++j) mp = fmaxf(mp, xp[j]);
+    if (mp != -INFINITY) {
+        const float mc = mp * c;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ms_add(mq, sqq, ww[e], c);
-            }
-        }
-    } else {
-        for (int t = tid; t < cnt; t += kPrepThreads) {
-            const float v = __ldg(xrow + lo + t);
-            sp[t] = v;
-            ms_add(mp, spp, v, c);
-            if (has_q) {
-                const float w = __ldg(yrow + lo + t);
-                sq[t] = w;
-                ms_add(mq, sqq, w, c);
-            }
+        for (int j = 0; j < kE; ++j) spp += fast_exp2(fmaf(xp[j], c, -mc));
+    }
+    if (has_q) {
+#pragma unroll
+        for (int j = 0; j < kE; ++j) mq = fmaxf(mq, xq[j]);
+        if (mq != -INFINITY) {
+            const float mc = mq * c;
+#pragma unroll
+            for (int j = 0; j < kE; ++j) sqq += fast_exp2(fmaf(xq[j], c, -mc));
         }
     }
 #pragma unroll
@@ -218,208 +220,231 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kPrepThreads)
         ms_merge(mp, spp, __shfl_xor_sync(0xffffffffu, mp, off), __shfl_xor_sync(0xffffffffu, spp, off), c);
         ms_merge(mq, sqq, __shfl_xor_sync(0xffffffffu, mq, off), __shfl_xor_sync(0xffffffffu, sqq, off), c);
     }
-    __shared__ float4 s_ms[kPrepThreads / 32];
-    if ((tid & 31) == 0) s_ms[tid >> 5] = make_float4(mp, spp, mq, sqq);
-    __syncthreads();
     {
-        float M0 = -INFINITY, S0 = 0.f, M1 = -INFINITY, S1 = 0.f;
-        for (int w = 0; w < kPrepThreads / 32; ++w) {
-            ms_merge(M0, S0, s_ms[w].x, s_ms[w].y, c);
-            ms_merge(M1, S1, s_ms[w].z, s_ms[w].w, c);
+        const int slot = publish(make_float4(mp, spp, mq, sqq));
+        if (warp == 0) {
+            // row-wide max, then the scaled sums in double; identical in every CTA (same partials,
+            // same order)
+            float4 v[kParts / 32];
+            float Mp = -INFINITY, Mq = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < kParts / 32; ++h) {
+                v[h] = fetch(slot, lane + 32 * h);
+                Mp = fmaxf(Mp, v[h].x);
+                Mq = fmaxf(Mq, v[h].z);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, off));
+                Mq = fmaxf(Mq, __shfl_xor_sync(0xffffffffu, Mq, off));
+            }
+            double Sp = 0.0, Sq = 0.0;
+#pragma unroll
+            for (int h = 0; h < kParts / 32; ++h) {
+                if (v[h].x != -INFINITY) Sp += double(v[h].y) * double(exp2f((v[h].x - Mp) * c));
+                if (v[h].z != -INFINITY) Sq += double(v[h].w) * double(exp2f((v[h].z - Mq) * c));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                Sp += __shfl_xor_sync(0xffffffffu, Sp, off);
+                Sq += __shfl_xor_sync(0xffffffffu, Sq, off);
+            }
+            if (lane == 0) {
+                s_M[0] = Mp;
+                s_M[1] = Mq;
+                s_lnS[0] = log(Sp);
+                s_lnS[1] = has_q ? log(Sq) : 0.0;
+            }
         }
-        const unsigned long long mine[4] = {dbl(M0), dbl(S0), dbl(M1), dbl(S1)};
-        exchange(mine, 4);
+        __syncthreads();
     }
-    // row-wide max and log of the scaled sum (one thread computes, every CTA of the cluster gets
-    // the same values because it reduces the same partials in the same order)
-    __shared__ float s_M[2];
-    __shared__ double s_lnS[2];
-    if (tid == 0) {
-        float Mp = -INFINITY, Mq = -INFINITY;
-        for (int r = 0; r < kCl; ++r) {
-            Mp = fmaxf(Mp, float(all(r, 0)));
-            Mq = fmaxf(Mq, float(all(r, 2)));
-        }
-        double Sp = 0.0, Sq = 0.0;
-        for (int r = 0; r < kCl; ++r) {
-            const float m0 = float(all(r, 0)), m1 = float(all(r, 2));
-            if (m0 != -INFINITY) Sp += all(r, 1) * double(exp2f((m0 - Mp) * c));
-            if (m1 != -INFINITY) Sq += all(r, 3) * double(exp2f((m1 - Mq) * c));
-        }
-        s_M[0] = Mp;
-        s_M[1] = Mq;
-        s_lnS[0] = log(Sp);
-        s_lnS[1] = has_q ? log(Sq) : 0.0;
-    }
-    __syncthreads();
     const float Mp = s_M[0], Mq = s_M[1];
     const double lnSp = s_lnS[0], lnSq = s_lnS[1];
-    const float lp_hi = float(lnSp), lp_lo = float(lnSp - double(lp_hi));
-    const float lq_hi = float(lnSq), lq_lo = float(lnSq - double(lq_hi));
-    const float inv_t = a.inv_t;
-    // p0(t) = exp((x - Mp)/T - ln Sp), with ln Sp carried as hi + lo
-    auto p_of = [&](float x) { return expf(fmaf(x - Mp, inv_t, -lp_hi) - lp_lo); };
-    auto q_of = [&](float y) { return expf(fmaf(y - Mq, inv_t, -lq_hi) - lq_lo); };
-
-    // pass B: convert the slices to probabilities in place
-    for (int t = tid; t < cnt; t += kPrepThreads) {
-        sp[t] = p_of(sp[t]);
-        if (has_q) sq[t] = q_of(sq[t]);
-    }
-    __syncthreads();
-
-    // rejection chain at this node: ratio_j for child j, then the residual of the final draw
-    double cj = 0.0, Sj = 1.0;  // c_0, S_0
-    for (int j = 0; j < J; ++j) {
-        const int child = s_kids[j];
-        if (tid == 0 && rank == 0) {
-            // the accept ratio of child j in double: p0(t) - c_j q(t) cancels when the two are close
-            const int t = tok[child];
-            float r = NAN;
-            if (has_q && t >= 0 && t < V) {
-                const double p0 = exp((double(__ldg(xrow + t)) - double(Mp)) * a.inv_td - lnSp);
-                const double q0 = exp((double(__ldg(yrow + t)) - double(Mq)) * a.inv_td - lnSq);
-                const double num = j == 0 ? p0 : fmax(p0 - cj * q0, 0.0);
-                const double den = Sj * q0;
-                r = den > 0.0 ? float(num / den) : INFINITY;
-            }
-            a.ratio[size_t(b) * n + child] = r;
-            if (a.out_ratio) a.out_ratio[size_t(b) * n + child] = r;
+    {
+        // probabilities in place: p0 = 2^(((x - Mp)/T - ln Sp) log2 e), ln S carried as hi + lo
+        const float lp_hi = float(lnSp), lp_lo = float(lnSp - double(lp_hi));
+        const float lq_hi = float(lnSq), lq_lo = float(lnSq - double(lq_hi));
+        const float inv_t = a.inv_t;
+#pragma unroll
+        for (int j = 0; j < kE; ++j)
+            xp[j] = xp[j] == -INFINITY ? 0.f : fast_exp2((fmaf(xp[j] - Mp, inv_t, -lp_hi) - lp_lo) * kLog2e);
+        if (has_q) {
+#pragma unroll
+            for (int j = 0; j < kE; ++j)
+                xq[j] = xq[j] == -INFINITY ? 0.f : fast_exp2((fmaf(xq[j] - Mq, inv_t, -lq_hi) - lq_lo) * kLog2e);
         }
-        // reject child j: c_{j+1} = c_j + S_j, S_{j+1} = sum (p0 - c_{j+1} q)+
+    }
+
+    // rejection chain: c_0 = 0, S_0 = 1; after rejecting child j: c_{j+1} = c_j + S_j and
+    // S_{j+1} = sum (p0 - c_{j+1} q)+ (a zero sum keeps the previous distribution)
+    double cj = 0.0, Sj = 1.0;
+    if (tid == 0) {
+        s_cj[0] = 0.0;
+        s_Sj[0] = 1.0;
+    }
+    for (int j = 0; j < J && has_q; ++j) {
         const double cn = cj + Sj;
         const float cnf = float(cn);
         float part = 0.f;
-        if (has_q)
-            for (int t = tid; t < cnt; t += kPrepThreads) part += fmaxf(fmaf(-cnf, sq[t], sp[t]), 0.f);
-        part = block_sum(part, s_scratch);
-        const unsigned long long mine[1] = {dbl(double(part))};
-        exchange(mine, 1);
-        double Sn = 0.0;
-        for (int r = 0; r < kCl; ++r) Sn += all(r, 0);  // few double adds, same order everywhere
-        if (Sn > 0.0) {  // otherwise the adjusted distribution keeps p_j
+#pragma unroll
+        for (int e = 0; e < kE; ++e) part += fmaxf(fmaf(-cnf, xq[e], xp[e]), 0.f);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+        const int slot = publish(make_float4(part, 0.f, 0.f, 0.f));
+        if (warp == 0) {
+            double S = 0.0;
+#pragma unroll
+            for (int h = 0; h < kParts / 32; ++h) S += double(fetch(slot, lane + 32 * h).x);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
+            if (lane == 0) s_tot = S;
+        }
+        __syncthreads();
+        const double Sn = s_tot;
+        if (Sn > 0.0) {
             cj = cn;
             Sj = Sn;
         }
+        if (tid == 0) {
+            s_cj[j + 1] = cj;
+            s_Sj[j + 1] = Sj;
+        }
+    }
+    __syncthreads();
+    // accept ratios of the children, in double (p0 - c_j q cancels when the two are close)
+    if (rank == 0 && tid < J) {
+        float r = NAN;
+        if (has_q) {
+            const double p0 = exp((double(s_xk[tid]) - double(Mp)) * a.inv_td - lnSp);
+            const double q0 = exp((double(s_yk[tid]) - double(Mq)) * a.inv_td - lnSq);
+            const double num = tid == 0 ? p0 : fmax(p0 - s_cj[tid] * q0, 0.0);
+            const double den = s_Sj[tid] * q0;
+            r = den > 0.0 ? float(num / den) : INFINITY;
+        }
+        a.ratio[size_t(b) * n + s_kids[tid]] = r;
+        if (a.out_ratio) a.out_ratio[size_t(b) * n + s_kids[tid]] = r;
     }
     if (i == 0 && rank == 0 && tid == 0 && a.out_ratio) a.out_ratio[size_t(b) * n] = NAN;
 
     // final draw at this node: residual r(t) = (p0 - c_J q)+ (p0 itself when J == 0), inverse CDF
-    // with u[0].  Each thread owns a contiguous run of the slice.
+    // with u[0] over ascending token ids; this thread's run is tokens lo + t0 ... lo + t0 + kE - 1
     const float cjf = float(cj);
     const bool use_res = J > 0 && has_q;
-    const int run = (cnt + kPrepThreads - 1) / kPrepThreads;
-    const int t0 = min(cnt, tid * run), t1 = min(cnt, t0 + run);
     float tsum = 0.f;
     int tlast = -1;
-    for (int t = t0; t < t1; ++t) {
-        const float r = use_res ? fmaxf(fmaf(-cjf, sq[t], sp[t]), 0.f) : sp[t];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+        const float r = use_res ? fmaxf(fmaf(-cjf, xq[e], xp[e]), 0.f) : xp[e];
+        xp[e] = r;  // keep the residual for the scan below
         tsum += r;
-        if (r > 0.f) tlast = t;
+        if (r > 0.f) tlast = t0 + e;
     }
-    // exclusive scan of the run sums across the block
-    const int lane = tid & 31, warp = tid >> 5;
-    float incl = tsum;
+    float incl = tsum;  // inclusive scan of the run sums within the warp
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const float o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
     }
-    __shared__ float s_wtot[kPrepThreads / 32];
-    __shared__ int s_wlast[kPrepThreads / 32];
     int wl = tlast;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) wl = max(wl, __shfl_xor_sync(0xffffffffu, wl, off));
-    if (lane == 31) s_wtot[warp] = incl;
-    if (lane == 0) s_wlast[warp] = wl;
+    const float wtot = __shfl_sync(0xffffffffu, incl, 31);
+    const int slot = publish(make_float4(wtot, __int_as_float(wl), 0.f, 0.f));
+    if (warp == 0 && lane < CL) {
+        // rank `lane`: total and last positive index (its warps in order)
+        double rt = 0.0;
+        int rl = -1;
+        for (int w = 0; w < kWarpsPrep; ++w) {
+            const float4 v = fetch(slot, lane * kWarpsPrep + w);
+            rt += double(v.x);
+            rl = max(rl, __float_as_int(v.y));
+        }
+        s_rank[lane] = rt;
+        s_rlast[lane] = rl;
+    }
+    if (tid == 0) s_claim = kPrepThreads;
     __syncthreads();
-    float wbase = 0.f, ctot = 0.f;
-    int clast = -1;
-    for (int w = 0; w < kPrepThreads / 32; ++w) {
-        if (w < warp) wbase += s_wtot[w];
-        ctot += s_wtot[w];
-        clast = max(clast, s_wlast[w]);
-    }
-    const float excl = wbase + incl - tsum;
-    {
-        const unsigned long long mine[2] = {dbl(double(ctot)), dbl(double(clast))};
-        exchange(mine, 2);
-    }
     double total = 0.0;
-    for (int r = 0; r < kCl; ++r) total += all(r, 0);
+    for (int r = 0; r < CL; ++r) total += s_rank[r];
     const double target = double(a.uniforms[size_t(b) * n]) * total;
     // The owner CTA holds the first CDF step above the target (running double sums over the
     // ranks are monotone).  If rounding leaves the target at or above the total, the draw clamps
     // to the last token of positive mass.
-    double base = 0.0;
+    double base = 0.0, rbase = 0.0;
     int owner = -1, last_rank = -1;
-    for (int r = 0; r < kCl; ++r) {
-        if (owner < 0 && target < base + all(r, 0)) owner = r;
-        base += all(r, 0);
-        if (all(r, 1) >= 0.0) last_rank = r;
+    for (int r = 0; r < CL; ++r) {
+        if (owner < 0 && target < base + s_rank[r]) {
+            owner = r;
+            rbase = base;
+        }
+        base += s_rank[r];
+        if (s_rlast[r] >= 0) last_rank = r;
     }
     const bool clamp = owner < 0;
     if (clamp) owner = last_rank;
-    __shared__ int s_claim;
-    if (tid == 0) s_claim = kPrepThreads;
-    __syncthreads();
-    float local = 0.f;
-    if (rank == owner && !clamp) {
-        double rbase = 0.0;
-        for (int r = 0; r < rank; ++r) rbase += all(r, 0);
-        local = float(target - rbase);
-        // the first thread whose run ends above the local target owns the step
-        if (tsum > 0.f && excl + tsum > local) atomicMin(&s_claim, tid);
-    }
+    float wbase = 0.f;
+    if (rank == owner && !clamp)
+        for (int w = 0; w < warp; ++w) wbase += s_part[slot][w].x;  // this CTA's earlier warps
+    const float excl = wbase + incl - tsum;
+    const float local = float(target - rbase);
+    // the first thread whose run ends above the local target owns the step
+    if (rank == owner && !clamp && tsum > 0.f && excl + tsum > local) atomicMin(&s_claim, tid);
     __syncthreads();
     if (rank == owner) {
         if (!clamp && tid == s_claim) {
             float acc = excl;
             int found = tlast;
-            for (int t = t0; t < t1; ++t) {
-                const float r = use_res ? fmaxf(fmaf(-cjf, sq[t], sp[t]), 0.f) : sp[t];
-                acc += r;
-                if (r > 0.f && acc > local) {
-                    found = t;
-                    break;
+            bool done = false;
+#pragma unroll
+            for (int e = 0; e < kE; ++e) {
+                acc += xp[e];
+                if (!done && xp[e] > 0.f && acc > local) {
+                    found = t0 + e;
+                    done = true;
                 }
             }
             a.final_tok[size_t(b) * n + i] = lo + found;
         } else if (tid == 0 && (clamp || s_claim == kPrepThreads)) {
-            a.final_tok[size_t(b) * n + i] = lo + clast;
+            a.final_tok[size_t(b) * n + i] = lo + s_rlast[owner];
         }
     }
     if (owner < 0 && rank == 0 && tid == 0) a.final_tok[size_t(b) * n + i] = 0;  // no positive mass at all
     cluster.sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 
-__global__ void verify_walk_kernel(VerifyArgs a) {
-    const int b = blockIdx.x;
-    if (threadIdx.x != 0) return;
+__global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
+    __shared__ int s_tok[64], s_par[64], s_row[64], s_fin[64];
+    __shared__ float s_u[64], s_ratio[64];
+    __shared__ int s_bad;
+    const int b = blockIdx.x, tid = threadIdx.x;
     const int n = a.n, D = a.D;
-    const int32_t *tok = a.tokens + size_t(b) * n;
-    const int32_t *par = a.parents + size_t(b) * n;
-    const int32_t *row = a.node_row + size_t(b) * n;
-    const float *u = a.uniforms + size_t(b) * n;
-    const float *ratio = a.ratio + size_t(b) * n;
-    const int32_t *fin = a.final_tok + size_t(b) * n;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    if (tid < n) {
+        const size_t o = size_t(b) * n + tid;
+        const int t = a.tokens[o], p = a.parents[o];
+        s_tok[tid] = t;
+        s_par[tid] = p;
+        s_row[tid] = a.node_row[o];
+        s_fin[tid] = a.final_tok[o];
+        s_u[tid] = a.uniforms[o];
+        s_ratio[tid] = a.ratio[o];
+        bool bad = t < 0 || t >= a.V;
+        bad |= tid == 0 ? p != -1 : (p < 0 || p >= tid);
+        if (bad) s_bad = 1;
+    }
+    __syncthreads();
+    if (!a.greedy && tid > 0 && tid < n && !s_bad) {
+        const int p = s_par[tid];
+        if (s_row[p] < 0 || s_row[p] >= a.R) s_bad = 1;
+    }
+    __syncthreads();
     int32_t *ot = a.out_tokens + size_t(b) * (D + 1);
     int32_t *op = a.out_path + size_t(b) * D;
+    if (tid != 0) return;
     for (int j = 0; j <= D; ++j) ot[j] = -1;
     for (int j = 0; j < D; ++j) op[j] = -1;
-
-    bool bad = par[0] != -1;
-    for (int j = 0; j < n; ++j) {
-        if (tok[j] < 0 || tok[j] >= a.V) bad = true;
-        if (j > 0 && (par[j] < 0 || par[j] >= j)) bad = true;
-    }
-    if (!bad && !a.greedy) {
-        for (int j = 1; j < n; ++j) {
-            const int p = par[j];
-            if (row[p] < 0 || row[p] >= a.R) bad = true;
-        }
-    }
-    if (bad) {
+    if (s_bad) {
         set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
         a.out_len[b] = 0;
         return;
@@ -428,25 +453,25 @@ __global__ void verify_walk_kernel(VerifyArgs a) {
     for (;;) {
         int next = -1;
         if (a.greedy) {
-            const int g = fin[node];
+            const int g = s_fin[node];
             for (int j = node + 1; j < n; ++j)
-                if (par[j] == node && tok[j] == g) {
+                if (s_par[j] == node && s_tok[j] == g) {
                     next = j;
                     break;
                 }
         } else {
             for (int j = node + 1; j < n; ++j)
-                if (par[j] == node && u[j] < ratio[j]) {
+                if (s_par[j] == node && s_u[j] < s_ratio[j]) {
                     next = j;
                     break;
                 }
         }
         if (next < 0 || len >= D) {
             if (next >= 0) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);  // tree deeper than D
-            ot[len++] = fin[node];
+            ot[len++] = s_fin[node];
             break;
         }
-        ot[len] = tok[next];
+        ot[len] = s_tok[next];
         op[len] = next;
         ++len;
         node = next;
@@ -461,6 +486,31 @@ size_t tree_verify_workspace_bytes(const eagle_verify_cfg &c) {
     return kWsHeader + align_up(size_t(c.batch) * n * sizeof(float), 256) +
            align_up(size_t(c.batch) * n * sizeof(int32_t), 256);
 }
+
+namespace {
+template <int CL>
+cudaError_t launch_prep(const VerifyArgs &a, int n, int batch, cudaStream_t stream) {
+    static bool attr = false;
+    if (!attr && CL > 8) {
+        cudaError_t e = cudaFuncSetAttribute(verify_prep_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    attr = true;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL, n, batch);
+    cfg.blockDim = dim3(kPrepThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = CL;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, verify_prep_kernel<CL>, a);
+}
+}  // namespace
 
 eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, const float *draft,
                                 const int32_t *tokens, const int32_t *parents, const int32_t *node_row,
@@ -487,32 +537,23 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
     a.V = c.vocab;
     a.R = 1 + (c.depth - 1) * c.topk;
     a.D = c.depth;
-    int slice = (c.vocab + kCl - 1) / kCl;
-    slice = (slice + 3) & ~3;
-    a.slice = slice;
     a.greedy = c.temperature <= 0.f;
     a.inv_t = a.greedy ? 1.f : 1.f / c.temperature;
     a.inv_td = a.greedy ? 1.0 : 1.0 / double(c.temperature);
     a.c = kLog2e * a.inv_t;
-    const size_t smem = a.greedy ? 0 : size_t(2) * slice * sizeof(float);
-    static size_t attr = 0;
-    if (smem > attr) {
-        if (cudaFuncSetAttribute(verify_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-            cudaSuccess)
-            return EAGLE_ERR_CUDA;
-        attr = smem;
-    }
-    dim3 grid(kCl, n, c.batch);
-    verify_prep_kernel<<<grid, kPrepThreads, smem, stream>>>(a);
+    const int per_cta = kPrepThreads * kE;
+    const int cl = c.vocab <= 8 * per_cta ? 8 : 16;
+    int slice = (c.vocab + cl - 1) / cl;
+    slice = (slice + 3) & ~3;
+    a.slice = slice;
+    const cudaError_t e = cl == 8 ? launch_prep<8>(a, n, c.batch, stream) : launch_prep<16>(a, n, c.batch, stream);
+    if (e != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();
-    verify_walk_kernel<<<c.batch, 32, 0, stream>>>(a);
+    verify_walk_kernel<<<c.batch, 64, 0, stream>>>(a);
     note_launch();
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
 
-size_t verify_max_vocab() {
-    // two fp32 slices of V/8 entries must fit the opt-in shared memory of one CTA (227 KB)
-    return size_t(227 * 1024 - 4096) / (2 * sizeof(float)) * kCl;
-}
+size_t verify_max_vocab() { return size_t(16) * kPrepThreads * kE; }
 
 }  // namespace eagle

@@ -19,10 +19,23 @@
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 
 namespace eagle {
+
+struct AttnTcParams {
+    const uint64_t *mask;
+    const int32_t *ctx_len;
+    __nv_bfloat16 *out;
+    int32_t *status;
+    int L, B, n, Hq, Hkv, G, S_max, rows, mgroups;
+    float scale_log2;
+};
+bool tree_attention_tc_supported(int head_dim, int dtype, int G, int S_max);
+eagle_status tree_attention_tc_launch(const AttnTcParams &p, const void *q, const void *k_cache, const void *v_cache,
+                                      const void *k_tree, const void *v_tree, cudaStream_t stream);
 
 struct AttnArgs {
     const void *q, *k_cache, *v_cache, *k_tree, *v_tree;
@@ -374,6 +387,16 @@ eagle_status launch_f32(const AttnArgs &a, cudaStream_t stream) {
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
 
+// EAGLE_ATTN_LEGACY=1 selects the mma.sync kernel (kept as the comparison baseline).
+bool legacy_path() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("EAGLE_ATTN_LEGACY");
+        v = (e && e[0] == '1') ? 1 : 0;
+    }
+    return v == 1;
+}
+
 }  // namespace
 
 size_t tree_attention_workspace_bytes(const eagle_attn_cfg &) { return kWsHeader; }
@@ -403,6 +426,25 @@ eagle_status tree_attention_launch(const eagle_attn_cfg &c, const void *q, const
     a.scale = c.scale > 0.f ? c.scale : 1.f / sqrtf(float(c.head_dim));
     a.scale_log2 = a.scale * kLog2e;
     if (c.dtype == EAGLE_DTYPE_BF16) {
+        if (tree_attention_tc_supported(c.head_dim, c.dtype, a.G, c.max_seq) && !legacy_path()) {
+            AttnTcParams tp;
+            tp.mask = mask;
+            tp.ctx_len = ctx_len;
+            tp.out = static_cast<__nv_bfloat16 *>(out);
+            tp.status = a.status;
+            tp.L = a.L;
+            tp.B = a.B;
+            tp.n = a.n;
+            tp.Hq = a.Hq;
+            tp.Hkv = a.Hkv;
+            tp.G = a.G;
+            tp.S_max = a.S_max;
+            tp.rows = a.rows;
+            tp.mgroups = (a.rows + 255) / 256;
+            tp.scale_log2 = a.scale_log2;
+            const eagle_status st = tree_attention_tc_launch(tp, q, k_cache, v_cache, k_tree, v_tree, stream);
+            if (st != EAGLE_ERR_UNSUPPORTED) return st;
+        }
         return c.head_dim == 128 ? launch_bf16<128>(a, stream) : launch_bf16<64>(a, stream);
     }
     return c.head_dim == 128 ? launch_f32<128>(a, stream) : launch_f32<64>(a, stream);

@@ -1,0 +1,513 @@
+// tree_attention_tc.cu -- tree-masked GQA attention on the 5th-generation tensor cores (sm_103a).
+//
+// Pages: "LLM speculative decoding explained" (hubwiz.com) section 5 -- the flattened tree is
+// scored in one target pass and every candidate sees only its ancestors and the context; and
+// "(EAGLE 2) EAGLE-2 ..." section "Tree Attention Mask".
+//
+// One CTA = one (layer, sequence, KV head) unit and up to two 128-row M-tiles of its query block
+// (row r = node * G + head-in-group).  The context streams through in 64-key tiles; the n <= 64
+// tree keys form one last tile whose visibility is the node's ancestor bit mask.
+//
+//   warp 0     TMA producer: Q once (two 64-column halves per M-tile), then K and V tiles
+//              (128B-swizzled boxes of 64 keys x 64 head dims) through a 3-stage ring.
+//   warp 1     MMA issuer (one thread): S_t = Q_t K^T into TMEM (double-buffered, issued one
+//              tile ahead of the softmax), then O_t += P_t V with P_t from shared memory; TMEM
+//              allocation and release (the whole warp).
+//   warps 4-11 two softmax warpgroups, one per M-tile, one thread per query row: tcgen05.ld of
+//              the S row, mask, scale, base-2 online softmax with lazy rescaling (O in TMEM is
+//              rescaled only when the running max grows by more than 8, i.e. P <= 2^8), P to
+//              shared memory in the K-major swizzled layout, and the final O / l epilogue.
+//
+// Every mbarrier wait is bounded; a wait that runs out records EAGLE_ERR_TIMEOUT in the status
+// word, raises a CTA-wide abort flag that ends every role's loop, and the CTA still drains its
+// issued copies and MMAs (bounded) before releasing TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace eagle {
+
+struct AttnTcParams {  // same layout as the declaration in tree_attention.cu
+    const uint64_t *mask;
+    const int32_t *ctx_len;
+    __nv_bfloat16 *out;
+    int32_t *status;
+    int L, B, n, Hq, Hkv, G, S_max, rows, mgroups;
+    float scale_log2;
+};
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kNkv = 64;                   // keys per tile
+constexpr int kStages = 3;
+constexpr uint32_t kHalf = kNkv * 128;     // one 64-dim half of a K or V tile: 64 rows x 128 B
+constexpr uint32_t kStageBytes = 4 * kHalf;  // K lo, K hi, V lo, V hi
+constexpr uint32_t kQHalf = 128 * 128;     // 128 rows x 128 B
+constexpr uint32_t kQTile = 2 * kQHalf;
+constexpr uint32_t kPTile = 128 * 128;     // 128 rows x 64 keys x 2 B
+constexpr uint32_t kOffK = 2 * kQTile;
+constexpr uint32_t kOffP = kOffK + kStages * kStageBytes;
+constexpr uint32_t kSmemBytes = kOffP + 4 * kPTile;  // 224 KB: P double-buffered per M-tile
+constexpr uint32_t kTmemCols = 512;        // O_0, O_1 (128 each), S[2 M-tiles][2 buffers] (64 each)
+constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait counts as stuck
+
+__device__ __forceinline__ uint32_t sa(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    // start >> 4 [0,14), LBO >> 4 [16,30), SBO >> 4 [32,46), version 1 at bit 46, 128B swizzle (2)
+    return uint64_t((addr >> 4) & 0x3FFF) | (uint64_t((lbo >> 4) & 0x3FFF) << 16) |
+           (uint64_t((sbo >> 4) & 0x3FFF) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+// kind::f16 instruction descriptor: D f32, A and B bf16, K-major A, B K- or MN-major
+constexpr uint32_t idesc(int M, int N, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn) << 16) | (uint32_t(N >> 3) << 17) |
+           (uint32_t(M >> 4) << 24);
+}
+constexpr uint32_t kIdescQK = idesc(128, kNkv, 0);
+constexpr uint32_t kIdescPV = idesc(128, 128, 1);
+
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sa(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(bar)) : "memory");
+}
+__device__ __forceinline__ void tma_3d(const CUtensorMap *map, void *dst, uint64_t *bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(sa(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(sa(bar))
+        : "memory");
+}
+// 16 consecutive TMEM columns of this warp's 32 lanes (no wait)
+__device__ __forceinline__ void tld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tst16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]));
+}
+__device__ __forceinline__ void tst_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t s_full[2][2];
+    uint64_t s_free[2][2];
+    uint64_t p_full[2][2];   // [M-tile][P buffer]
+    uint64_t o_ready[2][2];  // [M-tile][P buffer]: the PV that read this buffer has completed
+    uint64_t drain;
+};
+
+// Bounded wait; gives up (and raises the abort flag) when the CTA aborted or the limit ran out.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                              int32_t *status) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255) == 255 && *abort_flag) return false;
+    }
+    *abort_flag = 1;
+    set_status(status, EAGLE_ERR_TIMEOUT);
+    return false;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, the warp leaves converged.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *status) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag, status);
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap ktmap,
+                        const __grid_constant__ CUtensorMap vtmap, AttnTcParams p) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ Bars bars;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int mg = blockIdx.x % p.mgroups;
+    const int unit = blockIdx.x / p.mgroups;
+    const int g = unit % p.Hkv;
+    const int b = (unit / p.Hkv) % p.B;
+    const int l = unit / (p.Hkv * p.B);
+    const int ctx = p.ctx_len[b];
+    if (ctx < 0 || ctx > p.S_max) {
+        if (tid == 0 && mg == 0 && g == 0) set_status(p.status, EAGLE_ERR_DEVICE_INPUT);
+        return;  // uniform for the CTA: nothing allocated yet
+    }
+    const int row0 = mg * 256;                             // first query row of this CTA
+    const int tm = min(2, (p.rows - row0 + 127) / 128);     // M-tiles in this CTA (1 or 2)
+    const int nctx = (ctx + kNkv - 1) / kNkv;               // context tiles
+    const int ntiles = nctx + 1;                            // + the tree tile
+
+    if (tid == 0) {
+        s_abort = 0;
+        mbar_init(&bars.q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars.kv_full[s], 1);
+            mbar_init(&bars.kv_empty[s], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            for (int q = 0; q < 2; ++q) {
+                mbar_init(&bars.s_full[t][q], 1);
+                mbar_init(&bars.s_free[t][q], 4);
+            }
+            for (int pb = 0; pb < 2; ++pb) {
+                mbar_init(&bars.p_full[t][pb], 4);
+                mbar_init(&bars.o_ready[t][pb], 1);
+            }
+        }
+        mbar_init(&bars.drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sa(&s_tmem)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int *abort_flag = &s_abort;
+
+    int issued = 0;  // producer: K/V tiles whose copies were issued
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            const int zq = (l * p.B + b) * p.n + row0 / p.G;  // first node of this CTA's rows
+            mbar_expect_tx(&bars.q_full, uint32_t(tm) * kQTile);
+            for (int t = 0; t < tm; ++t)
+                for (int h = 0; h < 2; ++h)
+                    tma_3d(&qmap, sm + t * kQTile + h * kQHalf, &bars.q_full, 64 * h, g * p.G, zq + t * (128 / p.G));
+            const int zc = (l * p.B + b) * p.S_max;
+            const int zt = (l * p.B + b) * p.n;
+            for (int j = 0; j < ntiles; ++j) {
+                const int s = j % kStages;
+                if (j >= kStages && !wait_or_abort(&bars.kv_empty[s], ((j / kStages) - 1) & 1, abort_flag, p.status))
+                    break;
+                unsigned char *st = sm + kOffK + s * kStageBytes;
+                mbar_expect_tx(&bars.kv_full[s], kStageBytes);
+                const bool tree = j == nctx;
+                const CUtensorMap *km = tree ? &ktmap : &kmap;
+                const CUtensorMap *vm = tree ? &vtmap : &vmap;
+                const int z = tree ? zt : zc + j * kNkv;
+                tma_3d(km, st, &bars.kv_full[s], 0, g, z);
+                tma_3d(km, st + kHalf, &bars.kv_full[s], 64, g, z);
+                tma_3d(vm, st + 2 * kHalf, &bars.kv_full[s], 0, g, z);
+                tma_3d(vm, st + 3 * kHalf, &bars.kv_full[s], 64, g, z);
+                issued = j + 1;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            bool ok = wait_or_abort(&bars.q_full, 0, abort_flag, p.status);
+            tc_fence_after();
+            auto issue_qk = [&](int j) -> bool {
+                const int s = j % kStages;
+                if (!wait_or_abort(&bars.kv_full[s], (j / kStages) & 1, abort_flag, p.status)) return false;
+                tc_fence_after();
+                const uint32_t kbase = sa(sm + kOffK + s * kStageBytes);
+                for (int t = 0; t < tm; ++t) {
+                    const int q = j & 1;
+                    if (j >= 2 && !wait_or_abort(&bars.s_free[t][q], ((j - 2) >> 1) & 1, abort_flag, p.status))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t qbase = sa(sm + t * kQTile);
+                    const uint32_t dS = tmem + 256 + (t * 2 + q) * kNkv;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
+                        const uint32_t offk = (kk >> 2) * kHalf + (kk & 3) * 32;
+                        umma(dS, sdesc(qbase + off, 16, 1024), sdesc(kbase + offk, 16, 1024), kIdescQK, kk > 0);
+                    }
+                    umma_commit(&bars.s_full[t][q]);
+                }
+                return true;
+            };
+            if (ok) ok = issue_qk(0);
+            for (int j = 0; j < ntiles && ok; ++j) {
+                if (j + 1 < ntiles && !issue_qk(j + 1)) break;
+                const int s = j % kStages;
+                const uint32_t vbase = sa(sm + kOffK + s * kStageBytes + 2 * kHalf);
+                for (int t = 0; t < tm && ok; ++t) {
+                    const int pb = j & 1;
+                    if (!wait_or_abort(&bars.p_full[t][pb], (j >> 1) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t pbase = sa(sm + kOffP + (t * 2 + pb) * kPTile);
+                    const uint32_t dO = tmem + t * 128;
+#pragma unroll
+                    for (int kk = 0; kk < kNkv / 16; ++kk)
+                        umma(dO, sdesc(pbase + kk * 32, 16, 1024), sdesc(vbase + kk * 2048, kHalf, 1024), kIdescPV,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&bars.o_ready[t][pb]);
+                }
+                if (!ok) break;
+                umma_commit(&bars.kv_empty[s]);
+            }
+            // drain: every MMA issued by this thread has completed once `drain` completes
+            umma_commit(&bars.drain);
+            for (uint32_t it = 0; it < kWaitLimit && !mbar_try_wait(&bars.drain, 0); ++it) {
+            }
+        }
+    } else if (warp >= 4 && warp - 4 < 4 * tm) {
+        // ---------------- softmax warpgroup t ----------------
+        const int t = (warp - 4) >> 2;
+        const int wq = warp & 3;  // TMEM lane quarter of this warp
+        const int rho = wq * 32 + lane;
+        const int r = row0 + t * 128 + rho;
+        const bool valid = r < p.rows;
+        const int node = valid ? r / p.G : 0;
+        const int gh = valid ? r % p.G : 0;
+        const uint64_t tmask = valid ? p.mask[size_t(b) * p.n + node] : 0ull;
+        const uint32_t lane_off = uint32_t(wq * 32) << 16;
+        const float c = p.scale_log2;
+        float m_raw = -INFINITY;  // reference max in raw score units (P = 2^((s - m_raw) c))
+        float l_sum = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int q = j & 1;
+            if (!warp_wait(&bars.s_full[t][q], (j >> 1) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            float sv[kNkv];
+            {
+                uint32_t raw[kNkv];
+                uint32_t (&r0)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw);
+                uint32_t (&r1)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 16);
+                uint32_t (&r2)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 32);
+                uint32_t (&r3)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 48);
+                const uint32_t tS = tmem + lane_off + 256 + (t * 2 + q) * kNkv;
+                tld16(tS, r0);
+                tld16(tS + 16, r1);
+                tld16(tS + 32, r2);
+                tld16(tS + 48, r3);
+                tld_wait();
+#pragma unroll
+                for (int cc = 0; cc < kNkv; ++cc) sv[cc] = __uint_as_float(raw[cc]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.s_free[t][q]);  // S buffer q may be overwritten now
+            // masking: only the context tail tile and the tree tile have invisible keys
+            const bool tree = j == nctx;
+            const int kvalid = tree ? p.n : min(kNkv, ctx - j * kNkv);
+            if (tree || kvalid < kNkv) {
+#pragma unroll
+                for (int cc = 0; cc < kNkv; ++cc) {
+                    bool vis = cc < kvalid;
+                    if (tree) vis = vis && ((tmask >> cc) & 1ull);
+                    if (!vis) sv[cc] = -INFINITY;
+                }
+            }
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int cc = 0; cc < kNkv; cc += 4) {
+                mx0 = fmaxf(mx0, sv[cc]);
+                mx1 = fmaxf(mx1, sv[cc + 1]);
+                mx2 = fmaxf(mx2, sv[cc + 2]);
+                mx3 = fmaxf(mx3, sv[cc + 3]);
+            }
+            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            // lazy rescale: the reference moves only when the row max exceeds it by more than 8
+            // in base-2 units, so every P stays below 2^8
+            const bool rescale = (mx - m_raw) * c > 8.f;
+            float alpha = 1.f;
+            if (rescale) {
+                alpha = m_raw == -INFINITY ? 0.f : fast_exp2((m_raw - mx) * c);
+                m_raw = mx;
+            }
+            const float mc = m_raw == -INFINITY ? 0.f : m_raw * c;
+            float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+            uint32_t pk[kNkv / 2];
+#pragma unroll
+            for (int cc = 0; cc < kNkv; cc += 4) {
+                const float p0 = fast_exp2(fmaf(sv[cc], c, -mc));
+                const float p1 = fast_exp2(fmaf(sv[cc + 1], c, -mc));
+                const float p2 = fast_exp2(fmaf(sv[cc + 2], c, -mc));
+                const float p3 = fast_exp2(fmaf(sv[cc + 3], c, -mc));
+                ps0 += p0;
+                ps1 += p1;
+                ps2 += p2;
+                ps3 += p3;
+                __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
+                __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
+                pk[cc / 2] = *reinterpret_cast<uint32_t *>(&h0);
+                pk[cc / 2 + 1] = *reinterpret_cast<uint32_t *>(&h1);
+            }
+            l_sum = l_sum * alpha + ((ps0 + ps1) + (ps2 + ps3));
+            // O_t must be final before it is rescaled (PV of tile j-1 complete); P buffer (j & 1)
+            // is free once the PV of tile j-2 is complete
+            // (each o_ready[t][pb] completes once per use of P buffer pb: tiles pb, pb + 2, ...; the
+            // awaited phase is always that barrier's most recent one, so its parity cannot alias)
+            if (rescale && j > 0) {
+                if (!warp_wait(&bars.o_ready[t][(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tO = tmem + lane_off + t * 128;
+#pragma unroll
+                for (int cc = 0; cc < 128; cc += 16) {
+                    uint32_t o[16];
+                    tld16(tO + cc, o);
+                    tld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tst16(tO + cc, o);
+                }
+                tst_wait();
+            } else if (j >= 2) {
+                if (!warp_wait(&bars.o_ready[t][j & 1], ((j - 2) >> 1) & 1, abort_flag, p.status)) {  // PV(j-2)
+                    ok = false;
+                    break;
+                }
+            }
+            unsigned char *prow = sm + kOffP + (t * 2 + (j & 1)) * kPTile + rho * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint4 v = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                *reinterpret_cast<uint4 *>(prow + ((ch ^ (rho & 7)) << 4)) = v;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.p_full[t][j & 1]);
+        }
+        // epilogue: O / l to global, bf16
+        if (ok && warp_wait(&bars.o_ready[t][(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag, p.status)) {
+            tc_fence_after();
+            const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            __nv_bfloat16 *orow = p.out + ((((size_t)l * p.B + b) * p.n + node) * p.Hq + g * p.G + gh) * 128;
+            const uint32_t tO = tmem + lane_off + t * 128;
+#pragma unroll
+            for (int c = 0; c < 128; c += 16) {
+                uint32_t o[16];
+                tld16(tO + c, o);
+                tld_wait();
+                uint32_t w[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
+                                                             __uint_as_float(o[2 * e + 1]) * inv);
+                    w[e] = *reinterpret_cast<uint32_t *>(&h);
+                }
+                if (valid) {
+                    reinterpret_cast<uint4 *>(orow + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    reinterpret_cast<uint4 *>(orow + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+        }
+    }
+
+    // teardown: let every issued TMA copy land before the shared memory is given up
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+        // the last copy issued into each stage has landed (already true unless the CTA aborted)
+        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+            for (uint32_t it = 0; it < kWaitLimit && !mbar_try_wait(&bars.kv_full[j % kStages], (j / kStages) & 1);
+                 ++it) {
+            }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 3-D map over a [outer][mid][128] bf16 tensor with a {64, box_mid, box_outer} 128B-swizzled box
+bool make_map(CUtensorMap *map, const void *base, uint64_t mid, uint64_t outer, uint32_t box_mid,
+              uint32_t box_outer) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, mid, outer};
+    cuuint64_t strides[2] = {128 * 2, mid * 128 * 2};
+    cuuint32_t box[3] = {64, box_mid, box_outer};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// True when the tensor-core kernel handles this configuration.
+bool tree_attention_tc_supported(int head_dim, int dtype, int G, int S_max) {
+    return dtype == EAGLE_DTYPE_BF16 && head_dim == 128 && G >= 1 && 128 % G == 0 && S_max >= 1 &&
+           encode_fn() != nullptr;
+}
+
+eagle_status tree_attention_tc_launch(const AttnTcParams &p, const void *q, const void *k_cache, const void *v_cache,
+                                      const void *k_tree, const void *v_tree, cudaStream_t stream) {
+    CUtensorMap qm, km, vm, ktm, vtm;
+    const uint64_t LB = uint64_t(p.L) * p.B;
+    if (!make_map(&qm, q, p.Hq, LB * p.n, p.G, 128 / p.G) || !make_map(&km, k_cache, p.Hkv, LB * p.S_max, 1, kNkv) ||
+        !make_map(&vm, v_cache, p.Hkv, LB * p.S_max, 1, kNkv) || !make_map(&ktm, k_tree, p.Hkv, LB * p.n, 1, kNkv) ||
+        !make_map(&vtm, v_tree, p.Hkv, LB * p.n, 1, kNkv))
+        return EAGLE_ERR_UNSUPPORTED;  // the caller falls back to the mma.sync kernel
+    static bool attr = false;
+    const size_t smem = kSmemBytes + 1024;
+    if (!attr) {
+        if (cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+            cudaSuccess)
+            return EAGLE_ERR_CUDA;
+        attr = true;
+    }
+    const long grid = long(p.L) * p.B * p.Hkv * p.mgroups;
+    tree_attn_tc_kernel<<<unsigned(grid), kThreads, smem, stream>>>(qm, km, vm, ktm, vtm, p);
+    note_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
+}
+
+}  // namespace eagle

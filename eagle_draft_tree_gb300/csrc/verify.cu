@@ -238,22 +238,22 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
                 Mp = fmaxf(Mp, __shfl_xor_sync(0xffffffffu, Mp, off));
                 Mq = fmaxf(Mq, __shfl_xor_sync(0xffffffffu, Mq, off));
             }
-            double Sp = 0.0, Sq = 0.0;
+            FF Sp, Sq;
 #pragma unroll
             for (int h = 0; h < kParts / 32; ++h) {
-                if (v[h].x != -INFINITY) Sp += double(v[h].y) * double(exp2f((v[h].x - Mp) * c));
-                if (v[h].z != -INFINITY) Sq += double(v[h].w) * double(exp2f((v[h].z - Mq) * c));
+                FF tp, tq;
+                tp.hi = v[h].x != -INFINITY ? v[h].y * exp2f((v[h].x - Mp) * c) : 0.f;
+                tq.hi = v[h].z != -INFINITY ? v[h].w * exp2f((v[h].z - Mq) * c) : 0.f;
+                Sp = ff_add(Sp, tp);
+                Sq = ff_add(Sq, tq);
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                Sp += __shfl_xor_sync(0xffffffffu, Sp, off);
-                Sq += __shfl_xor_sync(0xffffffffu, Sq, off);
-            }
+            Sp = ff_warp_sum(Sp);
+            Sq = ff_warp_sum(Sq);
             if (lane == 0) {
                 s_M[0] = Mp;
                 s_M[1] = Mq;
-                s_lnS[0] = log(Sp);
-                s_lnS[1] = has_q ? log(Sq) : 0.0;
+                s_lnS[0] = log_fast(ff_to_double(Sp));
+                s_lnS[1] = has_q ? log_fast(ff_to_double(Sq)) : 0.0;
             }
         }
         __syncthreads();
@@ -292,12 +292,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
         const int slot = publish(make_float4(part, 0.f, 0.f, 0.f));
         if (warp == 0) {
-            double S = 0.0;
+            FF S;
 #pragma unroll
-            for (int h = 0; h < kParts / 32; ++h) S += double(fetch(slot, lane + 32 * h).x);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
-            if (lane == 0) s_tot = S;
+            for (int h = 0; h < kParts / 32; ++h) {
+                FF t;
+                t.hi = fetch(slot, lane + 32 * h).x;
+                S = ff_add(S, t);
+            }
+            S = ff_warp_sum(S);
+            if (lane == 0) s_tot = ff_to_double(S);
         }
         __syncthreads();
         const double Sn = s_tot;

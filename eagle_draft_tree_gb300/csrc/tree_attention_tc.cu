@@ -9,14 +9,19 @@
 // tree keys form one last tile whose visibility is the node's ancestor bit mask.
 //
 //   warp 0     TMA producer: Q once (two 64-column halves per M-tile), then K and V tiles
-//              (128B-swizzled boxes of 64 keys x 64 head dims) through a 3-stage ring.
-//   warp 1     MMA issuer (one thread): S_t = Q_t K^T into TMEM (double-buffered, issued one
-//              tile ahead of the softmax), then O_t += P_t V with P_t from shared memory; TMEM
-//              allocation and release (the whole warp).
+//              (128B-swizzled boxes of 64 keys x 64 head dims) through two rings: K tiles are
+//              released right after QK^T has read them (2 stages), V tiles after PV (4 stages),
+//              so the longer-lived V tiles get the deeper ring.  Loads issue whenever a stage is
+//              free (non-blocking polls of both rings).
+//   warp 1     MMA issuer (one thread), a state machine over non-blocking barrier tests: S_t =
+//              Q_t K^T into TMEM (double-buffered, up to two tiles ahead of PV) and O_t += P_t V
+//              with P_t read from TMEM (A operand in tensor memory), each issued as soon as its
+//              operands are ready; TMEM allocation and release (the whole warp).
 //   warps 4-11 two softmax warpgroups, one per M-tile, one thread per query row: tcgen05.ld of
 //              the S row, mask, scale, base-2 online softmax with lazy rescaling (O in TMEM is
-//              rescaled only when the running max grows by more than 8, i.e. P <= 2^8), P to
-//              shared memory in the K-major swizzled layout, and the final O / l epilogue.
+//              rescaled only when the running max grows by more than 8, i.e. P <= 2^8), P packed
+//              to bf16 pairs and stored over the row's own S columns, and the final O / l epilogue.
+//              Keeping P out of shared memory leaves 160 KB for the K and V rings.
 //
 // Every mbarrier wait is bounded; a wait that runs out records EAGLE_ERR_TIMEOUT in the status
 // word, raises a CTA-wide abort flag that ends every role's loop, and the CTA still drains its
@@ -45,16 +50,18 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kNkv = 64;                   // keys per tile
-constexpr int kStages = 3;
+constexpr int kKStages = 4;                // K tiles are released as soon as QK^T has read them
+constexpr int kVStages = 6;                // V tiles are held until PV, later in the tile's life
 constexpr uint32_t kHalf = kNkv * 128;     // one 64-dim half of a K or V tile: 64 rows x 128 B
-constexpr uint32_t kStageBytes = 4 * kHalf;  // K lo, K hi, V lo, V hi
+constexpr uint32_t kTileBytes = 2 * kHalf;  // a K (or V) tile: both halves
 constexpr uint32_t kQHalf = 128 * 128;     // 128 rows x 128 B
 constexpr uint32_t kQTile = 2 * kQHalf;
-constexpr uint32_t kPTile = 128 * 128;     // 128 rows x 64 keys x 2 B
 constexpr uint32_t kOffK = 2 * kQTile;
-constexpr uint32_t kOffP = kOffK + kStages * kStageBytes;
-constexpr uint32_t kSmemBytes = kOffP + 4 * kPTile;  // 224 KB: P double-buffered per M-tile
-constexpr uint32_t kTmemCols = 512;        // O_0, O_1 (128 each), S[2 M-tiles][2 buffers] (64 each)
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+constexpr uint32_t kSmemBytes = kOffV + kVStages * kTileBytes;  // 224 KB
+// TMEM: O_0, O_1 (128 columns each), then S[2 M-tiles][2 buffers] (64 columns each); the bf16 P of
+// a tile is written over the first 32 columns of its own S buffer and read from there by PV
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait counts as stuck
 
 __device__ __forceinline__ uint32_t sa(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -70,12 +77,18 @@ constexpr uint32_t idesc(int M, int N, int b_mn) {
            (uint32_t(M >> 4) << 24);
 }
 constexpr uint32_t kIdescQK = idesc(128, kNkv, 0);
-constexpr uint32_t kIdescPV = idesc(128, 128, 1);
+constexpr uint32_t kIdescPV = idesc(128, 128, 1);  // A = P from TMEM, B = V MN-major
 
 __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
         "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+// A from TMEM (K-major, two bf16 per 32-bit column), B from shared memory
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
 }
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sa(bar))
@@ -85,6 +98,14 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(bar)) : "memory");
+}
+// One 4-D box: both 64-dim halves of kNkv rows of one KV head; lands as [half][row][128 B].
+__device__ __forceinline__ void tma_kv(const CUtensorMap *map, void *dst, uint64_t *bar, int row, int head) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(sa(dst)),
+        "l"(map), "r"(0), "r"(row), "r"(0), "r"(head), "r"(sa(bar))
+        : "memory");
 }
 __device__ __forceinline__ void tma_3d(const CUtensorMap *map, void *dst, uint64_t *bar, int x, int y, int z) {
     asm volatile(
@@ -113,12 +134,11 @@ __device__ __forceinline__ void tst_wait() { asm volatile("tcgen05.wait::st.sync
 
 struct Bars {
     uint64_t q_full;
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
-    uint64_t s_full[2][2];
-    uint64_t s_free[2][2];
-    uint64_t p_full[2][2];   // [M-tile][P buffer]
-    uint64_t o_ready[2][2];  // [M-tile][P buffer]: the PV that read this buffer has completed
+    uint64_t k_full[kKStages], k_empty[kKStages];
+    uint64_t v_full[kVStages], v_empty[kVStages];
+    uint64_t s_full[2][2];   // [M-tile][S buffer]: QK^T of the buffer's tile landed
+    uint64_t p_full[2][2];   // [M-tile][S buffer]: P of the buffer's tile written over S
+    uint64_t o_ready[2][2];  // [M-tile][S buffer]: the PV that read this buffer's P has completed
     uint64_t drain;
 };
 
@@ -133,6 +153,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     set_status(status, EAGLE_ERR_TIMEOUT);
     return false;
 }
+
+// Non-blocking test of a phase (state-machine roles poll several barriers alternately).
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(sa(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+constexpr uint32_t kSpinLimit = 1u << 26;  // polls without progress before a role counts as stuck
 
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, the warp leaves converged.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *status) {
@@ -172,18 +204,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         s_abort = 0;
         mbar_init(&bars.q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars.kv_full[s], 1);
-            mbar_init(&bars.kv_empty[s], 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.k_empty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&bars.v_full[s], 1);
+            mbar_init(&bars.v_empty[s], 1);
         }
         for (int t = 0; t < 2; ++t) {
             for (int q = 0; q < 2; ++q) {
                 mbar_init(&bars.s_full[t][q], 1);
-                mbar_init(&bars.s_free[t][q], 4);
-            }
-            for (int pb = 0; pb < 2; ++pb) {
-                mbar_init(&bars.p_full[t][pb], 4);
-                mbar_init(&bars.o_ready[t][pb], 1);
+                mbar_init(&bars.p_full[t][q], 4);
+                mbar_init(&bars.o_ready[t][q], 1);
             }
         }
         mbar_init(&bars.drain, 1);
@@ -200,9 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = s_tmem;
     volatile int *abort_flag = &s_abort;
 
-    int issued = 0;  // producer: K/V tiles whose copies were issued
+    int k_issued = 0, v_issued = 0;  // producer: K / V tiles whose copies were issued
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
+        // ---------------- TMA producer: two rings, issued whenever a stage is free ----------------
         if (lane == 0) {
             const int zq = (l * p.B + b) * p.n + row0 / p.G;  // first node of this CTA's rows
             mbar_expect_tx(&bars.q_full, uint32_t(tm) * kQTile);
@@ -211,72 +244,115 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_3d(&qmap, sm + t * kQTile + h * kQHalf, &bars.q_full, 64 * h, g * p.G, zq + t * (128 / p.G));
             const int zc = (l * p.B + b) * p.S_max;
             const int zt = (l * p.B + b) * p.n;
-            for (int j = 0; j < ntiles; ++j) {
-                const int s = j % kStages;
-                if (j >= kStages && !wait_or_abort(&bars.kv_empty[s], ((j / kStages) - 1) & 1, abort_flag, p.status))
+            uint32_t spins = 0;
+            while (k_issued < ntiles || v_issued < ntiles) {
+                bool prog = false;
+                // K tiles feed QK^T, the critical path: they go first; a V tile is issued only when
+                // the K ring cannot take another tile (the TMA engine serves boxes in order)
+                if (k_issued < ntiles) {
+                    const int j = k_issued, s = j % kKStages;
+                    if (j < kKStages || mbar_test(&bars.k_empty[s], ((j / kKStages) - 1) & 1)) {
+                        const bool tree = j == nctx;
+                        const CUtensorMap *m = tree ? &ktmap : &kmap;
+                        const int z = tree ? zt : zc + j * kNkv;
+                        unsigned char *st = sm + kOffK + s * kTileBytes;
+                        mbar_expect_tx(&bars.k_full[s], kTileBytes);
+                        tma_kv(m, st, &bars.k_full[s], z, g);
+                        ++k_issued;
+                        prog = true;
+                    }
+                }
+                if (!prog && v_issued < k_issued) {
+                    const int j = v_issued, s = j % kVStages;
+                    if (j < kVStages || mbar_test(&bars.v_empty[s], ((j / kVStages) - 1) & 1)) {
+                        const bool tree = j == nctx;
+                        const CUtensorMap *m = tree ? &vtmap : &vmap;
+                        const int z = tree ? zt : zc + j * kNkv;
+                        unsigned char *st = sm + kOffV + s * kTileBytes;
+                        mbar_expect_tx(&bars.v_full[s], kTileBytes);
+                        tma_kv(m, st, &bars.v_full[s], z, g);
+                        ++v_issued;
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    spins = 0;
+                } else if (++spins >= kSpinLimit || ((spins & 255) == 0 && *abort_flag)) {
+                    if (spins >= kSpinLimit) {
+                        *abort_flag = 1;
+                        set_status(p.status, EAGLE_ERR_TIMEOUT);
+                    }
                     break;
-                unsigned char *st = sm + kOffK + s * kStageBytes;
-                mbar_expect_tx(&bars.kv_full[s], kStageBytes);
-                const bool tree = j == nctx;
-                const CUtensorMap *km = tree ? &ktmap : &kmap;
-                const CUtensorMap *vm = tree ? &vtmap : &vmap;
-                const int z = tree ? zt : zc + j * kNkv;
-                tma_3d(km, st, &bars.kv_full[s], 0, g, z);
-                tma_3d(km, st + kHalf, &bars.kv_full[s], 64, g, z);
-                tma_3d(vm, st + 2 * kHalf, &bars.kv_full[s], 0, g, z);
-                tma_3d(vm, st + 3 * kHalf, &bars.kv_full[s], 64, g, z);
-                issued = j + 1;
+                }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+        // ---------------- MMA issuer: QK^T and PV issued in whatever order they become ready ----
         if (lane == 0) {
             bool ok = wait_or_abort(&bars.q_full, 0, abort_flag, p.status);
             tc_fence_after();
-            auto issue_qk = [&](int j) -> bool {
-                const int s = j % kStages;
-                if (!wait_or_abort(&bars.kv_full[s], (j / kStages) & 1, abort_flag, p.status)) return false;
-                tc_fence_after();
-                const uint32_t kbase = sa(sm + kOffK + s * kStageBytes);
-                for (int t = 0; t < tm; ++t) {
-                    const int q = j & 1;
-                    if (j >= 2 && !wait_or_abort(&bars.s_free[t][q], ((j - 2) >> 1) & 1, abort_flag, p.status))
-                        return false;
-                    tc_fence_after();
-                    const uint32_t qbase = sa(sm + t * kQTile);
-                    const uint32_t dS = tmem + 256 + (t * 2 + q) * kNkv;
+            int nq = 0, npv = 0, pv_t = 0;
+            uint32_t spins = 0;
+            while (ok && npv < ntiles) {
+                bool prog = false;
+                // S_t(nq) = Q_t K(nq)^T: K landed, and the PV that read S buffer nq & 1 (tile nq - 2,
+                // whose P lives there) has completed for every M-tile
+                if (nq < ntiles && nq < npv + 2) {
+                    const int s = nq % kKStages, q = nq & 1;
+                    bool ready = mbar_test(&bars.k_full[s], (nq / kKStages) & 1);
+                    for (int t = 0; t < tm && ready && nq >= 2; ++t)
+                        ready = mbar_test(&bars.o_ready[t][q], ((nq - 2) >> 1) & 1);
+                    if (ready) {
+                        tc_fence_after();
+                        const uint32_t kbase = sa(sm + kOffK + s * kTileBytes);
+                        for (int t = 0; t < tm; ++t) {
+                            const uint32_t qbase = sa(sm + t * kQTile);
+                            const uint32_t dS = tmem + 256 + (t * 2 + q) * kNkv;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
-                        const uint32_t offk = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        umma(dS, sdesc(qbase + off, 16, 1024), sdesc(kbase + offk, 16, 1024), kIdescQK, kk > 0);
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
+                                const uint32_t offk = (kk >> 2) * kHalf + (kk & 3) * 32;
+                                umma(dS, sdesc(qbase + off, 16, 1024), sdesc(kbase + offk, 16, 1024), kIdescQK,
+                                     kk > 0);
+                            }
+                            umma_commit(&bars.s_full[t][q]);
+                        }
+                        umma_commit(&bars.k_empty[s]);
+                        ++nq;
+                        prog = true;
                     }
-                    umma_commit(&bars.s_full[t][q]);
                 }
-                return true;
-            };
-            if (ok) ok = issue_qk(0);
-            for (int j = 0; j < ntiles && ok; ++j) {
-                if (j + 1 < ntiles && !issue_qk(j + 1)) break;
-                const int s = j % kStages;
-                const uint32_t vbase = sa(sm + kOffK + s * kStageBytes + 2 * kHalf);
-                for (int t = 0; t < tm && ok; ++t) {
-                    const int pb = j & 1;
-                    if (!wait_or_abort(&bars.p_full[t][pb], (j >> 1) & 1, abort_flag, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t pbase = sa(sm + kOffP + (t * 2 + pb) * kPTile);
-                    const uint32_t dO = tmem + t * 128;
+                // O_t += P_t(npv) V(npv): V landed and P_t written (in TMEM, over S)
+                if (npv < nq) {
+                    const int sv = npv % kVStages, pb = npv & 1;
+                    if (mbar_test(&bars.v_full[sv], (npv / kVStages) & 1) &&
+                        mbar_test(&bars.p_full[pv_t][pb], (npv >> 1) & 1)) {
+                        tc_fence_after();
+                        const uint32_t vbase = sa(sm + kOffV + sv * kTileBytes);
+                        const uint32_t aP = tmem + 256 + (pv_t * 2 + pb) * kNkv;
+                        const uint32_t dO = tmem + pv_t * 128;
 #pragma unroll
-                    for (int kk = 0; kk < kNkv / 16; ++kk)
-                        umma(dO, sdesc(pbase + kk * 32, 16, 1024), sdesc(vbase + kk * 2048, kHalf, 1024), kIdescPV,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&bars.o_ready[t][pb]);
+                        for (int kk = 0; kk < kNkv / 16; ++kk)
+                            umma_ts(dO, aP + kk * 8, sdesc(vbase + kk * 2048, kHalf, 1024), kIdescPV,
+                                    (npv > 0 || kk > 0) ? 1u : 0u);
+                        umma_commit(&bars.o_ready[pv_t][pb]);
+                        if (++pv_t == tm) {
+                            umma_commit(&bars.v_empty[sv]);
+                            pv_t = 0;
+                            ++npv;
+                        }
+                        prog = true;
+                    }
                 }
-                if (!ok) break;
-                umma_commit(&bars.kv_empty[s]);
+                if (prog) {
+                    spins = 0;
+                } else if (++spins >= kSpinLimit || ((spins & 255) == 0 && *abort_flag)) {
+                    if (spins >= kSpinLimit) {
+                        *abort_flag = 1;
+                        set_status(p.status, EAGLE_ERR_TIMEOUT);
+                    }
+                    ok = false;
+                }
             }
             // drain: every MMA issued by this thread has completed once `drain` completes
             umma_commit(&bars.drain);
@@ -321,9 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int cc = 0; cc < kNkv; ++cc) sv[cc] = __uint_as_float(raw[cc]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.s_free[t][q]);  // S buffer q may be overwritten now
             // masking: only the context tail tile and the tree tile have invisible keys
             const bool tree = j == nctx;
             const int kvalid = tree ? p.n : min(kNkv, ctx - j * kNkv);
@@ -371,10 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[cc / 2 + 1] = *reinterpret_cast<uint32_t *>(&h1);
             }
             l_sum = l_sum * alpha + ((ps0 + ps1) + (ps2 + ps3));
-            // O_t must be final before it is rescaled (PV of tile j-1 complete); P buffer (j & 1)
-            // is free once the PV of tile j-2 is complete
-            // (each o_ready[t][pb] completes once per use of P buffer pb: tiles pb, pb + 2, ...; the
-            // awaited phase is always that barrier's most recent one, so its parity cannot alias)
+            // O_t must be final before it is rescaled (PV of tile j-1 complete).  o_ready[t][q]
+            // completes once per use of S buffer q (tiles q, q + 2, ...); the awaited phase is always
+            // that barrier's most recent one, so its parity cannot alias.
             if (rescale && j > 0) {
                 if (!warp_wait(&bars.o_ready[t][(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) {
                     ok = false;
@@ -392,22 +464,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tst16(tO + cc, o);
                 }
                 tst_wait();
-            } else if (j >= 2) {
-                if (!warp_wait(&bars.o_ready[t][j & 1], ((j - 2) >> 1) & 1, abort_flag, p.status)) {  // PV(j-2)
-                    ok = false;
-                    break;
-                }
             }
-            unsigned char *prow = sm + kOffP + (t * 2 + (j & 1)) * kPTile + rho * 128;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint4 v = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                *reinterpret_cast<uint4 *>(prow + ((ch ^ (rho & 7)) << 4)) = v;
+            // P (bf16 pairs) over the first 32 columns of this tile's S buffer
+            {
+                const uint32_t tP = tmem + lane_off + 256 + (t * 2 + q) * kNkv;
+                uint32_t (&p0)[16] = *reinterpret_cast<uint32_t(*)[16]>(pk);
+                uint32_t (&p1)[16] = *reinterpret_cast<uint32_t(*)[16]>(pk + 16);
+                tst16(tP, p0);
+                tst16(tP + 16, p1);
+                tst_wait();
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.p_full[t][j & 1]);
+            if (lane == 0) mbar_arrive(&bars.p_full[t][q]);
         }
         // epilogue: O / l to global, bf16
         if (ok && warp_wait(&bars.o_ready[t][(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag, p.status)) {
@@ -440,8 +509,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 0 && lane == 0) {
         // the last copy issued into each stage has landed (already true unless the CTA aborted)
-        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-            for (uint32_t it = 0; it < kWaitLimit && !mbar_try_wait(&bars.kv_full[j % kStages], (j / kStages) & 1);
+        for (int j = k_issued > kKStages ? k_issued - kKStages : 0; j < k_issued; ++j)
+            for (uint32_t it = 0; it < kWaitLimit && !mbar_try_wait(&bars.k_full[j % kKStages], (j / kKStages) & 1);
+                 ++it) {
+            }
+        for (int j = v_issued > kVStages ? v_issued - kVStages : 0; j < v_issued; ++j)
+            for (uint32_t it = 0; it < kWaitLimit && !mbar_try_wait(&bars.v_full[j % kVStages], (j / kVStages) & 1);
                  ++it) {
             }
     }
@@ -480,6 +553,20 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t mid, uint64_t outer, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over a [rows][heads][128] bf16 tensor seen as {64 elems, rows, 2 halves, heads} (strides
+// out of order) with a {64, kNkv, 2, 1} 128B-swizzled box: one box = both halves of kNkv rows.
+bool make_kv_map(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {64, rows, 2, heads};
+    cuuint64_t strides[3] = {heads * 128 * 2, 128, 128 * 2};
+    cuuint32_t box[4] = {64, kNkv, 2, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 // True when the tensor-core kernel handles this configuration.
@@ -492,9 +579,9 @@ eagle_status tree_attention_tc_launch(const AttnTcParams &p, const void *q, cons
                                       const void *k_tree, const void *v_tree, cudaStream_t stream) {
     CUtensorMap qm, km, vm, ktm, vtm;
     const uint64_t LB = uint64_t(p.L) * p.B;
-    if (!make_map(&qm, q, p.Hq, LB * p.n, p.G, 128 / p.G) || !make_map(&km, k_cache, p.Hkv, LB * p.S_max, 1, kNkv) ||
-        !make_map(&vm, v_cache, p.Hkv, LB * p.S_max, 1, kNkv) || !make_map(&ktm, k_tree, p.Hkv, LB * p.n, 1, kNkv) ||
-        !make_map(&vtm, v_tree, p.Hkv, LB * p.n, 1, kNkv))
+    if (!make_map(&qm, q, p.Hq, LB * p.n, p.G, 128 / p.G) || !make_kv_map(&km, k_cache, p.Hkv, LB * p.S_max) ||
+        !make_kv_map(&vm, v_cache, p.Hkv, LB * p.S_max) || !make_kv_map(&ktm, k_tree, p.Hkv, LB * p.n) ||
+        !make_kv_map(&vtm, v_tree, p.Hkv, LB * p.n))
         return EAGLE_ERR_UNSUPPORTED;  // the caller falls back to the mma.sync kernel
     static bool attr = false;
     const size_t smem = kSmemBytes + 1024;

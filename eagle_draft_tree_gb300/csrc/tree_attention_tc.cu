@@ -8,20 +8,23 @@
 // (row r = node * G + head-in-group).  The context streams through in 64-key tiles; the n <= 64
 // tree keys form one last tile whose visibility is the node's ancestor bit mask.
 //
-//   warp 0     TMA producer: Q once (two 64-column halves per M-tile), then K and V tiles
-//              (128B-swizzled boxes of 64 keys x 64 head dims) through two rings: K tiles are
-//              released right after QK^T has read them (2 stages), V tiles after PV (4 stages),
-//              so the longer-lived V tiles get the deeper ring.  Loads issue whenever a stage is
-//              free (non-blocking polls of both rings).
-//   warp 1     MMA issuer (one thread), a state machine over non-blocking barrier tests: S_t =
-//              Q_t K^T into TMEM (double-buffered, up to two tiles ahead of PV) and O_t += P_t V
-//              with P_t read from TMEM (A operand in tensor memory), each issued as soon as its
-//              operands are ready; TMEM allocation and release (the whole warp).
+//   warp 0     TMA producer: Q once (two 64-column halves per M-tile), then K and V tiles (one
+//              4-D box per tile: 64 keys x both 64-dim halves, 128B-swizzled) through two rings:
+//              K tiles are released right after QK^T has read them (4 stages), V tiles after PV
+//              (6 stages), issued in a fixed order K(j), V(j), each as soon as its stage is free.
+//   warps 1-2  MMA issuers, warp 1 + t for M-tile t (each whole warp follows a fixed schedule with
+//              blocking waits; one elected lane issues): S_t = Q_t K^T into TMEM as soon as the
+//              softmax has read the previous S_t, and O_t += P_t V with P_t read from TMEM (A
+//              operand in tensor memory).  S_t is
+//              single-buffered and P_t double-buffered, so the QK^T of tile j + 1 runs while the
+//              softmax of tile j is still computing, and the PVs trail off the critical path.
 //   warps 4-11 two softmax warpgroups, one per M-tile, one thread per query row: tcgen05.ld of
-//              the S row, mask, scale, base-2 online softmax with lazy rescaling (O in TMEM is
-//              rescaled only when the running max grows by more than 8, i.e. P <= 2^8), P packed
-//              to bf16 pairs and stored over the row's own S columns, and the final O / l epilogue.
-//              Keeping P out of shared memory leaves 160 KB for the K and V rings.
+//              the S row (then S_t is handed back), mask, scale, base-2 online softmax with lazy
+//              rescaling (O in TMEM is rescaled only when the running max grows by more than 8,
+//              i.e. P <= 2^8), P packed to bf16 pairs into its TMEM buffer, and the final O / l
+//              epilogue.  M-tile 0's warpgroup also zeroes the V rows past the last visible key of
+//              the ragged context tile and of the tree tile before their PV (P is 0 there, but
+//              0 x NaN would not be).
 //
 // Every mbarrier wait is bounded; a wait that runs out records EAGLE_ERR_TIMEOUT in the status
 // word, raises a CTA-wide abort flag that ends every role's loop, and the CTA still drains its
@@ -49,19 +52,19 @@ struct AttnTcParams {  // same layout as the declaration in tree_attention.cu
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kNkv = 64;                   // keys per tile
-constexpr int kKStages = 4;                // K tiles are released as soon as QK^T has read them
-constexpr int kVStages = 6;                // V tiles are held until PV, later in the tile's life
-constexpr uint32_t kHalf = kNkv * 128;     // one 64-dim half of a K or V tile: 64 rows x 128 B
+constexpr int kNkv = 64;                    // keys per tile
+constexpr int kKStages = 4;                 // K tiles are released as soon as QK^T has read them
+constexpr int kVStages = 6;                 // V tiles are held until PV, later in the tile's life
+constexpr uint32_t kHalf = kNkv * 128;      // one 64-dim half of a K or V tile: 64 rows x 128 B
 constexpr uint32_t kTileBytes = 2 * kHalf;  // a K (or V) tile: both halves
-constexpr uint32_t kQHalf = 128 * 128;     // 128 rows x 128 B
+constexpr uint32_t kQHalf = 128 * 128;      // 128 rows x 128 B
 constexpr uint32_t kQTile = 2 * kQHalf;
 constexpr uint32_t kOffK = 2 * kQTile;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
 constexpr uint32_t kSmemBytes = kOffV + kVStages * kTileBytes;  // 224 KB
-// TMEM: O_0, O_1 (128 columns each), then S[2 M-tiles][2 buffers] (64 columns each); the bf16 P of
-// a tile is written over the first 32 columns of its own S buffer and read from there by PV
+// TMEM columns: O_0, O_1 (128 each) | S_0, S_1 (64 each) | P_0[2], P_1[2] (32 each, bf16 pairs)
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 256, kColP = 384;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait counts as stuck
 
 __device__ __forceinline__ uint32_t sa(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -79,20 +82,26 @@ constexpr uint32_t idesc(int M, int N, int b_mn) {
 constexpr uint32_t kIdescQK = idesc(128, kNkv, 0);
 constexpr uint32_t kIdescPV = idesc(128, 128, 1);  // A = P from TMEM, B = V MN-major
 
+// The MMA issuer is a whole converged warp; one lane, picked by elect.sync, issues each operation
+// (issuing from a converged warp is faster than from one lane of a divergent branch).
 __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
         "l"(a), "l"(b), "r"(id), "r"(acc));
 }
 // A from TMEM (K-major, two bf16 per 32-bit column), B from shared memory
 __device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
         "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
 }
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sa(bar))
-                 : "memory");
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(sa(bar))
+        : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -132,14 +141,44 @@ __device__ __forceinline__ void tst16(uint32_t taddr, const uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void tst_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Two floats in one 64-bit register pair, for the f32x2 arithmetic of sm_100-class SMs.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float f2_lo(uint64_t r) {
+    float a;
+    asm("{\n .reg .f32 x;\n mov.b64 {%0, x}, %1;\n}" : "=f"(a) : "l"(r));
+    return a;
+}
+__device__ __forceinline__ float f2_hi(uint64_t r) {
+    float b;
+    asm("{\n .reg .f32 x;\n mov.b64 {x, %0}, %1;\n}" : "=f"(b) : "l"(r));
+    return b;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 struct Bars {
     uint64_t q_full;
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
-    uint64_t s_full[2][2];   // [M-tile][S buffer]: QK^T of the buffer's tile landed
-    uint64_t p_full[2][2];   // [M-tile][S buffer]: P of the buffer's tile written over S
-    uint64_t o_ready[2][2];  // [M-tile][S buffer]: the PV that read this buffer's P has completed
-    uint64_t drain;
+    uint64_t v_clean[2];   // V rows past the last visible key zeroed: [0] ragged context tile, [1] tree tile
+    uint64_t s_full[2];    // [M-tile]: QK^T of the current tile landed (and every MMA issued before it)
+    uint64_t s_free[2];    // [M-tile]: the softmax has read S_t; the next QK^T may overwrite it
+    uint64_t p_full[2][2];  // [M-tile][P buffer]: P of a tile written
+    uint64_t o_ready[2];   // [M-tile]: a PV of this M-tile completed (once per tile)
+    uint64_t o_done[2];    // [M-tile]: the last PV completed
+    uint64_t drain[2];     // [M-tile]: every MMA of that M-tile's issuing warp completed
 };
 
 // Bounded wait; gives up (and raises the abort flag) when the CTA aborted or the limit ran out.
@@ -154,25 +193,33 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     return false;
 }
 
-// Non-blocking test of a phase (state-machine roles poll several barriers alternately).
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(sa(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-constexpr uint32_t kSpinLimit = 1u << 26;  // polls without progress before a role counts as stuck
-
-// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, the warp leaves converged.
+// Warp-uniform bounded wait: every lane polls and the warp agrees by vote, so the warp never
+// diverges (a lane-0-only polling loop costs several hundred cycles to reconverge even when the
+// phase has long completed; this form costs a few dozen).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *status) {
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0) ok = wait_or_abort(bar, parity, abort_flag, status);
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if ((it & 255) == 255 && __any_sync(0xffffffffu, *abort_flag != 0)) return false;
+    }
+    if ((threadIdx.x & 31) == 0) {
+        *abort_flag = 1;
+        set_status(status, EAGLE_ERR_TIMEOUT);
+    }
     __syncwarp();
-    return ok;
+    return false;
+}
+
+// Rescale 128 TMEM columns of this warp's 32 lanes (a row of O) by alpha.
+__device__ __forceinline__ void tmem_scale128(uint32_t taddr, float alpha) {
+#pragma unroll
+    for (int cc = 0; cc < 128; cc += 16) {
+        uint32_t o[16];
+        tld16(taddr + cc, o);
+        tld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tst16(taddr + cc, o);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -196,30 +243,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && mg == 0 && g == 0) set_status(p.status, EAGLE_ERR_DEVICE_INPUT);
         return;  // uniform for the CTA: nothing allocated yet
     }
-    const int row0 = mg * 256;                             // first query row of this CTA
-    const int tm = min(2, (p.rows - row0 + 127) / 128);     // M-tiles in this CTA (1 or 2)
-    const int nctx = (ctx + kNkv - 1) / kNkv;               // context tiles
-    const int ntiles = nctx + 1;                            // + the tree tile
+    const int row0 = mg * 256;                          // first query row of this CTA
+    const int tm = min(2, (p.rows - row0 + 127) / 128);  // M-tiles in this CTA (1 or 2)
+    const int nctx = (ctx + kNkv - 1) / kNkv;            // context tiles
+    const int ntiles = nctx + 1;                         // + the tree tile
+    const int jtail = (ctx % kNkv) ? nctx - 1 : -1;      // the ragged context tile, if any
 
     if (tid == 0) {
         s_abort = 0;
         mbar_init(&bars.q_full, 1);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
-            mbar_init(&bars.k_empty[s], 1);
+            mbar_init(&bars.k_empty[s], tm);  // one release per M-tile's MMA warp
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars.v_full[s], 1);
-            mbar_init(&bars.v_empty[s], 1);
+            mbar_init(&bars.v_empty[s], tm);
         }
         for (int t = 0; t < 2; ++t) {
-            for (int q = 0; q < 2; ++q) {
-                mbar_init(&bars.s_full[t][q], 1);
-                mbar_init(&bars.p_full[t][q], 4);
-                mbar_init(&bars.o_ready[t][q], 1);
-            }
+            mbar_init(&bars.v_clean[t], 4);
+            mbar_init(&bars.s_full[t], 1);
+            mbar_init(&bars.s_free[t], 4);
+            mbar_init(&bars.p_full[t][0], 4);
+            mbar_init(&bars.p_full[t][1], 4);
+            mbar_init(&bars.o_ready[t], 1);
+            mbar_init(&bars.o_done[t], 1);
         }
-        mbar_init(&bars.drain, 1);
+        mbar_init(&bars.drain[0], 1);
+        mbar_init(&bars.drain[1], 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -244,120 +295,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_3d(&qmap, sm + t * kQTile + h * kQHalf, &bars.q_full, 64 * h, g * p.G, zq + t * (128 / p.G));
             const int zc = (l * p.B + b) * p.S_max;
             const int zt = (l * p.B + b) * p.n;
-            uint32_t spins = 0;
-            while (k_issued < ntiles || v_issued < ntiles) {
-                bool prog = false;
-                // K tiles feed QK^T, the critical path: they go first; a V tile is issued only when
-                // the K ring cannot take another tile (the TMA engine serves boxes in order)
-                if (k_issued < ntiles) {
-                    const int j = k_issued, s = j % kKStages;
-                    if (j < kKStages || mbar_test(&bars.k_empty[s], ((j / kKStages) - 1) & 1)) {
-                        const bool tree = j == nctx;
-                        const CUtensorMap *m = tree ? &ktmap : &kmap;
-                        const int z = tree ? zt : zc + j * kNkv;
-                        unsigned char *st = sm + kOffK + s * kTileBytes;
-                        mbar_expect_tx(&bars.k_full[s], kTileBytes);
-                        tma_kv(m, st, &bars.k_full[s], z, g);
-                        ++k_issued;
-                        prog = true;
-                    }
-                }
-                if (!prog && v_issued < k_issued) {
-                    const int j = v_issued, s = j % kVStages;
-                    if (j < kVStages || mbar_test(&bars.v_empty[s], ((j / kVStages) - 1) & 1)) {
-                        const bool tree = j == nctx;
-                        const CUtensorMap *m = tree ? &vtmap : &vmap;
-                        const int z = tree ? zt : zc + j * kNkv;
-                        unsigned char *st = sm + kOffV + s * kTileBytes;
-                        mbar_expect_tx(&bars.v_full[s], kTileBytes);
-                        tma_kv(m, st, &bars.v_full[s], z, g);
-                        ++v_issued;
-                        prog = true;
-                    }
-                }
-                if (prog) {
-                    spins = 0;
-                } else if (++spins >= kSpinLimit || ((spins & 255) == 0 && *abort_flag)) {
-                    if (spins >= kSpinLimit) {
-                        *abort_flag = 1;
-                        set_status(p.status, EAGLE_ERR_TIMEOUT);
-                    }
+            // fixed order K(j), V(j); each waits (blocking) for its stage's previous tile to be released
+            for (int j = 0; j < ntiles; ++j) {
+                const int sk = j % kKStages, sv = j % kVStages;
+                if (j >= kKStages && !wait_or_abort(&bars.k_empty[sk], ((j / kKStages) - 1) & 1, abort_flag, p.status))
                     break;
-                }
+                mbar_expect_tx(&bars.k_full[sk], kTileBytes);
+                tma_kv(j == nctx ? &ktmap : &kmap, sm + kOffK + sk * kTileBytes, &bars.k_full[sk],
+                       j == nctx ? zt : zc + j * kNkv, g);
+                ++k_issued;
+                if (j >= kVStages && !wait_or_abort(&bars.v_empty[sv], ((j / kVStages) - 1) & 1, abort_flag, p.status))
+                    break;
+                mbar_expect_tx(&bars.v_full[sv], kTileBytes);
+                tma_kv(j == nctx ? &vtmap : &vmap, sm + kOffV + sv * kTileBytes, &bars.v_full[sv],
+                       j == nctx ? zt : zc + j * kNkv, g);
+                ++v_issued;
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer: QK^T and PV issued in whatever order they become ready ----
-        if (lane == 0) {
-            bool ok = wait_or_abort(&bars.q_full, 0, abort_flag, p.status);
-            tc_fence_after();
-            int nq = 0, npv = 0, pv_t = 0;
-            uint32_t spins = 0;
-            while (ok && npv < ntiles) {
-                bool prog = false;
-                // S_t(nq) = Q_t K(nq)^T: K landed, and the PV that read S buffer nq & 1 (tile nq - 2,
-                // whose P lives there) has completed for every M-tile
-                if (nq < ntiles && nq < npv + 2) {
-                    const int s = nq % kKStages, q = nq & 1;
-                    bool ready = mbar_test(&bars.k_full[s], (nq / kKStages) & 1);
-                    for (int t = 0; t < tm && ready && nq >= 2; ++t)
-                        ready = mbar_test(&bars.o_ready[t][q], ((nq - 2) >> 1) & 1);
-                    if (ready) {
-                        tc_fence_after();
-                        const uint32_t kbase = sa(sm + kOffK + s * kTileBytes);
-                        for (int t = 0; t < tm; ++t) {
-                            const uint32_t qbase = sa(sm + t * kQTile);
-                            const uint32_t dS = tmem + 256 + (t * 2 + q) * kNkv;
+    } else if (warp == 1 || (warp == 2 && tm > 1)) {
+        // ---------------- MMA issuer of M-tile t = warp - 1: a fixed schedule, blocking waits -----
+        // Step j issues S_t(j) = Q_t K(j)^T (once the softmax has read S_t(j - 1)), then O_t +=
+        // P_t(j - 1) V(j - 1) (once P_t(j - 1) is written).  S_t is single-buffered and P_t
+        // double-buffered, so S_t(j) overlaps the softmax of tile j - 1; PV_t(j - 2), the last
+        // reader of the P buffer tile j fills, was issued in step j - 1, before S_t(j), whose commit
+        // therefore also covers it.  Each M-tile has its own issuing warp, so neither waits on the
+        // other's softmax; a K or V stage is released once both have read it.
+        const int t = warp - 1;
+        bool ok = warp_wait(&bars.q_full, 0, abort_flag, p.status);
+        tc_fence_after();
+        const uint32_t qbase = sa(sm + t * kQTile);
+        const uint32_t dS = tmem + kColS + t * 64;
+        const uint32_t dO = tmem + t * 128;
+        for (int j = 0; ok && j <= ntiles; ++j) {
+            if (j < ntiles) {
+                const int sk = j % kKStages;
+                ok = warp_wait(&bars.k_full[sk], (j / kKStages) & 1, abort_flag, p.status) &&
+                     (j == 0 || warp_wait(&bars.s_free[t], (j - 1) & 1, abort_flag, p.status));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t kbase = sa(sm + kOffK + sk * kTileBytes);
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
-                                const uint32_t offk = (kk >> 2) * kHalf + (kk & 3) * 32;
-                                umma(dS, sdesc(qbase + off, 16, 1024), sdesc(kbase + offk, 16, 1024), kIdescQK,
-                                     kk > 0);
-                            }
-                            umma_commit(&bars.s_full[t][q]);
-                        }
-                        umma_commit(&bars.k_empty[s]);
-                        ++nq;
-                        prog = true;
-                    }
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
+                    const uint32_t offk = (kk >> 2) * kHalf + (kk & 3) * 32;
+                    umma(dS, sdesc(qbase + off, 16, 1024), sdesc(kbase + offk, 16, 1024), kIdescQK, kk > 0);
                 }
-                // O_t += P_t(npv) V(npv): V landed and P_t written (in TMEM, over S)
-                if (npv < nq) {
-                    const int sv = npv % kVStages, pb = npv & 1;
-                    if (mbar_test(&bars.v_full[sv], (npv / kVStages) & 1) &&
-                        mbar_test(&bars.p_full[pv_t][pb], (npv >> 1) & 1)) {
-                        tc_fence_after();
-                        const uint32_t vbase = sa(sm + kOffV + sv * kTileBytes);
-                        const uint32_t aP = tmem + 256 + (pv_t * 2 + pb) * kNkv;
-                        const uint32_t dO = tmem + pv_t * 128;
+                umma_commit(&bars.s_full[t]);
+                umma_commit(&bars.k_empty[sk]);  // this M-tile has read K(j)
+            }
+            if (j > 0) {
+                const int jv = j - 1, sv = jv % kVStages, pb = jv & 1;
+                ok = warp_wait(&bars.v_full[sv], (jv / kVStages) & 1, abort_flag, p.status) &&
+                     (jv != jtail || warp_wait(&bars.v_clean[0], 0, abort_flag, p.status)) &&
+                     (jv != nctx || warp_wait(&bars.v_clean[1], 0, abort_flag, p.status)) &&
+                     warp_wait(&bars.p_full[t][pb], (jv >> 1) & 1, abort_flag, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t vbase = sa(sm + kOffV + sv * kTileBytes);
+                const uint32_t aP = tmem + kColP + t * 64 + pb * 32;
 #pragma unroll
-                        for (int kk = 0; kk < kNkv / 16; ++kk)
-                            umma_ts(dO, aP + kk * 8, sdesc(vbase + kk * 2048, kHalf, 1024), kIdescPV,
-                                    (npv > 0 || kk > 0) ? 1u : 0u);
-                        umma_commit(&bars.o_ready[pv_t][pb]);
-                        if (++pv_t == tm) {
-                            umma_commit(&bars.v_empty[sv]);
-                            pv_t = 0;
-                            ++npv;
-                        }
-                        prog = true;
-                    }
-                }
-                if (prog) {
-                    spins = 0;
-                } else if (++spins >= kSpinLimit || ((spins & 255) == 0 && *abort_flag)) {
-                    if (spins >= kSpinLimit) {
-                        *abort_flag = 1;
-                        set_status(p.status, EAGLE_ERR_TIMEOUT);
-                    }
-                    ok = false;
-                }
+                for (int kk = 0; kk < kNkv / 16; ++kk)
+                    umma_ts(dO, aP + kk * 8, sdesc(vbase + kk * 2048, kHalf, 1024), kIdescPV,
+                            (jv > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars.o_ready[t]);
+                if (jv == ntiles - 1) umma_commit(&bars.o_done[t]);
+                umma_commit(&bars.v_empty[sv]);  // this M-tile has read V(j - 1)
             }
-            // drain: every MMA issued by this thread has completed once `drain` completes
-            umma_commit(&bars.drain);
-            for (uint32_t it = 0; it < kWaitLimit && !mbar_try_wait(&bars.drain, 0); ++it) {
-            }
+        }
+        // drain: every MMA issued by this warp has completed once its `drain` barrier completes
+        umma_commit(&bars.drain[t]);
+        for (uint32_t it = 0; it < kWaitLimit && !__all_sync(0xffffffffu, mbar_try_wait(&bars.drain[t], 0)); ++it) {
         }
     } else if (warp >= 4 && warp - 4 < 4 * tm) {
         // ---------------- softmax warpgroup t ----------------
@@ -370,13 +377,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gh = valid ? r % p.G : 0;
         const uint64_t tmask = valid ? p.mask[size_t(b) * p.n + node] : 0ull;
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
+        const uint32_t tS = tmem + lane_off + kColS + t * 64;  // this row's S columns
+        const uint32_t tP = tmem + lane_off + kColP + t * 64;  // this row's two P buffers
+        const uint32_t tO = tmem + lane_off + t * 128;         // this row's O columns
         const float c = p.scale_log2;
         float m_raw = -INFINITY;  // reference max in raw score units (P = 2^((s - m_raw) c))
         float l_sum = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            const int q = j & 1;
-            if (!warp_wait(&bars.s_full[t][q], (j >> 1) & 1, abort_flag, p.status)) {
+            // S_t(j) landed; its commit also covers PV_t(j - 2), the last reader of P buffer j & 1
+            if (!warp_wait(&bars.s_full[t], j & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
             }
@@ -388,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t (&r1)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 16);
                 uint32_t (&r2)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 32);
                 uint32_t (&r3)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 48);
-                const uint32_t tS = tmem + lane_off + 256 + (t * 2 + q) * kNkv;
                 tld16(tS, r0);
                 tld16(tS + 16, r1);
                 tld16(tS + 32, r2);
@@ -397,9 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int cc = 0; cc < kNkv; ++cc) sv[cc] = __uint_as_float(raw[cc]);
             }
-            // masking: only the context tail tile and the tree tile have invisible keys
+            // S_t is in registers: hand it back so QK^T of the next tile overlaps this softmax
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars.s_free[t]);
             const bool tree = j == nctx;
             const int kvalid = tree ? p.n : min(kNkv, ctx - j * kNkv);
+            // masking: only the ragged context tile and the tree tile have invisible keys (a masked
+            // score is replaced, so whatever the fetched K row held is irrelevant)
             if (tree || kvalid < kNkv) {
 #pragma unroll
                 for (int cc = 0; cc < kNkv; ++cc) {
@@ -417,88 +431,95 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mx3 = fmaxf(mx3, sv[cc + 3]);
             }
             const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-            // lazy rescale: the reference moves only when the row max exceeds it by more than 8
-            // in base-2 units, so every P stays below 2^8
-            const bool rescale = (mx - m_raw) * c > 8.f;
-            float alpha = 1.f;
-            if (rescale) {
-                alpha = m_raw == -INFINITY ? 0.f : fast_exp2((m_raw - mx) * c);
+            // lazy rescale: the reference moves only when the max exceeds it by more than 8 in
+            // base-2 units, so every P stays below 2^8
+            if ((mx - m_raw) * c > 8.f) {
+                const float alpha = m_raw == -INFINITY ? 0.f : fast_exp2((m_raw - mx) * c);
                 m_raw = mx;
+                if (j > 0) {
+                    // O_t must hold tiles < j: wait for PV_t(j - 1).  o_ready completes once per PV
+                    // of this M-tile and PV_t(j) needs this tile's P, so the phase cannot alias.
+                    if (!warp_wait(&bars.o_ready[t], (j - 1) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    tmem_scale128(tO, alpha);
+                }
+                l_sum *= alpha;
             }
             const float mc = m_raw == -INFINITY ? 0.f : m_raw * c;
-            float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+            // scale and row sums on the paired f32x2 pipe (two lanes of work per instruction)
+            const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-mc, -mc);
+            uint64_t s01 = f2_pack(0.f, 0.f), s23 = s01;
             uint32_t pk[kNkv / 2];
 #pragma unroll
             for (int cc = 0; cc < kNkv; cc += 4) {
-                const float p0 = fast_exp2(fmaf(sv[cc], c, -mc));
-                const float p1 = fast_exp2(fmaf(sv[cc + 1], c, -mc));
-                const float p2 = fast_exp2(fmaf(sv[cc + 2], c, -mc));
-                const float p3 = fast_exp2(fmaf(sv[cc + 3], c, -mc));
-                ps0 += p0;
-                ps1 += p1;
-                ps2 += p2;
-                ps3 += p3;
+                const uint64_t a01 = f2_fma(f2_pack(sv[cc], sv[cc + 1]), c2, nm2);
+                const uint64_t a23 = f2_fma(f2_pack(sv[cc + 2], sv[cc + 3]), c2, nm2);
+                const float p0 = fast_exp2(f2_lo(a01)), p1 = fast_exp2(f2_hi(a01));
+                const float p2 = fast_exp2(f2_lo(a23)), p3 = fast_exp2(f2_hi(a23));
+                s01 = f2_add(s01, f2_pack(p0, p1));
+                s23 = f2_add(s23, f2_pack(p2, p3));
                 __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
                 __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
                 pk[cc / 2] = *reinterpret_cast<uint32_t *>(&h0);
                 pk[cc / 2 + 1] = *reinterpret_cast<uint32_t *>(&h1);
             }
-            l_sum = l_sum * alpha + ((ps0 + ps1) + (ps2 + ps3));
-            // O_t must be final before it is rescaled (PV of tile j-1 complete).  o_ready[t][q]
-            // completes once per use of S buffer q (tiles q, q + 2, ...); the awaited phase is always
-            // that barrier's most recent one, so its parity cannot alias.
-            if (rescale && j > 0) {
-                if (!warp_wait(&bars.o_ready[t][(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t tO = tmem + lane_off + t * 128;
-#pragma unroll
-                for (int cc = 0; cc < 128; cc += 16) {
-                    uint32_t o[16];
-                    tld16(tO + cc, o);
-                    tld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tst16(tO + cc, o);
-                }
-                tst_wait();
-            }
-            // P (bf16 pairs) over the first 32 columns of this tile's S buffer
+            const uint64_t s4 = f2_add(s01, s23);
+            l_sum += f2_lo(s4) + f2_hi(s4);
+            // P (bf16 pairs) into P buffer j & 1; PV_t(j - 2), its previous reader, has completed
             {
-                const uint32_t tP = tmem + lane_off + 256 + (t * 2 + q) * kNkv;
                 uint32_t (&p0)[16] = *reinterpret_cast<uint32_t(*)[16]>(pk);
                 uint32_t (&p1)[16] = *reinterpret_cast<uint32_t(*)[16]>(pk + 16);
-                tst16(tP, p0);
-                tst16(tP + 16, p1);
+                tst16(tP + (j & 1) * 32, p0);
+                tst16(tP + (j & 1) * 32 + 16, p1);
                 tst_wait();
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.p_full[t][q]);
+            if (lane == 0) mbar_arrive(&bars.p_full[t][j & 1]);
+            // M-tile 0's warpgroup zeroes the V rows past the last visible key of the ragged context
+            // tile and of the tree tile before their PV (P is 0 there, but 0 x NaN would not be).
+            // Waiting on V(j)'s phase is safe here: that stage cannot move past tile j before the
+            // PV that this warpgroup's P(j) gates.
+            if (t == 0 && (j == jtail || j == nctx)) {
+                if (!warp_wait(&bars.v_full[j % kVStages], (j / kVStages) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char *st = sm + kOffV + (j % kVStages) * kTileBytes;
+                // a row is 128 contiguous bytes in each half (the swizzle permutes within the row)
+                for (int i = kvalid * 8 + rho; i < kNkv * 8; i += 128) {
+                    const int rr = i >> 3, c16 = i & 7;
+                    *reinterpret_cast<uint4 *>(st + rr * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(st + kHalf + rr * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.v_clean[j == nctx ? 1 : 0]);
+            }
         }
         // epilogue: O / l to global, bf16
-        if (ok && warp_wait(&bars.o_ready[t][(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag, p.status)) {
+        if (ok && warp_wait(&bars.o_done[t], 0, abort_flag, p.status)) {
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
             __nv_bfloat16 *orow = p.out + ((((size_t)l * p.B + b) * p.n + node) * p.Hq + g * p.G + gh) * 128;
-            const uint32_t tO = tmem + lane_off + t * 128;
 #pragma unroll
-            for (int c = 0; c < 128; c += 16) {
+            for (int cc = 0; cc < 128; cc += 16) {
                 uint32_t o[16];
-                tld16(tO + c, o);
+                tld16(tO + cc, o);
                 tld_wait();
                 uint32_t w[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
-                                                             __uint_as_float(o[2 * e + 1]) * inv);
-                    w[e] = *reinterpret_cast<uint32_t *>(&h);
+                    __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
+                                                              __uint_as_float(o[2 * e + 1]) * inv);
+                    w[e] = *reinterpret_cast<uint32_t *>(&hh);
                 }
                 if (valid) {
-                    reinterpret_cast<uint4 *>(orow + c)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    reinterpret_cast<uint4 *>(orow + c)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    reinterpret_cast<uint4 *>(orow + cc)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    reinterpret_cast<uint4 *>(orow + cc)[1] = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
         }
@@ -554,13 +575,14 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t mid, uint64_t outer, 
 }
 
 // 4-D map over a [rows][heads][128] bf16 tensor seen as {64 elems, rows, 2 halves, heads} (strides
-// out of order) with a {64, kNkv, 2, 1} 128B-swizzled box: one box = both halves of kNkv rows.
-bool make_kv_map(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows) {
+// out of order) with a {64, box_rows, box_halves, 1} 128B-swizzled box.
+bool make_kv_map(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows, uint32_t box_rows,
+                 uint32_t box_halves) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[4] = {64, rows, 2, heads};
     cuuint64_t strides[3] = {heads * 128 * 2, 128, 128 * 2};
-    cuuint32_t box[4] = {64, kNkv, 2, 1};
+    cuuint32_t box[4] = {64, box_rows, box_halves, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -579,9 +601,9 @@ eagle_status tree_attention_tc_launch(const AttnTcParams &p, const void *q, cons
                                       const void *k_tree, const void *v_tree, cudaStream_t stream) {
     CUtensorMap qm, km, vm, ktm, vtm;
     const uint64_t LB = uint64_t(p.L) * p.B;
-    if (!make_map(&qm, q, p.Hq, LB * p.n, p.G, 128 / p.G) || !make_kv_map(&km, k_cache, p.Hkv, LB * p.S_max) ||
-        !make_kv_map(&vm, v_cache, p.Hkv, LB * p.S_max) || !make_kv_map(&ktm, k_tree, p.Hkv, LB * p.n) ||
-        !make_kv_map(&vtm, v_tree, p.Hkv, LB * p.n))
+    if (!make_map(&qm, q, p.Hq, LB * p.n, p.G, 128 / p.G) || !make_kv_map(&km, k_cache, p.Hkv, LB * p.S_max, kNkv, 2) ||
+        !make_kv_map(&vm, v_cache, p.Hkv, LB * p.S_max, kNkv, 2) || !make_kv_map(&ktm, k_tree, p.Hkv, LB * p.n, kNkv, 2) ||
+        !make_kv_map(&vtm, v_tree, p.Hkv, LB * p.n, kNkv, 2))
         return EAGLE_ERR_UNSUPPORTED;  // the caller falls back to the mma.sync kernel
     static bool attr = false;
     const size_t smem = kSmemBytes + 1024;

@@ -117,6 +117,24 @@ def test_tree_attention_matches_oracle(case):
     assert err <= ATTN_TOL[dtype], err
 
 
+@pytest.mark.parametrize("case", [c for c in ATTN_CASES if min(c[6]) < max(c[6])],
+                         ids=lambda c: f"L{c[0]}B{c[1]}n{c[2]}G{c[3]//c[4]}d{c[5]}{c[7]}")
+def test_tree_attention_ignores_cache_past_context(case):
+    """Cache positions at or past ctx_len[b] may hold anything, NaN included: the output is unchanged."""
+    L, B, n, Hq, Hkv, d, ctx, dtype = case
+    wl, inp, mask = _attn_inputs(L, B, n, Hq, Hkv, d, ctx, dtype, seed=5 + n)
+    mask_t = torch.from_numpy(mask.reshape(B, n).view(np.int64).copy()).to(DEV)
+    args = lambda: (inp["q"], inp["k_cache"], inp["v_cache"], inp["ctx_len"], inp["k_tree"], inp["v_tree"], mask_t)
+    clean = eg.tree_attention(*args())
+    for b, c in enumerate(ctx):
+        inp["k_cache"][:, b, c:] = float("nan")
+        inp["v_cache"][:, b, c:] = float("nan")
+    dirty = eg.tree_attention(*args())
+    torch.cuda.synchronize()
+    assert torch.isfinite(dirty.float()).all()
+    assert torch.equal(dirty, clean)
+
+
 def test_tree_attention_chain_equals_causal_on_gpu():
     """A chain tree through the library equals causal attention computed by torch in fp64."""
     L, B, n, Hq, Hkv, d = 1, 1, 12, 4, 2, 128

@@ -251,7 +251,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
                    "dtype_detail": "bf16 K/V/Q/O with fp32 softmax and accumulation; fp32 logits"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": _traffic(attn_bytes),
-                     "kernel": "tree_attn_bf16_kernel" if wl.kv_dtype == "bf16" else "tree_attn_f32_kernel",
+                     "kernel": "tree_attn_tc_kernel" if wl.kv_dtype == "bf16" else "tree_attn_f32_kernel",
                      "algorithmic_bytes": attn_bytes, "avg_launch_ms": attn_ms,
                      "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)"},
         "end_to_end_hbm": {"metric_bytes": metric_bytes, "exact_bytes": bytes_["exact"],
@@ -312,18 +312,23 @@ def run_e2e(eg, lib, wl, rd: Round, outs, ws, stream, dev, steps, world) -> dict
             "d2h_bytes_per_step": d2h, "steps": steps}
 
 
+def attention_source_hash() -> str:
+    """sha256[:16] of the tensor-core attention kernel's source file."""
+    src = os.path.join(ROOT, "eagle_draft_tree_gb300", "csrc", "tree_attention_tc.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+
+
 def _traffic(attn_bytes: float):
     """DRAM bytes per attention launch from the committed ncu summary, if it was taken on the
     current attention kernel source (else null)."""
     path = os.path.join(ROOT, "profiles", "tree_attention_llama31_8b.md")
-    src = os.path.join(ROOT, "eagle_draft_tree_gb300", "csrc", "tree_attention.cu")
     if not os.path.exists(path):
         return None
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    h = attention_source_hash()
     fields = {}
     for line in open(path):
-        if line.startswith("- ") and ":" in line:
-            k, v = line[2:].split(":", 1)
+        if line.startswith("- ") and ": " in line:
+            k, v = line[2:].split(": ", 1)
             fields[k.strip()] = v.strip().strip("`")
     if fields.get("source sha256[:16]") != h:
         return None

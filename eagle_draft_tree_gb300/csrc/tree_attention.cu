@@ -387,15 +387,6 @@ eagle_status launch_f32(const AttnArgs &a, cudaStream_t stream) {
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
 
-// EAGLE_ATTN_LEGACY=1 selects the mma.sync kernel (kept as the comparison baseline).
-bool legacy_path() {
-    static int v = -1;
-    if (v < 0) {
-        const char *e = getenv("EAGLE_ATTN_LEGACY");
-        v = (e && e[0] == '1') ? 1 : 0;
-    }
-    return v == 1;
-}
 
 }  // namespace
 
@@ -426,7 +417,7 @@ eagle_status tree_attention_launch(const eagle_attn_cfg &c, const void *q, const
     a.scale = c.scale > 0.f ? c.scale : 1.f / sqrtf(float(c.head_dim));
     a.scale_log2 = a.scale * kLog2e;
     if (c.dtype == EAGLE_DTYPE_BF16) {
-        if (tree_attention_tc_supported(c.head_dim, c.dtype, a.G, c.max_seq) && !legacy_path()) {
+        if (tree_attention_tc_supported(c.head_dim, c.dtype, a.G, c.max_seq)) {
             AttnTcParams tp;
             tp.mask = mask;
             tp.ctx_len = ctx_len;

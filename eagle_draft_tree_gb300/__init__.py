@@ -64,6 +64,7 @@ _SIGS = {
     "eagle_tree_attention": (ctypes.c_int32, [ctypes.POINTER(AttnCfg)] + [_P] * 9 + [ctypes.c_size_t, _P]),
     "eagle_tree_verify_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(VerifyCfg)]),
     "eagle_tree_verify": (ctypes.c_int32, [ctypes.POINTER(VerifyCfg)] + [_P] * 11 + [ctypes.c_size_t, _P]),
+    "eagle_tree_verify_static": (ctypes.c_int32, [ctypes.POINTER(VerifyCfg)] + [_P] * 10 + [_P]),
     "eagle_workspace_init": (ctypes.c_int32, [_P, ctypes.c_size_t, _P]),
     "eagle_get_device_status": (ctypes.c_int32, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "eagle_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
@@ -272,4 +273,31 @@ def tree_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor, tree: d
                                _ptr(out["out_tokens"]), _ptr(out["out_len"]), _ptr(out["out_path"]),
                                _ptr(out.get("out_ratio")), ws.ptr, ctypes.c_size_t(ws.nbytes), _stream(stream))
     _check(st, "eagle_tree_verify")
+    return out
+
+
+def tree_verify_static(target_logits: torch.Tensor, draft_logits: torch.Tensor, tree: dict, uniforms: torch.Tensor,
+                       temperature: float, depth: int, topk: int, out: dict | None = None, with_ratio: bool = True,
+                       stream=None) -> dict:
+    """eagle_tree_verify_static: tree_verify with the library's static device scratch instead of a
+    caller workspace (same arguments and outputs; B * n <= 5034)."""
+    lib = load()
+    B, n, V = target_logits.shape
+    _need(target_logits, "target_logits", torch.float32)
+    _need(draft_logits, "draft_logits", torch.float32, (B, 1 + (depth - 1) * topk, V))
+    for key in ("tokens", "parents", "node_row"):
+        _need(tree[key], key, torch.int32, (B, n))
+    _need(uniforms, "uniforms", torch.float32, (B, n))
+    cfg = VerifyCfg(B, V, depth, topk, n - 1, float(temperature))
+    dev = target_logits.device
+    if out is None:
+        out = dict(out_tokens=torch.empty((B, depth + 1), dtype=torch.int32, device=dev),
+                   out_len=torch.empty((B,), dtype=torch.int32, device=dev),
+                   out_path=torch.empty((B, depth), dtype=torch.int32, device=dev),
+                   out_ratio=torch.empty((B, n), dtype=torch.float32, device=dev) if with_ratio else None)
+    st = lib.eagle_tree_verify_static(ctypes.byref(cfg), _ptr(target_logits), _ptr(draft_logits),
+                                      _ptr(tree["tokens"]), _ptr(tree["parents"]), _ptr(tree["node_row"]),
+                                      _ptr(uniforms), _ptr(out["out_tokens"]), _ptr(out["out_len"]),
+                                      _ptr(out["out_path"]), _ptr(out.get("out_ratio")), _stream(stream))
+    _check(st, "eagle_tree_verify_static")
     return out

@@ -190,6 +190,28 @@ eagle_status eagle_tree_verify(const eagle_verify_cfg *cfg, const float *target_
                                const float *uniforms, int32_t *out_tokens, int32_t *out_len, int32_t *out_path,
                                float *out_ratio, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * eagle_tree_verify without a caller workspace: the same computation and outputs (the same
+ * kernels run), with the scratch in the library's own static device storage of 256 KB, which
+ * holds up to 5034 tree nodes in all (B * n; e.g. 78 sequences of 64 nodes); a configuration
+ * needing more returns EAGLE_ERR_UNSUPPORTED before anything runs.  It exists for callers that cannot hand the library a device workspace:
+ * a serving process that reserves all device memory for weights and the KV cache at start-up and
+ * grants no further buffers, or a host framework whose plugin interface passes tensors but no
+ * scratch.  The pages describe no such entry point; it is an interface convenience only.
+ *   - Allocates nothing.  The first call on each device looks up the scratch's address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *   - The scratch starts zeroed (static storage) and needs no initialisation; no state carries
+ *     from one call to the next except the device status word, which this entry point never
+ *     reads: device-side errors show only through out_len (0 for a malformed tree).  Callers
+ *     that need the status word use eagle_tree_verify with their own workspace.
+ *   - There is one scratch per device: two calls that may overlap on the device (different
+ *     streams, or different host threads) race on it and must be serialised by the caller.
+ */
+eagle_status eagle_tree_verify_static(const eagle_verify_cfg *cfg, const float *target_logits,
+                                      const float *draft_logits, const int32_t *tokens, const int32_t *parents,
+                                      const int32_t *node_row, const float *uniforms, int32_t *out_tokens,
+                                      int32_t *out_len, int32_t *out_path, float *out_ratio, cudaStream_t stream);
+
 /* Zero `bytes` of a workspace on `stream` (needed once before a workspace's first use). */
 eagle_status eagle_workspace_init(void *ws, size_t bytes, cudaStream_t stream);
 

@@ -280,7 +280,7 @@ def tree_verify_static(target_logits: torch.Tensor, draft_logits: torch.Tensor, 
                        temperature: float, depth: int, topk: int, out: dict | None = None, with_ratio: bool = True,
                        stream=None) -> dict:
     """eagle_tree_verify_static: tree_verify with the library's static device scratch instead of a
-    caller workspace (same arguments and outputs; B * n <= 5034)."""
+    caller workspace (same arguments and outputs; B * n <= 7272)."""
     lib = load()
     B, n, V = target_logits.shape
     _need(target_logits, "target_logits", torch.float32)

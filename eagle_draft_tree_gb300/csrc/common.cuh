@@ -89,40 +89,6 @@ __device__ __forceinline__ uint64_t warp_bitonic_merge32(uint64_t v) {
     return v;
 }
 
-// Float-float accumulator (Knuth's TwoSum): about 48 bits of mantissa with fp32 instructions,
-// so cluster-wide sums avoid the slow fp64 pipe.
-struct FF {
-    float hi = 0.f, lo = 0.f;
-};
-__device__ __forceinline__ FF ff_add(FF x, FF y) {
-    const float s = x.hi + y.hi;
-    const float bb = s - x.hi;
-    float e = (x.hi - (s - bb)) + (y.hi - bb);
-    e += x.lo + y.lo;
-    FF r;
-    r.hi = s + e;
-    r.lo = e - (r.hi - s);
-    return r;
-}
-__device__ __forceinline__ FF ff_warp_sum(FF v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        FF o;
-        o.hi = __shfl_xor_sync(0xffffffffu, v.hi, off);
-        o.lo = __shfl_xor_sync(0xffffffffu, v.lo, off);
-        v = ff_add(v, o);
-    }
-    return v;
-}
-__device__ __forceinline__ double ff_to_double(FF v) { return double(v.hi) + double(v.lo); }
-
-// ln of a positive double via logf of its float rounding plus the first-order correction
-// (S - f)/f; absolute error about one float ulp of the result.
-__device__ __forceinline__ double log_fast(double S) {
-    const float f = float(S);
-    return double(logf(f)) + (S - double(f)) / double(f);
-}
-
 // Orderable 64-bit image of a double (integer order = numeric order; -0 folded onto +0).
 __device__ __forceinline__ uint64_t double_order_key(double d) {
     const uint64_t u = static_cast<uint64_t>(__double_as_longlong(d + 0.0));

@@ -29,6 +29,7 @@
 //                       (row maxima, log normalisers, each child's c_j and S_j) go to the workspace.
 //   verify_walk_kernel  one CTA per sequence: validates the tree, computes every child's accept
 //                       ratio in double precision (one thread per node), and walks the tree.
+#include <atomic>
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -44,19 +45,23 @@ namespace {
 
 constexpr int kPrepThreads = 512;
 constexpr int kWarpsPrep = kPrepThreads / 32;
-constexpr int kE = 32;  // tokens per thread and row
+constexpr int kE = 32;                       // tokens per thread and row, in kChunks chunks of 4
+constexpr int kChunks = kE / 4;
+constexpr int kSliceMax = kPrepThreads * kE;  // one CTA's slice of a row (16384 tokens)
+constexpr size_t kPrepSmem = 2 * size_t(kSliceMax) * sizeof(float);  // both rows' slices, 128 KB
 constexpr int kMaxNodes = 64;
+constexpr double kFxInv = 1.0 / 4503599627370496.0;  // fixed-point unit of weight sums: 2^-52
 
-// Per-node statistics the prep kernel leaves for the walk.  Row statistics (mp, mq, lnsp, lnsq)
-// belong to a node with children; (cj, sj) to a node as a child: its parent's rejection chain
-// state when this child is tested.
+// Per-node statistics the prep kernel leaves for the walk, in the forms the prep computes them
+// (the walk converts them to double).  Row statistics (mp, mq, lnsp, lnsq) belong to a node with
+// children; (cj, sj) to a node as a child: its parent's rejection chain state when this child is
+// tested.
 struct NodeStat {
-    double lnsp, lnsq;  // ln of the normaliser sum_t exp((x_t - max) / T), target and draft rows
-    double cj, sj;      // c_j, S_j of the parent's chain at this child's sibling index
-    float mp, mq;       // row maxima (logit units)
-    int32_t pad[2];
+    float mp, mq;      // row maxima (logit units)
+    float lnsp, lnsq;  // ln of the normaliser sum_t exp((x_t - max) / T), target and draft rows
+    uint64_t cj, sj;   // c_j, S_j of the parent's chain at this child's sibling index, in 2^-52 units
 };
-static_assert(sizeof(NodeStat) == 48, "NodeStat layout");
+static_assert(sizeof(NodeStat) == 32, "NodeStat layout");
 
 struct VerifyArgs {
     const float *target;    // [B][n][V]
@@ -77,49 +82,6 @@ struct VerifyArgs {
     int greedy;
 };
 
-__device__ __forceinline__ void ms_merge(float &m, float &s, float mo, float so, float c) {
-    const float M = fmaxf(m, mo);
-    if (M == -INFINITY) return;
-    const float x = (m == -INFINITY) ? 0.f : s * exp2f((m - M) * c);
-    const float y = (mo == -INFINITY) ? 0.f : so * exp2f((mo - M) * c);
-    m = M;
-    s = x + y;
-}
-
-// Load this thread's kE consecutive values of a row slice into registers (-inf past the end).
-__device__ __forceinline__ void load_run(float (&v)[kE], const float *src, int t0, int cnt, bool vec) {
-    if (vec) {
-#pragma unroll
-        for (int j = 0; j < kE / 4; ++j) {
-            const int idx = t0 + 4 * j;
-            const float4 w = idx < cnt ? __ldg(reinterpret_cast<const float4 *>(src + idx))
-                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            v[4 * j] = w.x;
-            v[4 * j + 1] = w.y;
-            v[4 * j + 2] = w.z;
-            v[4 * j + 3] = w.w;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < kE; ++j) v[j] = t0 + j < cnt ? __ldg(src + t0 + j) : -INFINITY;
-    }
-}
-
-// In place: v <- 2^((v - m) c) against the run's max m (0 past the end); returns the sum.
-__device__ __forceinline__ float exp_run(float (&v)[kE], float &m, float c) {
-    m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kE; ++j) m = fmaxf(m, v[j]);
-    const float mc = m == -INFINITY ? 0.f : m * c;
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < kE; ++j) {
-        v[j] = v[j] == -INFINITY ? 0.f : fast_exp2(fmaf(v[j], c, -mc));
-        s += v[j];
-    }
-    return s;
-}
-
 // ---- cluster record exchange.  Each CTA reduces a pass to one 16-byte record and pushes it into
 // every peer's receive slot with st.async, whose bytes complete on the receiver's own mbarrier; a
 // CTA then reads the CL records of the exchange from its own shared memory, in rank order, so all
@@ -137,126 +99,277 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t r
         "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
         : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {  // release, CTA scope
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+                 : "memory");
+}
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-__device__ __forceinline__ float4 shfl4(float4 v, int src) {
-    return make_float4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
-                       __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
-}
-// Warp-wide deterministic merges of (max, scaled sum) pairs held as (x, y) and (z, w).
-__device__ __forceinline__ float4 warp_ms_merge(float4 v, float c) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        ms_merge(v.x, v.y, __shfl_xor_sync(0xffffffffu, v.x, off), __shfl_xor_sync(0xffffffffu, v.y, off), c);
-        ms_merge(v.z, v.w, __shfl_xor_sync(0xffffffffu, v.z, off), __shfl_xor_sync(0xffffffffu, v.w, off), c);
-    }
-    return v;
-}
-__device__ __forceinline__ FF ff_from(float hi, float lo) {
-    FF r;
-    r.hi = hi;
-    r.lo = lo;
-    return r;
-}
 
-// Owner search of a final draw from the CL per-rank weight totals (float-float, in rank order):
-// the owner rank holds the first CDF step above u * total (running sums over the ranks are
-// monotone); if rounding leaves the target at or above the total, the draw clamps to the last rank
-// with mass.  Writes owner (-1: no mass at all), clamp and the target relative to the owner's start.
-template <int CL>
-__device__ __forceinline__ void decide_owner(const FF (&tot)[CL], float u, int &owner, int &clamp, float &local) {
-    FF total;
+// ---- token layout.  Thread t of a CTA holds chunk e (e < kChunks) of its slice at tokens
+// 4 (t + 512 e) .. 4 (t + 512 e) + 3, in registers v[4 e] .. v[4 e + 3]: a warp's accesses to a
+// row are 16-byte contiguous per lane, so shared-memory reads are conflict-free and global reads
+// coalesce.  Ascending token order is chunk column e first, then thread.
+__device__ __forceinline__ int chunk_tok(int e) { return 4 * (int(threadIdx.x) + kPrepThreads * e); }
+
+// This thread's chunks of a row slice from shared memory (cnt a multiple of 4; -inf past the end).
+__device__ __forceinline__ void read_chunks(float (&v)[kE], const float *srow, int cnt) {
 #pragma unroll
-    for (int r = 0; r < CL; ++r) total = ff_add(total, tot[r]);
-    // target = u * total in float-float (u * hi exactly as hi + lo via FMA)
-    const float th = u * total.hi;
-    FF target = ff_from(th, fmaf(u, total.hi, -th) + u * total.lo);
-    FF base;
-    int own = -1, last = -1;
-    FF rbase;
+    for (int e = 0; e < kChunks; ++e) {
+        const int t = chunk_tok(e);
+        const float4 w = t < cnt ? *reinterpret_cast<const float4 *>(srow + t)
+                                 : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        v[4 * e] = w.x;
+        v[4 * e + 1] = w.y;
+        v[4 * e + 2] = w.z;
+        v[4 * e + 3] = w.w;
+    }
+}
+// The same from global memory, one value at a time (rows that a bulk copy cannot take).
+__device__ __forceinline__ void load_chunks(float (&v)[kE], const float *src, int cnt) {
 #pragma unroll
-    for (int r = 0; r < CL; ++r) {
-        const FF next = ff_add(base, tot[r]);
-        const FF gap = ff_add(next, ff_from(-target.hi, -target.lo));  // next - target
-        if (own < 0 && (gap.hi > 0.f || (gap.hi == 0.f && gap.lo > 0.f))) {
-            own = r;
-            rbase = base;
+    for (int e = 0; e < kChunks; ++e)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = chunk_tok(e) + i;
+            v[4 * e + i] = t < cnt ? __ldg(src + t) : -INFINITY;
         }
-        base = next;
-        if (tot[r].hi > 0.f) last = r;
-    }
-    clamp = own < 0 ? 1 : 0;
-    owner = own < 0 ? last : own;
-    const FF lt = ff_add(target, ff_from(-rbase.hi, -rbase.lo));
-    local = lt.hi + lt.lo;
 }
 
-// Final draw at a node over this CTA's slice: w holds the weights (probabilities or residuals) of
-// this thread's run; the owner CTA finds the token whose cumulative weight first exceeds `local`
-// (ascending ids).  CTA-uniform call; uses s_wp, s_claim, s_last.
-__device__ __forceinline__ int draw_in_slice(const float (&w)[kE], float local, bool clamp, float4 *s_wp,
-                                             int *s_claim, int *s_last) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = tid * kE;
-    float tsum = 0.f;
-    int tlast = -1;
+// In place: v <- 2^((v - m) c) against the thread's max m (0 past the end); returns the sum.
+__device__ __forceinline__ float exp_run(float (&v)[kE], float &m, float c) {
+    m = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < kE; ++e) {
-        tsum += w[e];
-        if (w[e] > 0.f) tlast = t0 + e;
+    for (int j = 0; j < kE; ++j) m = fmaxf(m, v[j]);
+    const float mc = m == -INFINITY ? 0.f : m * c;
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < kE; ++j) {
+        v[j] = v[j] == -INFINITY ? 0.f : fast_exp2(fmaf(v[j], c, -mc));
+        s += v[j];
     }
-    float incl = tsum;  // inclusive scan of the run sums within the warp
+    return s;
+}
+
+// ---- fixed point.  Weight sums (probabilities, residuals) are carried as integers in units of
+// 2^-52, so every sum above the chunk level is exact: the same in every thread and CTA that forms
+// it, whatever the order, and consistent between the per-rank totals and a CTA's own scan.
+// A chunk's weight (<= 4 values in [0, 1]) is clamped to [0, 2); NaN maps to 0.  Conversions in
+// both directions use 32-bit integer arithmetic only: 64-bit conversions and doubles run on the
+// (slow) FP64 pipe.
+__device__ __forceinline__ uint64_t to_fx(float x) {
+    if (!(x > 0.f)) return 0ull;
+    const uint32_t bits = __float_as_uint(fminf(x, 1.99999988f));
+    const int ex = int(bits >> 23);  // biased exponent, <= 127
+    if (ex == 0) return 0ull;        // below 2^-126
+    const uint32_t m = (bits & 0x7fffffu) | 0x800000u;  // x = m 2^(ex - 150), fx = m 2^(ex - 98)
+    return ex >= 98 ? (uint64_t(m) << (ex - 98)) : (ex > 74 ? uint64_t(m >> (98 - ex)) : 0ull);
+}
+// A fixed-point value as a float (within 1.5 float ulps; every caller forms a given c the same way).
+__device__ __forceinline__ float fx_to_float(uint64_t v) {
+    return fmaf(__uint2float_rn(uint32_t(v >> 32)), 9.5367431640625e-07f /* 2^-20 */,
+                __uint2float_rn(uint32_t(v)) * 2.220446049250313e-16f /* 2^-52 */);
+}
+// Warp-wide exact sum of values below 2^53 (the result in every lane): two 32-bit reductions
+// of the low 27 bits and of the rest.
+__device__ __forceinline__ uint64_t warp_sum_fx(uint64_t v) {
+    const uint32_t lo = __reduce_add_sync(0xffffffffu, uint32_t(v) & 0x7ffffffu);
+    const uint32_t hi = __reduce_add_sync(0xffffffffu, uint32_t(v >> 27));
+    return (uint64_t(hi) << 27) + lo;
+}
+__device__ __forceinline__ float4 fx_rec(uint64_t v) {
+    return make_float4(__uint_as_float(uint32_t(v)), __uint_as_float(uint32_t(v >> 32)), 0.f, 0.f);
+}
+__device__ __forceinline__ uint64_t rec_fx(float4 r) {
+    return (uint64_t(__float_as_uint(r.y)) << 32) | __float_as_uint(r.x);
+}
+// A chunk's weight: its four weights summed in this order in float, then in fixed point.
+__device__ __forceinline__ uint64_t chunk_weight(float w0, float w1, float w2, float w3) {
+    return to_fx(((w0 + w1) + w2) + w3);
+}
+__device__ __forceinline__ uint64_t clamp53(uint64_t t) { return t < (1ull << 53) ? t : (1ull << 53) - 1; }
+// This thread's weight of (p - c q)+ (a pass of the rejection chain) or of w itself (q == nullptr).
+__device__ __forceinline__ uint64_t residual_fx(const float (&p)[kE], const float (&q)[kE], float c) {
+    uint64_t t = 0;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, incl, off);
+    for (int e = 0; e < kChunks; ++e)
+        t += chunk_weight(fmaxf(fmaf(-c, q[4 * e], p[4 * e]), 0.f), fmaxf(fmaf(-c, q[4 * e + 1], p[4 * e + 1]), 0.f),
+                          fmaxf(fmaf(-c, q[4 * e + 2], p[4 * e + 2]), 0.f), fmaxf(fmaf(-c, q[4 * e + 3], p[4 * e + 3]), 0.f));
+    return clamp53(t);
+}
+__device__ __forceinline__ uint64_t weight_fx(const float (&w)[kE]) {
+    uint64_t t = 0;
+#pragma unroll
+    for (int e = 0; e < kChunks; ++e) t += chunk_weight(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    return clamp53(t);
+}
+
+// floor(u * total) for u in [0, 1) given as a float, exactly (u = mant 2^-sh).
+__device__ __forceinline__ uint64_t scale_fx(uint64_t total, float u) {
+    if (!(u > 0.f)) return 0;
+    const uint32_t ub = __float_as_uint(u);
+    const int ex = int((ub >> 23) & 0xffu);
+    const uint64_t mant = (ub & 0x7fffffu) | (ex ? 0x800000u : 0u);
+    const int sh = 150 - (ex ? ex : 1);  // >= 24 for u < 1
+    const uint64_t lo = total * mant, hi = __umul64hi(total, mant);
+    if (sh >= 128) return 0;
+    if (sh >= 64) return hi >> (sh - 64);
+    return (hi << (64 - sh)) | (lo >> sh);
+}
+
+// Warp-wide merge of (max, scaled sum) pairs: M = max over the lanes, S = sum of s 2^((m - M) c)
+// (the same in every lane: one max reduction, one exponential per lane, a butterfly sum).
+__device__ __forceinline__ float2 ms_fold(float m, float s, float c) {
+    const float M = float_from_order_key(__reduce_max_sync(0xffffffffu, float_order_key(m)));
+    float t = m == -INFINITY ? 0.f : s * fast_exp2((m - M) * c);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    return make_float2(M, t);
+}
+__device__ __forceinline__ float4 ms_fold2(float4 v, float c) {
+    const float2 a = ms_fold(v.x, v.y, c), b = ms_fold(v.z, v.w, c);
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// Owner of a final draw, warp-parallel: lane r < CL holds rank r's weight total (fixed point, 0
+// in the other lanes; ascending rank = ascending token id).  The owner is the rank holding the
+// first cumulative step above u * total; owner = -1 when there is no mass at all; local = the
+// target minus the owner's starting sum.  Same result in every lane.
+template <int CL>
+__device__ __forceinline__ void decide_owner_warp(uint64_t t, float u, int &owner, uint64_t &local) {
+    const int lane = threadIdx.x & 31;
+    uint64_t incl = t;
+#pragma unroll
+    for (int off = 1; off < CL; off <<= 1) {
+        const uint64_t o = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += o;
     }
-    int wl = tlast;
+    const uint64_t total = __shfl_sync(0xffffffffu, incl, CL - 1);
+    owner = -1;
+    local = 0;
+    if (total == 0) return;
+    const uint64_t tgt = scale_fx(total, u);  // < total
+    const uint64_t excl = incl - t;
+    const unsigned m = __ballot_sync(0xffffffffu, lane < CL && excl <= tgt && tgt < incl);
+    owner = __ffs(m) - 1;  // exactly one lane: the steps tile [0, total)
+    local = __shfl_sync(0xffffffffu, tgt - excl, owner);
+}
+
+// Final draw over this CTA's slice (CTA-uniform call): w holds this thread's weights; the draw
+// takes the first token, in ascending id order, whose cumulative weight exceeds `local` (fixed
+// point, relative to the slice).  Column totals and the warp's lane scan are exact; inside the
+// chosen chunk the float partial sums are the ones its chunk weight was formed from.  If `local`
+// lies at or beyond the slice's total (per-rank totals formed from other sums), the last token of
+// positive weight is taken.  Returns the token's offset in the slice in one thread, -1 elsewhere.
+struct DrawSmem {
+    uint64_t col[kWarpsPrep][kChunks];  // per-warp totals of every chunk column
+    uint64_t rem;
+    int pick_col, pick_warp, last;
+};
+__device__ __forceinline__ int draw_in_slice(const float (&w)[kE], uint64_t local, DrawSmem &ds) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int tlast = -1;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) wl = max(wl, __shfl_xor_sync(0xffffffffu, wl, off));
-    __syncthreads();  // s_wp free
-    if (lane == 31) s_wp[warp].x = incl;
-    if (tid == 0) {
-        *s_claim = kPrepThreads;
-        *s_last = -1;
+    for (int e = 0; e < kChunks; ++e) {
+        const uint64_t t = warp_sum_fx(chunk_weight(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]));
+        if (lane == 0) ds.col[warp][e] = t;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (w[4 * e + i] > 0.f) tlast = max(tlast, chunk_tok(e) + i);
     }
+    tlast = __reduce_max_sync(0xffffffffu, tlast + 1) - 1;
+    if (tid == 0) ds.last = -1;
     __syncthreads();
-    if (lane == 0) atomicMax(s_last, wl);
-    float wbase = 0.f;
-    for (int w2 = 0; w2 < warp; ++w2) wbase += s_wp[w2].x;  // this CTA's earlier warps
-    const float excl = wbase + incl - tsum;
-    // the first thread whose run ends above the local target owns the step
-    if (!clamp && tsum > 0.f && excl + tsum > local) atomicMin(s_claim, tid);
-    __syncthreads();
-    int found = -1;
-    if (!clamp && tid == *s_claim) {
-        float acc = excl;
-        found = tlast;
-        bool done = false;
+    if (lane == 0 && tlast >= 0) atomicMax(&ds.last, tlast);
+    if (warp == 0) {
+        // the chunk column holding the target, then the warp within it (same in every lane)
+        uint64_t base = 0, colbase = 0;
+        int col = -1;
 #pragma unroll
-        for (int e = 0; e < kE; ++e) {
-            acc += w[e];
-            if (!done && w[e] > 0.f && acc > local) {
-                found = t0 + e;
-                done = true;
+        for (int e = 0; e < kChunks; ++e) {
+            uint64_t t = 0;
+            for (int w2 = 0; w2 < kWarpsPrep; ++w2) t += ds.col[w2][e];
+            if (col < 0 && local < base + t) {
+                col = e;
+                colbase = base;
+            }
+            base += t;
+        }
+        int wsel = -1;
+        uint64_t rem = 0;
+        if (col >= 0) {
+            uint64_t acc = colbase;
+            for (int w2 = 0; w2 < kWarpsPrep; ++w2) {
+                const uint64_t t = ds.col[w2][col];
+                if (wsel < 0 && local < acc + t) {
+                    wsel = w2;
+                    rem = local - acc;
+                }
+                acc += t;
             }
         }
-    } else if (tid == 0 && (clamp || *s_claim == kPrepThreads)) {
-        found = max(*s_last, 0);
+        if (lane == 0) {
+            ds.pick_col = col;
+            ds.pick_warp = wsel;
+            ds.rem = rem;
+        }
     }
-    return found;  // >= 0 in exactly one thread of the CTA
+    __syncthreads();
+    const int col = ds.pick_col;
+    int found = -1;
+    if (col < 0) {
+        if (tid == 0) found = max(ds.last, 0);
+    } else if (warp == ds.pick_warp) {
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll
+        for (int e = 0; e < kChunks; ++e)
+            if (e == col) {
+                c0 = w[4 * e];
+                c1 = w[4 * e + 1];
+                c2 = w[4 * e + 2];
+                c3 = w[4 * e + 3];
+            }
+        const uint64_t mine = chunk_weight(c0, c1, c2, c3);
+        uint64_t incl = mine;  // inclusive scan over the lanes
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint64_t o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        const uint64_t rem = ds.rem, excl = incl - mine;
+        const unsigned claim = __ballot_sync(0xffffffffu, excl <= rem && rem < incl);
+        if (claim && lane == __ffs(claim) - 1) {
+            // inside the chunk: the float partial sums of its weight, against the remainder
+            const float r = fx_to_float(rem - excl);
+            const float a1 = c0 + c1, a2 = a1 + c2, a3 = a2 + c3;
+            const int t0 = chunk_tok(col);
+            int lastp = -1;
+            if (c0 > 0.f) lastp = 0;
+            if (c1 > 0.f) lastp = 1;
+            if (c2 > 0.f) lastp = 2;
+            if (c3 > 0.f) lastp = 3;
+            int i = (c0 > 0.f && c0 > r) ? 0 : (c1 > 0.f && a1 > r) ? 1 : (c2 > 0.f && a2 > r) ? 2 : (c3 > 0.f && a3 > r) ? 3 : lastp;
+            found = t0 + max(i, 0);
+        } else if (!claim && lane == 0) {
+            found = max(ds.last, 0);  // cannot happen with exact sums; kept as a guard
+        }
+    }
+    return found;
 }
 
 template <int CL>
 __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs a) {
-    __shared__ float4 s_wp[kWarpsPrep];  // per-warp partials of the current pass
-    __shared__ float4 s_recv[2][CL];     // the cluster's records of an exchange, by parity
+    extern __shared__ __align__(16) float s_rows[];  // [2][kSliceMax]: the two held rows' slices
+    __shared__ float4 s_wp[kWarpsPrep];              // per-warp partials of the current pass
+    __shared__ float4 s_recv[2][CL];                 // the cluster's records of an exchange, by parity
     __shared__ __align__(8) uint64_t s_rbar[2];
-    __shared__ int s_kid[kMaxNodes];     // children of the node (sampling), ascending
-    __shared__ int s_nk, s_claim, s_last, s_fail, s_second;
-    __shared__ float s_bc[8];  // broadcasts: maxima, log2 normalisers, next c, c_J
-    __shared__ int s_own[2], s_clamp[2];
-    __shared__ float s_local[2];
+    __shared__ __align__(8) uint64_t s_pbar;     // every warp's partial of the current pass posted
+    __shared__ __align__(8) uint64_t s_lbar[2];  // a row slice landed
+    __shared__ int s_kid[kMaxNodes];             // children of the node (sampling), ascending
+    __shared__ int s_nk, s_fail, s_second;
+    __shared__ int s_own[2];
+    __shared__ uint64_t s_local[2];
+    __shared__ DrawSmem s_draw;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = int(cluster.block_rank());
@@ -265,7 +378,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     const int lo = rank * a.slice;
     const int hi = min(V, lo + a.slice);
     const int cnt = hi > lo ? hi - lo : 0;
-    const int t0 = tid * kE;  // this thread's run, relative to lo
     const int32_t *par = a.parents + size_t(b) * n;
 
     // ---- work of this cluster.  Greedy: nodes 2y and 2y + 1 (argmax of two target rows).
@@ -273,14 +385,23 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     // (in ascending order among the leaves) takes y and the next leaf, an odd-ranked leaf's exits.
     const int y = blockIdx.y;
     const int nodeA = a.greedy ? 2 * y : y;
-    const float *rowA = a.target + (size_t(b) * n + nodeA) * V;
-    const bool vecA = ((V & 3) == 0) && ((lo & 3) == 0) && ((reinterpret_cast<uintptr_t>(rowA) & 15) == 0);
-    float xp[kE], xq[kE];
-    load_run(xp, rowA + lo, t0, cnt, vecA);  // node y's target row is needed in every case
+    const int nrow = a.greedy ? -1 : __ldg(a.node_row + size_t(b) * n + nodeA);
+    // The barriers exist before anything else, and the cluster barrier that publishes them to the
+    // peers is arrived at now and waited on only before the first exchange, so its latency hides
+    // behind the tree scan, the slice copies and the first register pass.
+    if (tid == 0) {
+        mbar_init(&s_rbar[0], 1);
+        mbar_init(&s_rbar[1], 1);
+        mbar_init(&s_pbar, kWarpsPrep);
+        mbar_init(&s_lbar[0], 1);
+        mbar_init(&s_lbar[1], 1);
+        fence_barrier_init();
+    }
+    cluster_arrive();
     if (warp == 0) {
         // every node's "has children" bit, and the children of node y, from the <= 64 parents
-        const int p0 = lane < n ? par[lane] : -1;
-        const int p1 = lane + 32 < n ? par[lane + 32] : -1;
+        const int p0 = lane < n ? __ldg(par + lane) : -1;
+        const int p1 = lane + 32 < n ? __ldg(par + lane + 32) : -1;
         uint64_t mine = 0;
         if (lane > 0 && p0 >= 0 && p0 < n) mine |= 1ull << p0;
         if (p1 >= 0 && p1 < n) mine |= 1ull << p1;
@@ -308,87 +429,160 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
             if (a.greedy) second = 2 * y + 1 < n ? 2 * y + 1 : -1;
             s_second = second;
             s_fail = 0;
+            s_own[0] = s_own[1] = -1;
         }
     }
     __syncthreads();
     const int second = s_second;
-    if (second == -2) return;  // uniform for the cluster: no barrier has been touched yet
+    if (second == -2) return;  // uniform for the cluster: no exchange or copy has started
     const int J = a.greedy ? 0 : s_nk;
     const bool pair = J == 0;  // a leaf pair (sampling) or a node pair (greedy)
     const int nodeB = pair ? second : -1;
-    const int rowq = J > 0 ? a.node_row[size_t(b) * n + nodeA] : -1;
+    const int rowq = J > 0 ? nrow : -1;
     const bool has_q = J > 0 && rowq >= 0 && rowq < a.R;
-    if (tid == 0) {
-        mbar_init(&s_rbar[0], 1);
-        mbar_init(&s_rbar[1], 1);
-        fence_barrier_init();
-    }
-    cluster_arrive();  // peers may push records only after these barriers exist (wait below)
+    const float *rowA = a.target + (size_t(b) * n + nodeA) * V + lo;
     const float *rowB = nullptr;
-    if (nodeB >= 0) rowB = a.target + (size_t(b) * n + nodeB) * V;
-    else if (has_q) rowB = a.draft + (size_t(b) * a.R + rowq) * V;
-    if (rowB) load_run(xq, rowB + lo, t0, cnt, vecA && (reinterpret_cast<uintptr_t>(rowB) & 15) == 0);
+    if (nodeB >= 0) rowB = a.target + (size_t(b) * n + nodeB) * V + lo;
+    else if (has_q) rowB = a.draft + (size_t(b) * a.R + rowq) * V + lo;
+    // whole slices by bulk copy into shared memory (16-byte aligned rows of a multiple of 4 floats)
+    auto bulk_ok = [&](const float *r) {
+        return r && ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(r) & 15) == 0) && cnt > 0;
+    };
+    const bool bulkA = bulk_ok(rowA), bulkB = bulk_ok(rowB);
+    if (tid == 0) {
+        if (bulkA) {
+            mbar_expect_tx(&s_lbar[0], uint32_t(cnt) * 4u);
+            bulk_g2s(s_rows, rowA, uint32_t(cnt) * 4u, &s_lbar[0]);
+        }
+        if (bulkB) {
+            mbar_expect_tx(&s_lbar[1], uint32_t(cnt) * 4u);
+            bulk_g2s(s_rows + kSliceMax, rowB, uint32_t(cnt) * 4u, &s_lbar[1]);
+        }
+    }
     // every final draw uses the sequence's first uniform (the root's, which no accept test uses)
-    const float uA = __ldg(a.uniforms + size_t(b) * n), uB = uA;
-    cluster_wait();
+    const float uA = __ldg(a.uniforms + size_t(b) * n);
+    float xp[kE], xq[kE];
+    if (!bulkA) load_chunks(xp, rowA, cnt);
+    if (rowB && !bulkB) load_chunks(xq, rowB, cnt);
+    // A slice copy that does not land marks the CTA failed; the CTA still waits (bounded) for it
+    // before it can leave, as the copy writes into its shared memory.
+    auto wait_slice = [&](int i) {
+        bool got = false;
+        for (uint32_t it = 0; it < (1u << 22) && !got; ++it) got = __all_sync(0xffffffffu, mbar_try_wait(&s_lbar[i], 0));
+        if (!got && lane == 0) {
+            s_fail = 1;
+            set_status(a.status, EAGLE_ERR_TIMEOUT);
+        }
+    };
+    if (bulkA) {
+        wait_slice(0);
+        read_chunks(xp, s_rows, cnt);
+    }
+    if (bulkB) {
+        wait_slice(1);
+        read_chunks(xq, s_rows + kSliceMax, cnt);
+    }
 
-    // One exchange, executed by warp 0 (all lanes): rec (valid in lane 0) goes to every CTA; on
-    // return lanes r < CL hold rank r's record.  A receive that times out marks the CTA failed
-    // (its results are then not written).
-    int xch = 0;
-    auto exchange = [&](float4 rec, float4 neutral) -> float4 {
+    // One pass = one exchange.  Every warp leaves its partial in s_wp[warp] and arrives on s_pbar;
+    // warp 0 waits for all sixteen, folds them into the CTA's record and pushes it to every CTA of
+    // the cluster; then each warp that needs the pass's totals waits for the CL records itself and
+    // folds them in rank order (identical in every thread of the cluster), so a pass costs no
+    // CTA-wide barrier and no broadcast.  A wait that runs out marks the CTA failed (its results
+    // are then not written) and later waits return at once.
+    int xch = 0, nposts = 0;  // exchanges received, posts waited on
+    auto failed = [&]() { return __any_sync(0xffffffffu, *reinterpret_cast<volatile int *>(&s_fail) != 0); };
+    auto fail = [&]() {
+        if (lane == 0) {
+            s_fail = 1;
+            set_status(a.status, EAGLE_ERR_TIMEOUT);
+        }
+    };
+    auto post = [&](float4 v) {  // lane 0's v: this warp's partial
+        if (lane == 0) {
+            s_wp[warp] = v;
+            mbar_arrive(&s_pbar);
+        }
+    };
+    auto wait_posts = [&]() -> bool {  // warp 0
+        bool got = false;
+        if (!failed())
+            for (uint32_t it = 0; it < (1u << 22) && !got; ++it)
+                got = __all_sync(0xffffffffu, mbar_try_wait(&s_pbar, nposts & 1));
+        ++nposts;
+        if (!got) fail();
+        return got;
+    };
+    auto send = [&](float4 rec) {  // warp 0, rec the same in every lane
         const int slot = xch & 1;
-        rec = shfl4(rec, 0);
         if (lane == 0) mbar_expect_tx(&s_rbar[slot], CL * 16);
         __syncwarp();
         if (lane < CL)
             st_async_v4(mapa_u32(static_cast<uint32_t>(__cvta_generic_to_shared(&s_recv[slot][rank])), lane), rec,
                         mapa_u32(static_cast<uint32_t>(__cvta_generic_to_shared(&s_rbar[slot])), lane));
+    };
+    auto wait_recv = [&]() -> bool {  // the CL records of the current exchange are in s_recv
+        const int slot = xch & 1;
         bool got = false;
-        for (uint32_t it = 0; it < (1u << 22) && !got; ++it)
-            got = __all_sync(0xffffffffu, mbar_try_wait(&s_rbar[slot], (xch >> 1) & 1));
+        if (!failed())
+            for (uint32_t it = 0; it < (1u << 22) && !got; ++it)
+                got = __all_sync(0xffffffffu, mbar_try_wait(&s_rbar[slot], (xch >> 1) & 1));
         ++xch;
-        if (!got) {
-            if (lane == 0) {
-                s_fail = 1;
-                set_status(a.status, EAGLE_ERR_TIMEOUT);
-            }
-            return neutral;
-        }
-        return lane < CL ? s_recv[slot][lane] : neutral;
+        if (!got) fail();
+        return got;
+    };
+    // exact sums of fixed-point records: the sixteen warp partials, the CL CTA records
+    auto fold_posts = [&]() {
+        uint64_t t = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < kWarpsPrep; ++w2) t += rec_fx(s_wp[w2]);
+        return t;
+    };
+    auto recv_fx = [&]() -> uint64_t {  // the exchange's total; its records stay in s_recv
+        const int slot = xch & 1;
+        uint64_t t = 0;
+        if (wait_recv())
+#pragma unroll
+            for (int r = 0; r < CL; ++r) t += rec_fx(s_recv[slot][r]);
+        return t;
     };
 
     if (a.greedy) {
         // argmax of the two target rows (ties to the lower id): thread, warp, CTA, cluster
         uint64_t ba = 0, bb = 0;
 #pragma unroll
-        for (int j = 0; j < kE; ++j) {
-            const uint32_t t = uint32_t(lo + t0 + j);
-            const uint64_t ka = xp[j] == -INFINITY ? 0ull : topk_key(xp[j], t);
-            ba = ka > ba ? ka : ba;
-            if (nodeB >= 0) {
-                const uint64_t kb = xq[j] == -INFINITY ? 0ull : topk_key(xq[j], t);
-                bb = kb > bb ? kb : bb;
+        for (int e = 0; e < kChunks; ++e)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = 4 * e + i;
+                const uint32_t t = uint32_t(lo + chunk_tok(e) + i);
+                const uint64_t ka = xp[j] == -INFINITY ? 0ull : topk_key(xp[j], t);
+                ba = ka > ba ? ka : ba;
+                if (nodeB >= 0) {
+                    const uint64_t kb = xq[j] == -INFINITY ? 0ull : topk_key(xq[j], t);
+                    bb = kb > bb ? kb : bb;
+                }
             }
-        }
         ba = warp_max_u64(ba);
         bb = warp_max_u64(bb);
-        if (lane == 0)
-            s_wp[warp] = make_float4(__uint_as_float(uint32_t(ba)), __uint_as_float(uint32_t(ba >> 32)),
-                                     __uint_as_float(uint32_t(bb)), __uint_as_float(uint32_t(bb >> 32)));
-        __syncthreads();
+        cluster_wait();  // every peer's barriers exist
+        post(make_float4(__uint_as_float(uint32_t(ba)), __uint_as_float(uint32_t(ba >> 32)),
+                         __uint_as_float(uint32_t(bb)), __uint_as_float(uint32_t(bb >> 32))));
         if (warp == 0) {
             uint64_t ga = 0, gb = 0;
-            if (lane < kWarpsPrep) {
-                const float4 v = s_wp[lane];
-                ga = (uint64_t(__float_as_uint(v.y)) << 32) | __float_as_uint(v.x);
-                gb = (uint64_t(__float_as_uint(v.w)) << 32) | __float_as_uint(v.z);
+            if (wait_posts()) {
+                if (lane < kWarpsPrep) {
+                    const float4 v = s_wp[lane];
+                    ga = (uint64_t(__float_as_uint(v.y)) << 32) | __float_as_uint(v.x);
+                    gb = (uint64_t(__float_as_uint(v.w)) << 32) | __float_as_uint(v.z);
+                }
+                ga = warp_max_u64(ga);
+                gb = warp_max_u64(gb);
+                send(make_float4(__uint_as_float(uint32_t(ga)), __uint_as_float(uint32_t(ga >> 32)),
+                                 __uint_as_float(uint32_t(gb)), __uint_as_float(uint32_t(gb >> 32))));
             }
-            ga = warp_max_u64(ga);
-            gb = warp_max_u64(gb);
-            const float4 v = exchange(make_float4(__uint_as_float(uint32_t(ga)), __uint_as_float(uint32_t(ga >> 32)),
-                                                  __uint_as_float(uint32_t(gb)), __uint_as_float(uint32_t(gb >> 32))),
-                                      make_float4(0.f, 0.f, 0.f, 0.f));
+            const int slot = xch & 1;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (wait_recv() && lane < CL) v = s_recv[slot][lane];
             ga = (uint64_t(__float_as_uint(v.y)) << 32) | __float_as_uint(v.x);
             gb = (uint64_t(__float_as_uint(v.w)) << 32) | __float_as_uint(v.z);
             ga = warp_max_u64(ga);
@@ -404,60 +598,49 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     }
 
     const float c = a.c;
-    // ---- row statistics of both held rows.  Values become 2^((x - m) c) against the run's max
+    // ---- row statistics of both held rows.  Values become 2^((x - m) c) against the thread's max
     // m, so the probabilities later cost one multiply each (no second exponential).
     float mA, mB = -INFINITY, sB = 0.f;
     const float sA = exp_run(xp, mA, c);
     if (rowB) sB = exp_run(xq, mB, c);
+    cluster_wait();  // every peer's barriers exist
     {
-        const float4 wv = warp_ms_merge(make_float4(mA, sA, mB, sB), c);
-        if (lane == 0) s_wp[warp] = wv;
-        __syncthreads();
-        if (warp == 0) {
-            const float4 neutral = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-            const float4 cta = warp_ms_merge(lane < kWarpsPrep ? s_wp[lane] : neutral, c);
-            const float4 mine = exchange(cta, neutral);  // lane r < CL: rank r's record
-            const float4 g = warp_ms_merge(mine, c);
-            const float l2A = g.y > 0.f ? log2f(g.y) : 0.f;
-            const float l2B = g.w > 0.f ? log2f(g.w) : 0.f;
-            // per-rank probability totals of both rows (the final draws' weights, for leaves)
-            const float trA = lane < CL && mine.x != -INFINITY ? mine.y * exp2f((mine.x - g.x) * c - l2A) : 0.f;
-            const float trB = lane < CL && mine.z != -INFINITY ? mine.w * exp2f((mine.z - g.z) * c - l2B) : 0.f;
-            FF tA[CL], tB[CL];
-#pragma unroll
-            for (int r = 0; r < CL; ++r) {
-                tA[r] = ff_from(__shfl_sync(0xffffffffu, trA, r), 0.f);
-                tB[r] = ff_from(__shfl_sync(0xffffffffu, trB, r), 0.f);
-            }
+        const float4 neutral = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+        post(ms_fold2(make_float4(mA, sA, mB, sB), c));
+        if (warp == 0 && wait_posts()) send(ms_fold2(lane < kWarpsPrep ? s_wp[lane] : neutral, c));
+        const int slot = xch & 1;
+        const bool ok = wait_recv();
+        const float4 mine = ok && lane < CL ? s_recv[slot][lane] : neutral;  // lane r < CL: rank r's record
+        const float4 g = ms_fold2(mine, c);
+        const float l2A = g.y > 0.f ? log2f(g.y) : 0.f;
+        const float l2B = g.w > 0.f ? log2f(g.w) : 0.f;
+        // side work off warp 0 (which gathers the next pass): the leaves' draw owners from the
+        // per-rank probability totals, and the node's row statistics
+        if ((warp == 1 && !has_q) || (warp == 2 && nodeB >= 0)) {
+            const int k = warp - 1;
+            const float m = k ? mine.z : mine.x, sm = k ? mine.w : mine.y, M = k ? g.z : g.x, l2 = k ? l2B : l2A;
+            const float tr = m == -INFINITY ? 0.f : sm * fast_exp2((m - M) * c - l2);
+            int own;
+            uint64_t loc;
+            decide_owner_warp<CL>(lane < CL ? to_fx(tr) : 0ull, uA, own, loc);
             if (lane == 0) {
-                s_bc[0] = g.x;
-                s_bc[1] = l2A;
-                s_bc[2] = g.z;
-                s_bc[3] = l2B;
-                s_bc[4] = 1.f;  // c_1 = c_0 + S_0
-                s_bc[5] = 0.f;
-                s_own[0] = s_own[1] = -1;
-                s_clamp[0] = s_clamp[1] = 0;
-                if (!has_q) decide_owner<CL>(tA, uA, s_own[0], s_clamp[0], s_local[0]);
-                if (nodeB >= 0) decide_owner<CL>(tB, uB, s_own[1], s_clamp[1], s_local[1]);
-                if (rank == 0 && J > 0 && !s_fail) {
-                    NodeStat *st = a.stat + size_t(b) * n + nodeA;
-                    st->mp = g.x;
-                    st->mq = g.z;
-                    st->lnsp = log_fast(double(g.y));
-                    st->lnsq = has_q && g.w > 0.f ? log_fast(double(g.w)) : 0.0;
-                }
+                s_own[k] = own;
+                s_local[k] = loc;
             }
         }
-        __syncthreads();
-    }
-    {
-        // probabilities: p = 2^((x - m) c) * 2^((m - M) c - log2 S), one exponential per run
-        const float fA = mA == -INFINITY ? 0.f : fast_exp2(fmaf(mA - s_bc[0], c, -s_bc[1]));
+        if (warp == 3 && lane == 0 && rank == 0 && J > 0 && !s_fail) {
+            NodeStat *st = a.stat + size_t(b) * n + nodeA;
+            st->mp = g.x;
+            st->mq = g.z;
+            st->lnsp = logf(g.y);
+            st->lnsq = has_q && g.w > 0.f ? logf(g.w) : 0.f;
+        }
+        // probabilities: p = 2^((x - m) c) * 2^((m - M) c - log2 S), one exponential per thread
+        const float fA = mA == -INFINITY ? 0.f : fast_exp2(fmaf(mA - g.x, c, -l2A));
 #pragma unroll
         for (int j = 0; j < kE; ++j) xp[j] *= fA;
         if (rowB) {
-            const float fB = mB == -INFINITY ? 0.f : fast_exp2(fmaf(mB - s_bc[2], c, -s_bc[3]));
+            const float fB = mB == -INFINITY ? 0.f : fast_exp2(fmaf(mB - g.z, c, -l2B));
 #pragma unroll
             for (int j = 0; j < kE; ++j) xq[j] *= fB;
         }
@@ -465,91 +648,112 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
 
     // ---- rejection chain of a node with children: c_0 = 0, S_0 = 1; after rejecting child j:
     // c_{j+1} = c_j + S_j and S_{j+1} = sum (p0 - c_{j+1} q)+ (a zero sum keeps the previous
-    // distribution).  Lane 0 of warp 0 carries c_j, S_j in float-float; every thread sees c_{j+1}
-    // rounded to float.  When the last pass moves c, its per-rank sums are exactly the final
-    // draw's per-rank weights.
-    FF cj = ff_from(0.f, 0.f), Sj = ff_from(1.f, 0.f);  // meaningful in lane 0 of warp 0
+    // distribution).  c_j and S_j are fixed-point integers, the same in every thread; each pass
+    // uses c_{j+1} rounded to float.  When the last pass moves c, its per-rank sums are exactly
+    // the final draw's per-rank weights: the residual below is formed with the same float c.
+    uint64_t cj = 0, Sj = 1ull << 52;
+    float cnf = 1.f;  // c_1 = c_0 + S_0
     bool decided = !has_q;
     for (int j = 0; j < J && has_q; ++j) {
-        if (rank == 0 && warp == 0 && lane == 0 && !s_fail) {  // the child tested at step j
+        if (rank == 0 && tid == 0 && !s_fail) {  // the child tested at step j
             NodeStat *st = a.stat + size_t(b) * n + s_kid[j];
-            st->cj = double(cj.hi) + double(cj.lo);
-            st->sj = double(Sj.hi) + double(Sj.lo);
+            st->cj = cj;
+            st->sj = Sj;
         }
-        const float cnf = s_bc[4];
-        float part = 0.f;
+        // the last pass forms exact chunk weights (they may become the final draw's); earlier
+        // passes need only the sum: one float sum per thread
+        uint64_t part;
+        if (j == J - 1) {
+            part = residual_fx(xp, xq, cnf);
+        } else {
+            float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;  // four chains of dependent adds
 #pragma unroll
-        for (int e = 0; e < kE; ++e) part += fmaxf(fmaf(-cnf, xq[e], xp[e]), 0.f);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (lane == 0) s_wp[warp].x = part;
-        __syncthreads();
-        if (warp == 0) {
-            FF t = ff_from(lane < kWarpsPrep ? s_wp[lane].x : 0.f, 0.f);
-            t = ff_warp_sum(t);
-            const float4 mine = exchange(make_float4(t.hi, t.lo, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
-            const FF g = ff_warp_sum(ff_from(mine.x, mine.y));
-            FF tot[CL];
-#pragma unroll
-            for (int r = 0; r < CL; ++r) tot[r] = ff_from(__shfl_sync(0xffffffffu, mine.x, r), __shfl_sync(0xffffffffu, mine.y, r));
-            const bool moved = g.hi > 0.f;
-            if (moved) {
-                cj = ff_add(cj, Sj);
-                Sj = g;
+            for (int e = 0; e < kE; e += 4) {
+                t0 += fmaxf(fmaf(-cnf, xq[e], xp[e]), 0.f);
+                t1 += fmaxf(fmaf(-cnf, xq[e + 1], xp[e + 1]), 0.f);
+                t2 += fmaxf(fmaf(-cnf, xq[e + 2], xp[e + 2]), 0.f);
+                t3 += fmaxf(fmaf(-cnf, xq[e + 3], xp[e + 3]), 0.f);
             }
-            if (lane == 0) {
-                const FF nx = ff_add(cj, Sj);
-                s_bc[4] = nx.hi + nx.lo;
-                s_bc[5] = cj.hi + cj.lo;
-                if (j == J - 1 && moved) decide_owner<CL>(tot, uA, s_own[0], s_clamp[0], s_local[0]);
-            }
-            decided = j == J - 1 && moved;
+            part = to_fx((t0 + t1) + (t2 + t3));
         }
-        __syncthreads();
+        post(fx_rec(warp_sum_fx(part)));
+        if (warp == 0 && wait_posts()) send(fx_rec(fold_posts()));
+        const int slot = xch & 1;
+        const uint64_t g = recv_fx();
+        const bool moved = g > 0;
+        if (moved) {
+            cj += Sj;
+            Sj = g;
+        }
+        cnf = fx_to_float(cj + Sj);
+        if (j == J - 1) {
+            decided = moved;
+            if (moved && warp == 0) {
+                int own;
+                uint64_t loc;
+                decide_owner_warp<CL>(lane < CL ? rec_fx(s_recv[slot][lane]) : 0ull, uA, own, loc);
+                if (lane == 0) {
+                    s_own[0] = own;
+                    s_local[0] = loc;
+                }
+            }
+        }
     }
-    const float cjf = s_bc[5];
+    // residual weights of a node with children: (p0 - c_J q)+, with c_J as the pass that set it
+    // rounded it
     if (has_q) {
-        decided = __shfl_sync(0xffffffffu, decided ? 1 : 0, 0) != 0;  // warp 0's verdict ...
-        if (warp == 0 && lane == 0) s_nk = decided ? 1 : 0;             // ... for the whole CTA
-        __syncthreads();
-        decided = s_nk != 0;
-    }
-    // residual weights of a node with children: (p0 - c_J q)+
-    if (has_q) {
+        const float cjf = fx_to_float(cj);
 #pragma unroll
         for (int e = 0; e < kE; ++e) xp[e] = fmaxf(fmaf(-cjf, xq[e], xp[e]), 0.f);
     }
     if (has_q && !decided) {
         // the last pass left c unchanged: one more exchange for the residual's per-rank weights
-        float part = 0.f;
-#pragma unroll
-        for (int e = 0; e < kE; ++e) part += xp[e];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        if (lane == 0) s_wp[warp].x = part;
-        __syncthreads();
+        post(fx_rec(warp_sum_fx(weight_fx(xp))));
         if (warp == 0) {
-            FF t = ff_from(lane < kWarpsPrep ? s_wp[lane].x : 0.f, 0.f);
-            t = ff_warp_sum(t);
-            const float4 mine = exchange(make_float4(t.hi, t.lo, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
-            FF tot[CL];
-#pragma unroll
-            for (int r = 0; r < CL; ++r) tot[r] = ff_from(__shfl_sync(0xffffffffu, mine.x, r), __shfl_sync(0xffffffffu, mine.y, r));
-            if (lane == 0) decide_owner<CL>(tot, uA, s_own[0], s_clamp[0], s_local[0]);
+            if (wait_posts()) send(fx_rec(fold_posts()));
+            const int slot = xch & 1;
+            recv_fx();
+            int own;
+            uint64_t loc;
+            decide_owner_warp<CL>(lane < CL ? rec_fx(s_recv[slot][lane]) : 0ull, uA, own, loc);
+            if (lane == 0) {
+                s_own[0] = own;
+                s_local[0] = loc;
+            }
         }
-        __syncthreads();
     }
     // every record this CTA sends has been sent: the closing cluster barrier can start
     cluster_arrive();
+    __syncthreads();  // the draw decisions are visible
 
-    // ---- final draws: node A over xp (probabilities or residual), leaf B over xq
+    // ---- final draws: node A over xp (probabilities or residual), leaf B over xq.  Leaf B's weights
+    // wait in this thread's own chunks of the second slice buffer (its copy was consumed), so one
+    // draw instance serves both and only one row is live in registers.
+    if (nodeB >= 0) {
+        float *dst = s_rows + kSliceMax;
+#pragma unroll
+        for (int e = 0; e < kChunks; ++e)
+            *reinterpret_cast<float4 *>(dst + chunk_tok(e)) = make_float4(xq[4 * e], xq[4 * e + 1], xq[4 * e + 2], xq[4 * e + 3]);
+    }
     for (int k = 0; k < (nodeB >= 0 ? 2 : 1); ++k) {
         const int owner = s_own[k];
         const int node = k ? nodeB : nodeA;
+        if (k == 1) {
+            __syncthreads();  // every thread is done with the first draw's shared state
+            const float *src = s_rows + kSliceMax;
+#pragma unroll
+            for (int e = 0; e < kChunks; ++e) {
+                const float4 v = *reinterpret_cast<const float4 *>(src + chunk_tok(e));
+                xp[4 * e] = v.x;
+                xp[4 * e + 1] = v.y;
+                xp[4 * e + 2] = v.z;
+                xp[4 * e + 3] = v.w;
+            }
+        }
         if (owner < 0) {
             if (rank == 0 && tid == 0 && !s_fail) a.final_tok[size_t(b) * n + node] = 0;  // no positive mass
         } else if (rank == owner) {
-            const int found = draw_in_slice(k ? xq : xp, s_local[k], s_clamp[k] != 0, s_wp, &s_claim, &s_last);
+            const int found = draw_in_slice(xp, s_local[k], s_draw);
             if (found >= 0 && !s_fail) a.final_tok[size_t(b) * n + node] = lo + found;
         }
     }
@@ -557,83 +761,82 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
 }
 
 __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
-    __shared__ int s_tok[64], s_par[64], s_row[64], s_fin[64];
-    __shared__ float s_u[64], s_ratio[64];
+    __shared__ int s_tok[64], s_par[64], s_row[64], s_fin[64], s_next[64];
     __shared__ int s_bad;
     const int b = blockIdx.x, tid = threadIdx.x;
     const int n = a.n, D = a.D;
-    if (tid == 0) s_bad = 0;
-    __syncthreads();
-    if (tid < n) {
+    int t = 0, p = -1;
+    float u = 0.f;
+    if (tid < n) {  // every load of the node's own inputs at once
         const size_t o = size_t(b) * n + tid;
-        const int t = a.tokens[o], p = a.parents[o];
-        s_tok[tid] = t;
-        s_par[tid] = p;
+        t = a.tokens[o];
+        p = a.parents[o];
+        u = a.uniforms[o];
         s_row[tid] = a.node_row[o];
         s_fin[tid] = a.final_tok[o];
-        s_u[tid] = a.uniforms[o];
-        bool bad = t < 0 || t >= a.V;
+    }
+    s_next[tid] = n;  // no accepted child (yet)
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    bool bad = false;
+    if (tid < n) {
+        s_tok[tid] = t;
+        s_par[tid] = p;
+        bad = t < 0 || t >= a.V;
         bad |= tid == 0 ? p != -1 : (p < 0 || p >= tid);
-        if (bad) s_bad = 1;
     }
+    if (bad) s_bad = 1;
     __syncthreads();
-    if (!a.greedy && tid > 0 && tid < n && !s_bad) {
-        const int p = s_par[tid];
-        if (s_row[p] < 0 || s_row[p] >= a.R) s_bad = 1;
-    }
+    if (!a.greedy && tid > 0 && tid < n && !s_bad && (s_row[p] < 0 || s_row[p] >= a.R)) s_bad = 1;
     __syncthreads();
-    // accept ratio of every child (one thread per node, double precision):
-    //   p0 = exp((x - Mp)/T - ln Sp), q0 = exp((y - Mq)/T - ln Sq) at the child's token, then
-    //   (p0 - c_j q0)+ / (S_j q0) for the child tested after j rejected siblings (p0 / q0 first)
+    // accept ratio of every child (one thread per node, double precision).  With the parent's
+    // row statistics, p0 / q0 = exp(((x - Mp) - (y - Mq)) / T - ln Sp + ln Sq) at the child's
+    // token; the child tested after j rejected siblings has ratio (p0 / q0 - c_j)+ / S_j
+    // (p0 / q0 itself for j = 0), as p_j / q = (p0 - c_j q)+ / (S_j q).
+    const bool ok = !s_bad;
+    bool acc = false;
     if (tid < n) {
         float r = NAN;
-        if (!a.greedy && !s_bad && tid > 0) {
-            const int p = s_par[tid], t = s_tok[tid];
+        if (!a.greedy && ok && tid > 0) {
             int sib = 0;
             for (int j = p + 1; j < tid; ++j) sib += s_par[j] == p;
             const NodeStat ps = a.stat[size_t(b) * n + p];
             const NodeStat cs = a.stat[size_t(b) * n + tid];
             const double x = a.target[(size_t(b) * n + p) * a.V + t];
             const double yv = a.draft[(size_t(b) * a.R + s_row[p]) * a.V + t];
-            const double p0 = exp((x - double(ps.mp)) * a.inv_td - ps.lnsp);
-            const double q0 = exp((yv - double(ps.mq)) * a.inv_td - ps.lnsq);
-            const double num = sib == 0 ? p0 : fmax(p0 - cs.cj * q0, 0.0);
-            const double den = cs.sj * q0;
-            r = den > 0.0 ? float(num / den) : INFINITY;
+            const double lp = (x - double(ps.mp)) * a.inv_td - double(ps.lnsp);
+            const double lq = (yv - double(ps.mq)) * a.inv_td - double(ps.lnsq);
+            const double rr = exp(lp - lq);
+            if (sib == 0) {
+                r = float(rr);
+            } else {
+                const double sj = double(cs.sj) * kFxInv;
+                r = sj > 0.0 ? float(fmax(rr - double(cs.cj) * kFxInv, 0.0) / sj) : INFINITY;
+            }
+            acc = u < r;
+        } else if (a.greedy && ok && tid > 0) {
+            acc = t == s_fin[p];
         }
-        s_ratio[tid] = r;
         if (a.out_ratio) a.out_ratio[size_t(b) * n + tid] = r;
     }
+    // each parent's first accepted child (children in index order)
+    if (acc) atomicMin(&s_next[p], tid);
     __syncthreads();
+    if (tid != 0) return;
     int32_t *ot = a.out_tokens + size_t(b) * (D + 1);
     int32_t *op = a.out_path + size_t(b) * D;
-    if (tid != 0) return;
     for (int j = 0; j <= D; ++j) ot[j] = -1;
     for (int j = 0; j < D; ++j) op[j] = -1;
-    if (s_bad) {
+    if (!ok) {
         set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
         a.out_len[b] = 0;
         return;
     }
     int node = 0, len = 0;
     for (;;) {
-        int next = -1;
-        if (a.greedy) {
-            const int g = s_fin[node];
-            for (int j = node + 1; j < n; ++j)
-                if (s_par[j] == node && s_tok[j] == g) {
-                    next = j;
-                    break;
-                }
-        } else {
-            for (int j = node + 1; j < n; ++j)
-                if (s_par[j] == node && s_u[j] < s_ratio[j]) {
-                    next = j;
-                    break;
-                }
-        }
-        if (next < 0 || len >= D) {
-            if (next >= 0) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);  // tree deeper than D
+        const int next = s_next[node];
+        if (next >= n || len >= D) {
+            if (next < n) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);  // tree deeper than D
             ot[len++] = s_fin[node];
             break;
         }
@@ -656,16 +859,23 @@ size_t tree_verify_workspace_bytes(const eagle_verify_cfg &c) {
 namespace {
 template <int CL>
 cudaError_t launch_prep(const VerifyArgs &a, int clusters, int batch, cudaStream_t stream) {
-    static bool attr = false;
-    if (!attr && CL > 8) {
-        cudaError_t e = cudaFuncSetAttribute(verify_prep_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    // function attributes are per device: set them once for each device this process launches on
+    static std::atomic<uint64_t> ready{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (!bit || !(ready.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(verify_prep_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(kPrepSmem));
+        if (e == cudaSuccess && CL > 8)
+            e = cudaFuncSetAttribute(verify_prep_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
+        ready.fetch_or(bit);
     }
-    attr = true;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CL, clusters, batch);
     cfg.blockDim = dim3(kPrepThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = kPrepSmem;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;

@@ -9,7 +9,7 @@
 
 namespace {
 
-constexpr size_t kVerifyScratchBytes = size_t(256) << 10;  // 256 KB: B x n <= 5034 tree nodes
+constexpr size_t kVerifyScratchBytes = size_t(256) << 10;  // 256 KB: B x n <= 7272 tree nodes
 constexpr int kMaxDevices = 64;
 
 // The scratch itself: file-scope device storage, zero-filled when the module is loaded.  Only its

@@ -55,22 +55,20 @@ struct RowArgs {
     double inv_t;       // 1 / tree_temp
 };
 
-// KMAX-th largest key of the warp's 32 lane keys (bitonic sort across lanes, descending).
-template <int KMAX>
-__device__ __forceinline__ uint64_t warp_kth_key(uint64_t v) {
+// The warp's 32 lane keys sorted descending across the lanes (bitonic network).
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             const uint64_t o = shfl_xor_u64(v, stride);
-            const bool up = (lane & size) == 0;         // this pair sorts descending when up
-            const bool lower = (lane & stride) == 0;    // this lane holds the earlier position
-            const bool keep_max = (up == lower);
-            v = keep_max ? (o > v ? o : v) : (o < v ? o : v);
+            const bool up = (lane & size) == 0;       // this pair sorts descending when up
+            const bool lower = (lane & stride) == 0;  // this lane holds the earlier position
+            v = (up == lower) ? (o > v ? o : v) : (o < v ? o : v);
         }
     }
-    return __shfl_sync(0xffffffffu, v, KMAX - 1);
+    return v;
 }
 
 // Fold `count` descending 16-key lists (zero padded) stored in buf[0][0..count) into buf[?][0]
@@ -97,6 +95,7 @@ __device__ __forceinline__ int tree_merge16(uint64_t (*buf)[kRowWarps][16], int 
 
 __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
     __shared__ uint64_t s_lists[2][kRowWarps][16];
+    __shared__ unsigned long long s_bound;  // CTA-wide lower bound of the slice's 16th key
     __shared__ float2 s_ms[kRowWarps];
     __shared__ uint64_t s_blk[16];  // this CTA's list, read by the cluster's rank 0
     __shared__ float2 s_blkms;
@@ -114,22 +113,20 @@ __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
 
     float m = -INFINITY, s = 0.f;
     WarpTopK<16> top;
-    uint64_t seed = 0;  // per-warp lower bound of the warp's top-16, from its first batch
+    uint64_t seed = 0;  // CTA-wide lower bound of the slice's top-16, from the first batch
     bool seeded = false;
 
-    // One batch: kRowVals values per thread.  Statistics in registers, then the top-16 offer:
-    // a value can only be in the warp's top-16 if its key reaches both the warp's current 16th
-    // key and the seed (the 16th largest lane maximum of the first batch: 16 distinct values at
-    // or above it are known).
+    // One batch: kRowVals values per thread.  Statistics in registers, then the top-16 offer: a
+    // value can only be in the slice's top-16 if its key reaches the bound, the larger of the
+    // seed (the 16th largest of the CTA's 512 thread maxima of the first batch, found by sorting
+    // each warp's lane maxima and merging the sixteen top halves) and the largest of the warps'
+    // current 16th keys, which the warps publish with atomicMax: 16 distinct keys at or above
+    // either are known.  A lane offers values only when its batch maximum reaches the bound (one
+    // vote per batch).  The first batch is CTA-uniform (block barriers inside the seed).
     auto batch = [&](const float (&x)[kRowVals], const int (&tk)[kRowVals]) {
         float mx = x[0];
-        int tmx = tk[0];
 #pragma unroll
-        for (int j = 1; j < kRowVals; ++j)
-            if (x[j] > mx) {
-                mx = x[j];
-                tmx = tk[j];
-            }
+        for (int j = 1; j < kRowVals; ++j) mx = fmaxf(mx, x[j]);
         if (mx > m) {
             s = (m == -INFINITY) ? 0.f : s * fast_exp2((m - mx) * c);
             m = mx;
@@ -140,11 +137,23 @@ __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
             for (int j = 0; j < kRowVals; ++j) s += fast_exp2(fmaf(x[j], c, -mc));
         }
         if (!seeded) {
-            seed = warp_kth_key<16>(mx == -INFINITY ? 0ull : topk_key(mx, uint32_t(tmx)));
+            int tmx = -1;  // the lane maximum's token (lowest id among equal values)
+#pragma unroll
+            for (int j = kRowVals - 1; j >= 0; --j)
+                if (x[j] == mx) tmx = tk[j];
+            const uint64_t srt = warp_sort_desc(mx == -INFINITY ? 0ull : topk_key(mx, uint32_t(tmx)));
+            if (lane < 16) s_lists[0][warp][lane] = srt;
+            __syncthreads();
+            const int cur = tree_merge16(s_lists, kRowWarps);
+            seed = s_lists[cur][0][15];
             seeded = true;
+            __syncthreads();  // s_lists is reused by the final merge
         }
-        const uint64_t bound = seed > top.thr ? seed : top.thr;
+        const uint64_t shared_bound = *reinterpret_cast<volatile unsigned long long *>(&s_bound);
+        uint64_t bound = seed > top.thr ? seed : top.thr;
+        bound = shared_bound > bound ? shared_bound : bound;
         const float bval = bound == 0 ? -INFINITY : topk_key_value(bound);
+        if (!__any_sync(0xffffffffu, mx >= bval && mx != -INFINITY)) return;
 #pragma unroll
         for (int j = 0; j < kRowVals; ++j) {
             const bool cand = x[j] >= bval && x[j] != -INFINITY;
@@ -153,10 +162,13 @@ __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
                 top.insert(key >= bound ? key : 0ull);
             }
         }
+        if (lane == 0 && top.thr > bound) atomicMax(&s_bound, static_cast<unsigned long long>(top.thr));
     };
 
     constexpr int kBatch = kRowThreads * kRowVals;
     const int nb = (hi - lo + kBatch - 1) / kBatch;  // same for every thread of the CTA
+    if (tid == 0) s_bound = 0;
+    __syncthreads();
     if (vec) {
         const float4 *row4 = reinterpret_cast<const float4 *>(row);
         float4 nxt[kRowVals / 4];

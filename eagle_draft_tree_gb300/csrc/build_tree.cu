@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     __shared__ int s_slot[16];
     __shared__ int s_hist[256];
     __shared__ uint64_t s_prefix;
-    __shared__ int s_remaining;
+    __shared__ uint64_t s_gather[32];
+    __shared__ int s_remaining, s_bcount;
     __shared__ int s_wsum[kMaxPool / 32];
 
     const int b = blockIdx.x;
@@ -323,8 +324,16 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     for (int f = 1; f <= D - 1; ++f) {
         for (int e = lb + tid; e < lb + cnt; e += kSelThreads) {
             const uint64_t v = s_key[e];
-            int rank = 0;
-            for (int o = lb; o < lb + cnt; ++o) rank += s_key[o] > v;
+            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent chains of shared loads
+            int o = lb;
+            for (; o + 4 <= lb + cnt; o += 4) {
+                r0 += s_key[o] > v;
+                r1 += s_key[o + 1] > v;
+                r2 += s_key[o + 2] > v;
+                r3 += s_key[o + 3] > v;
+            }
+            for (; o < lb + cnt; ++o) r0 += s_key[o] > v;
+            const int rank = (r0 + r1) + (r2 + r3);
             if (rank < k) {
                 s_slot[rank] = e;
                 s_row[e] = 1 + (f - 1) * k + rank;
@@ -351,10 +360,16 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         np += nf * k;
     }
 
-    // rerank: radix-select the m-th largest composite key (keys are unique)
+    // rerank: the m-th largest composite key (keys are unique).  Radix passes over 8-bit digits
+    // from the top: a histogram of the digit among the keys sharing the prefix found so far (equal
+    // digits of a warp counted once per warp, via __match_any_sync: most keys share their top
+    // bits, and per-key atomics on one bucket serialise); the bucket holding the m-th largest
+    // extends the prefix.  Once that bucket holds at most 32 keys, one warp gathers them, sorts
+    // them and reads the answer off.
     if (tid == 0) {
         s_prefix = 0;
         s_remaining = m;
+        s_bcount = 0x7fffffff;
     }
     __syncthreads();
     uint64_t hmask = 0;
@@ -362,9 +377,13 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         s_hist[tid] = 0;  // kSelThreads == 256 buckets
         __syncthreads();
         const uint64_t prefix = s_prefix;
-        for (int e = tid; e < np; e += kSelThreads) {
-            const uint64_t key = s_key[e];
-            if ((key & hmask) == prefix) atomicAdd(&s_hist[(key >> shift) & 255], 1);
+        for (int e0 = 0; e0 < np; e0 += kSelThreads) {  // whole warps take part in the match
+            const int e = e0 + tid;
+            const uint64_t key = e < np ? s_key[e] : 0ull;
+            const bool in = e < np && (key & hmask) == prefix;
+            const unsigned dig = in ? unsigned((key >> shift) & 255) : 256u + unsigned(lane);
+            const unsigned grp = __match_any_sync(0xffffffffu, dig);
+            if (in && lane == __ffs(grp) - 1) atomicAdd(&s_hist[dig], __popc(grp));
         }
         __syncthreads();
         if (warp == 0) {
@@ -388,6 +407,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
                     if (acc + h >= need) {
                         s_prefix = prefix | (uint64_t(bucket) << shift);
                         s_remaining = need - acc;
+                        s_bcount = h;
                         break;
                     }
                     acc += h;
@@ -396,7 +416,30 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         }
         hmask |= uint64_t(255) << shift;
         __syncthreads();
+        if (s_bcount <= 32) break;  // CTA-uniform
     }
+    if (warp == 0) {
+        // the <= 32 keys of the chosen bucket, in creation order, then sorted descending
+        const uint64_t prefix = s_prefix;
+        uint64_t mine = 0;
+        int filled = 0;
+        for (int e0 = 0; e0 < np; e0 += 32) {
+            const int e = e0 + lane;
+            const bool in = e < np && (s_key[e] & hmask) == prefix;
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            const int pos = filled + __popc(bal & ((1u << lane) - 1u));
+            const uint64_t key = in ? s_key[e] : 0ull;
+            // lane `pos` receives it: gather through shared memory
+            if (in && pos < 32) s_gather[pos] = key;
+            filled += __popc(bal);
+        }
+        __syncwarp();
+        mine = lane < min(filled, 32) ? s_gather[lane] : 0ull;
+        const uint64_t srt = warp_sort_desc(mine);
+        const uint64_t kth = __shfl_sync(0xffffffffu, srt, s_remaining - 1);
+        if (lane == 0) s_prefix = kth;
+    }
+    __syncthreads();
     const uint64_t thr = s_prefix;  // the m-th largest key itself
 
     // flatten: flat index = 1 + number of kept entries created earlier (ballots over creation order)

@@ -5,26 +5,26 @@
 // "(EAGLE 2) EAGLE-2 ..." section "Tree Attention Mask".
 //
 // One CTA = one (layer, sequence, KV head) unit and up to two 128-row M-tiles of its query block
-// (row r = node * G + head-in-group).  The context streams through in 64-key tiles; the n <= 64
+// (row r = node * G + head-in-group).  The context streams through in 128-key tiles; the n <= 64
 // tree keys form one last tile whose visibility is the node's ancestor bit mask.
 //
 //   warp 0     TMA producer: Q once (two 64-column halves per M-tile), then K and V tiles (one
-//              4-D box per tile: 64 keys x both 64-dim halves, 128B-swizzled) through two rings:
-//              K tiles are released right after QK^T has read them (4 stages), V tiles after PV
-//              (6 stages), issued in a fixed order K(j), V(j), each as soon as its stage is free.
-//   warps 1-2  MMA issuers, warp 1 + t for M-tile t (each whole warp follows a fixed schedule with
-//              blocking waits; one elected lane issues): S_t = Q_t K^T into TMEM as soon as the
-//              softmax has read the previous S_t, and O_t += P_t V with P_t read from TMEM (A
-//              operand in tensor memory).  S_t is
-//              single-buffered and P_t double-buffered, so the QK^T of tile j + 1 runs while the
-//              softmax of tile j is still computing, and the PVs trail off the critical path.
-//   warps 4-11 two softmax warpgroups, one per M-tile, one thread per query row: tcgen05.ld of
-//              the S row (then S_t is handed back), mask, scale, base-2 online softmax with lazy
-//              rescaling (O in TMEM is rescaled only when the running max grows by more than 8,
-//              i.e. P <= 2^8), P packed to bf16 pairs into its TMEM buffer, and the final O / l
-//              epilogue.  M-tile 0's warpgroup also zeroes the V rows past the last visible key of
-//              the ragged context tile and of the tree tile before their PV (P is 0 there, but
-//              0 x NaN would not be).
+//              4-D box per tile: 128 keys x both 64-dim halves, 128B-swizzled) through a 2-stage K
+//              ring and a 3-stage V ring, in the order K(j), V(j), each as soon as its stage is free.
+//   warp 1     the MMA issuer for both M-tiles (a whole converged warp, one elected lane issues),
+//              in a fixed order: S_0(0), S_1(0), then per tile j: O_0 += P_0(j) V(j), S_0(j + 1),
+//              O_1 += P_1(j) V(j), S_1(j + 1).  P_t (bf16 pairs, written by the softmax over the
+//              first 64 columns of S_t) is the A operand, read from tensor memory; S_t(j + 1) is
+//              issued right behind the PV that reads P_t(j) (the MMAs of one thread execute in
+//              order), so a softmax warpgroup restarts as soon as its own PV and next QK^T are
+//              through, and the two warpgroups settle half a period apart.
+//   warps 4-11 two softmax warpgroups, one per M-tile, one thread per query row, each tile in two
+//              64-key chunks: tcgen05.ld, mask, base-2 online softmax with lazy rescaling (O in
+//              TMEM is rescaled only when the running max grows by more than 8, i.e. P <= 2^8; the
+//              commit of S_t(j) covers PV_t(j - 1), so O_t is at rest then), P to TMEM, and the
+//              final O / l epilogue.  M-tile 0's warpgroup also zeroes the V rows past the last
+//              visible key of the ragged context tile and of the tree tile before their PV (P is 0
+//              there, but 0 x NaN would not be).
 //
 // Every mbarrier wait is bounded; a wait that runs out records EAGLE_ERR_TIMEOUT in the status
 // word, raises a CTA-wide abort flag that ends every role's loop, and the CTA still drains its
@@ -52,19 +52,19 @@ struct AttnTcParams {  // same layout as the declaration in tree_attention.cu
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kNkv = 64;                    // keys per tile
-constexpr int kKStages = 4;                 // K tiles are released as soon as QK^T has read them
-constexpr int kVStages = 6;                 // V tiles are held until PV, later in the tile's life
-constexpr uint32_t kHalf = kNkv * 128;      // one 64-dim half of a K or V tile: 64 rows x 128 B
+constexpr int kNkv = 128;                   // keys per tile
+constexpr int kKStages = 2;                 // K tiles are released as soon as both QK^T have read them
+constexpr int kVStages = 3;                 // V tiles are held until both PV, later in the tile's life
+constexpr uint32_t kHalf = kNkv * 128;      // one 64-dim half of a K or V tile: 128 rows x 128 B
 constexpr uint32_t kTileBytes = 2 * kHalf;  // a K (or V) tile: both halves
 constexpr uint32_t kQHalf = 128 * 128;      // 128 rows x 128 B
 constexpr uint32_t kQTile = 2 * kQHalf;
 constexpr uint32_t kOffK = 2 * kQTile;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
 constexpr uint32_t kSmemBytes = kOffV + kVStages * kTileBytes;  // 224 KB
-// TMEM columns: O_0, O_1 (128 each) | S_0, S_1 (64 each) | P_0[2], P_1[2] (32 each, bf16 pairs)
+// TMEM columns: O_0, O_1 (128 each) | S_0, S_1 (128 fp32 each; P_t over the first 64 of S_t)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 256, kColP = 384;
+constexpr uint32_t kColS = 256;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait counts as stuck
 
 __device__ __forceinline__ uint32_t sa(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
@@ -79,7 +79,7 @@ constexpr uint32_t idesc(int M, int N, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn) << 16) | (uint32_t(N >> 3) << 17) |
            (uint32_t(M >> 4) << 24);
 }
-constexpr uint32_t kIdescQK = idesc(128, kNkv, 0);
+constexpr uint32_t kIdescQK = idesc(128, kNkv, 0);  // N = 128 keys
 constexpr uint32_t kIdescPV = idesc(128, 128, 1);  // A = P from TMEM, B = V MN-major
 
 // The MMA issuer is a whole converged warp; one lane, picked by elect.sync, issues each operation
@@ -172,13 +172,11 @@ struct Bars {
     uint64_t q_full;
     uint64_t k_full[kKStages], k_empty[kKStages];
     uint64_t v_full[kVStages], v_empty[kVStages];
-    uint64_t v_clean[2];   // V rows past the last visible key zeroed: [0] ragged context tile, [1] tree tile
-    uint64_t s_full[2];    // [M-tile]: QK^T of the current tile landed (and every MMA issued before it)
-    uint64_t s_free[2];    // [M-tile]: the softmax has read S_t; the next QK^T may overwrite it
-    uint64_t p_full[2][2];  // [M-tile][P buffer]: P of a tile written
-    uint64_t o_ready[2];   // [M-tile]: a PV of this M-tile completed (once per tile)
-    uint64_t o_done[2];    // [M-tile]: the last PV completed
-    uint64_t drain[2];     // [M-tile]: every MMA of that M-tile's issuing warp completed
+    uint64_t v_clean[2];  // V rows past the last visible key zeroed: [0] ragged context tile, [1] tree tile
+    uint64_t s_full[2];   // [M-tile]: QK^T of the current tile landed (and every MMA issued before it)
+    uint64_t p_full[2];   // [M-tile]: P of the current tile written over S_t
+    uint64_t o_done[2];   // [M-tile]: the last PV completed
+    uint64_t drain;       // every MMA of the issuing warp completed
 };
 
 // Bounded wait; gives up (and raises the abort flag) when the CTA aborted or the limit ran out.
@@ -254,23 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars.q_full, 1);
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
-            mbar_init(&bars.k_empty[s], tm);  // one release per M-tile's MMA warp
+            mbar_init(&bars.k_empty[s], 1);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars.v_full[s], 1);
-            mbar_init(&bars.v_empty[s], tm);
+            mbar_init(&bars.v_empty[s], 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars.v_clean[t], 4);
             mbar_init(&bars.s_full[t], 1);
-            mbar_init(&bars.s_free[t], 4);
-            mbar_init(&bars.p_full[t][0], 4);
-            mbar_init(&bars.p_full[t][1], 4);
-            mbar_init(&bars.o_ready[t], 1);
+            mbar_init(&bars.p_full[t], 4);
             mbar_init(&bars.o_done[t], 1);
         }
-        mbar_init(&bars.drain[0], 1);
-        mbar_init(&bars.drain[1], 1);
+        mbar_init(&bars.drain, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -312,59 +306,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++v_issued;
             }
         }
-    } else if (warp == 1 || (warp == 2 && tm > 1)) {
-        // ---------------- MMA issuer of M-tile t = warp - 1: a fixed schedule, blocking waits -----
-        // Step j issues S_t(j) = Q_t K(j)^T (once the softmax has read S_t(j - 1)), then O_t +=
-        // P_t(j - 1) V(j - 1) (once P_t(j - 1) is written).  S_t is single-buffered and P_t
-        // double-buffered, so S_t(j) overlaps the softmax of tile j - 1; PV_t(j - 2), the last
-        // reader of the P buffer tile j fills, was issued in step j - 1, before S_t(j), whose commit
-        // therefore also covers it.  Each M-tile has its own issuing warp, so neither waits on the
-        // other's softmax; a K or V stage is released once both have read it.
-        const int t = warp - 1;
+    } else if (warp == 1) {
+        // ---------------- MMA issuer for both M-tiles, in a fixed order ----------------------------
         bool ok = warp_wait(&bars.q_full, 0, abort_flag, p.status);
         tc_fence_after();
-        const uint32_t qbase = sa(sm + t * kQTile);
-        const uint32_t dS = tmem + kColS + t * 64;
-        const uint32_t dO = tmem + t * 128;
-        for (int j = 0; ok && j <= ntiles; ++j) {
-            if (j < ntiles) {
-                const int sk = j % kKStages;
-                ok = warp_wait(&bars.k_full[sk], (j / kKStages) & 1, abort_flag, p.status) &&
-                     (j == 0 || warp_wait(&bars.s_free[t], (j - 1) & 1, abort_flag, p.status));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t kbase = sa(sm + kOffK + sk * kTileBytes);
+        // S_t(j) = Q_t K(j)^T into S_t (N = 128 keys)
+        auto issue_s = [&](int t, int j) {
+            const uint32_t qbase = sa(sm + t * kQTile);
+            const uint32_t kbase = sa(sm + kOffK + (j % kKStages) * kTileBytes);
+            const uint32_t dS = tmem + kColS + t * 128;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
-                    const uint32_t offk = (kk >> 2) * kHalf + (kk & 3) * 32;
-                    umma(dS, sdesc(qbase + off, 16, 1024), sdesc(kbase + offk, 16, 1024), kIdescQK, kk > 0);
-                }
-                umma_commit(&bars.s_full[t]);
-                umma_commit(&bars.k_empty[sk]);  // this M-tile has read K(j)
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
+                const uint32_t offk = (kk >> 2) * kHalf + (kk & 3) * 32;
+                umma(dS, sdesc(qbase + off, 16, 1024), sdesc(kbase + offk, 16, 1024), kIdescQK, kk > 0);
             }
-            if (j > 0) {
-                const int jv = j - 1, sv = jv % kVStages, pb = jv & 1;
-                ok = warp_wait(&bars.v_full[sv], (jv / kVStages) & 1, abort_flag, p.status) &&
-                     (jv != jtail || warp_wait(&bars.v_clean[0], 0, abort_flag, p.status)) &&
-                     (jv != nctx || warp_wait(&bars.v_clean[1], 0, abort_flag, p.status)) &&
-                     warp_wait(&bars.p_full[t][pb], (jv >> 1) & 1, abort_flag, p.status);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t vbase = sa(sm + kOffV + sv * kTileBytes);
-                const uint32_t aP = tmem + kColP + t * 64 + pb * 32;
+            umma_commit(&bars.s_full[t]);
+        };
+        // O_t += P_t(j) V(j), P_t read from the first 64 columns of S_t
+        auto issue_pv = [&](int t, int j) {
+            const uint32_t vbase = sa(sm + kOffV + (j % kVStages) * kTileBytes);
+            const uint32_t aP = tmem + kColS + t * 128, dO = tmem + t * 128;
 #pragma unroll
-                for (int kk = 0; kk < kNkv / 16; ++kk)
-                    umma_ts(dO, aP + kk * 8, sdesc(vbase + kk * 2048, kHalf, 1024), kIdescPV,
-                            (jv > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars.o_ready[t]);
-                if (jv == ntiles - 1) umma_commit(&bars.o_done[t]);
-                umma_commit(&bars.v_empty[sv]);  // this M-tile has read V(j - 1)
+            for (int kk = 0; kk < kNkv / 16; ++kk)
+                umma_ts(dO, aP + kk * 8, sdesc(vbase + kk * 2048, kHalf, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        };
+        if (ok && (ok = warp_wait(&bars.k_full[0], 0, abort_flag, p.status))) {
+            tc_fence_after();
+            issue_s(0, 0);
+            if (tm > 1) issue_s(1, 0);
+            umma_commit(&bars.k_empty[0]);
+        }
+        for (int j = 0; ok && j < ntiles; ++j) {
+            const int sv = j % kVStages, jn = j + 1;
+            // V(j) landed (and cleaned, for the ragged and the tree tile), P_0(j) written
+            ok = warp_wait(&bars.v_full[sv], (j / kVStages) & 1, abort_flag, p.status) &&
+                 (j != jtail || warp_wait(&bars.v_clean[0], 0, abort_flag, p.status)) &&
+                 (j != nctx || warp_wait(&bars.v_clean[1], 0, abort_flag, p.status)) &&
+                 warp_wait(&bars.p_full[0], j & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(0, j);
+            if (jn < ntiles) {
+                if (!(ok = warp_wait(&bars.k_full[jn % kKStages], (jn / kKStages) & 1, abort_flag, p.status))) break;
+                tc_fence_after();
+                issue_s(0, jn);  // overwrites P_0(j) after the PV just issued has read it
+            }
+            if (tm > 1) {
+                if (!(ok = warp_wait(&bars.p_full[1], j & 1, abort_flag, p.status))) break;
+                tc_fence_after();
+                issue_pv(1, j);
+            }
+            umma_commit(&bars.v_empty[sv]);  // both PVs of tile j have read V(j)
+            if (jn < ntiles) {
+                if (tm > 1) issue_s(1, jn);
+                umma_commit(&bars.k_empty[jn % kKStages]);  // both QK^T of tile j + 1 have read K(j + 1)
+            } else {
+                umma_commit(&bars.o_done[0]);
+                umma_commit(&bars.o_done[1]);
             }
         }
-        // drain: every MMA issued by this warp has completed once its `drain` barrier completes
-        umma_commit(&bars.drain[t]);
-        for (uint32_t it = 0; it < kWaitLimit && !__all_sync(0xffffffffu, mbar_try_wait(&bars.drain[t], 0)); ++it) {
+        // drain: every MMA issued by this warp has completed once `drain` completes
+        umma_commit(&bars.drain);
+        for (uint32_t it = 0; it < kWaitLimit && !__all_sync(0xffffffffu, mbar_try_wait(&bars.drain, 0)); ++it) {
         }
     } else if (warp >= 4 && warp - 4 < 4 * tm) {
         // ---------------- softmax warpgroup t ----------------
@@ -377,110 +381,125 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gh = valid ? r % p.G : 0;
         const uint64_t tmask = valid ? p.mask[size_t(b) * p.n + node] : 0ull;
         const uint32_t lane_off = uint32_t(wq * 32) << 16;
-        const uint32_t tS = tmem + lane_off + kColS + t * 64;  // this row's S columns
-        const uint32_t tP = tmem + lane_off + kColP + t * 64;  // this row's two P buffers
-        const uint32_t tO = tmem + lane_off + t * 128;         // this row's O columns
+        const uint32_t tS = tmem + lane_off + kColS + t * 128;  // this row's S (P over its first 64 columns)
+        const uint32_t tO = tmem + lane_off + t * 128;          // this row's O columns
         const float c = p.scale_log2;
         float m_raw = -INFINITY;  // reference max in raw score units (P = 2^((s - m_raw) c))
         float l_sum = 0.f;
         bool ok = true;
+        float sv[64];
+        uint32_t pk[32];
         for (int j = 0; j < ntiles; ++j) {
-            // S_t(j) landed; its commit also covers PV_t(j - 2), the last reader of P buffer j & 1
+            // S_t(j) landed; its commit also covers PV_t(j - 1), so O_t is at rest
             if (!warp_wait(&bars.s_full[t], j & 1, abort_flag, p.status)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float sv[kNkv];
-            {
-                uint32_t raw[kNkv];
-                uint32_t (&r0)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw);
-                uint32_t (&r1)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 16);
-                uint32_t (&r2)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 32);
-                uint32_t (&r3)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 48);
-                tld16(tS, r0);
-                tld16(tS + 16, r1);
-                tld16(tS + 32, r2);
-                tld16(tS + 48, r3);
-                tld_wait();
-#pragma unroll
-                for (int cc = 0; cc < kNkv; ++cc) sv[cc] = __uint_as_float(raw[cc]);
-            }
-            // S_t is in registers: hand it back so QK^T of the next tile overlaps this softmax
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.s_free[t]);
             const bool tree = j == nctx;
             const int kvalid = tree ? p.n : min(kNkv, ctx - j * kNkv);
-            // masking: only the ragged context tile and the tree tile have invisible keys (a masked
-            // score is replaced, so whatever the fetched K row held is irrelevant)
-            if (tree || kvalid < kNkv) {
+            float tile_sum = 0.f;
+#pragma unroll 1
+            for (int q = 0; q < 2; ++q) {  // 64-key chunks
+                {
+                    uint32_t raw[64];
+                    uint32_t (&r0)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw);
+                    uint32_t (&r1)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 16);
+                    uint32_t (&r2)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 32);
+                    uint32_t (&r3)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw + 48);
+                    tld16(tS + q * 64, r0);
+                    tld16(tS + q * 64 + 16, r1);
+                    tld16(tS + q * 64 + 32, r2);
+                    tld16(tS + q * 64 + 48, r3);
+                    tld_wait();
 #pragma unroll
-                for (int cc = 0; cc < kNkv; ++cc) {
-                    bool vis = cc < kvalid;
-                    if (tree) vis = vis && ((tmask >> cc) & 1ull);
-                    if (!vis) sv[cc] = -INFINITY;
+                    for (int cc = 0; cc < 64; ++cc) sv[cc] = __uint_as_float(raw[cc]);
                 }
-            }
-            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-            for (int cc = 0; cc < kNkv; cc += 4) {
-                mx0 = fmaxf(mx0, sv[cc]);
-                mx1 = fmaxf(mx1, sv[cc + 1]);
-                mx2 = fmaxf(mx2, sv[cc + 2]);
-                mx3 = fmaxf(mx3, sv[cc + 3]);
-            }
-            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-            // lazy rescale: the reference moves only when the max exceeds it by more than 8 in
-            // base-2 units, so every P stays below 2^8
-            if ((mx - m_raw) * c > 8.f) {
-                const float alpha = m_raw == -INFINITY ? 0.f : fast_exp2((m_raw - mx) * c);
-                m_raw = mx;
-                if (j > 0) {
-                    // O_t must hold tiles < j: wait for PV_t(j - 1).  o_ready completes once per PV
-                    // of this M-tile and PV_t(j) needs this tile's P, so the phase cannot alias.
-                    if (!warp_wait(&bars.o_ready[t], (j - 1) & 1, abort_flag, p.status)) {
-                        ok = false;
-                        break;
+                // masking: only the ragged context tile and the tree tile have invisible keys (a
+                // masked score is replaced, so whatever the fetched K row held is irrelevant)
+                const int hv = kvalid - q * 64;
+                if (tree || hv < 64) {
+                    const int hc = min(max(hv, 0), 64);
+                    uint32_t vlo = hc >= 32 ? ~0u : ((1u << hc) - 1u);
+                    uint32_t vhi = hc >= 64 ? ~0u : (hc <= 32 ? 0u : ((1u << (hc - 32)) - 1u));
+                    if (tree && q == 0) {  // tree keys are keys 0 .. n - 1 <= 63
+                        vlo &= uint32_t(tmask);
+                        vhi &= uint32_t(tmask >> 32);
                     }
-                    tc_fence_after();
-                    tmem_scale128(tO, alpha);
-                }
-                l_sum *= alpha;
-            }
-            const float mc = m_raw == -INFINITY ? 0.f : m_raw * c;
-            // scale and row sums on the paired f32x2 pipe (two lanes of work per instruction)
-            const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-mc, -mc);
-            uint64_t s01 = f2_pack(0.f, 0.f), s23 = s01;
-            uint32_t pk[kNkv / 2];
 #pragma unroll
-            for (int cc = 0; cc < kNkv; cc += 4) {
-                const uint64_t a01 = f2_fma(f2_pack(sv[cc], sv[cc + 1]), c2, nm2);
-                const uint64_t a23 = f2_fma(f2_pack(sv[cc + 2], sv[cc + 3]), c2, nm2);
-                const float p0 = fast_exp2(f2_lo(a01)), p1 = fast_exp2(f2_hi(a01));
-                const float p2 = fast_exp2(f2_lo(a23)), p3 = fast_exp2(f2_hi(a23));
-                s01 = f2_add(s01, f2_pack(p0, p1));
-                s23 = f2_add(s23, f2_pack(p2, p3));
-                __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
-                __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
-                pk[cc / 2] = *reinterpret_cast<uint32_t *>(&h0);
-                pk[cc / 2 + 1] = *reinterpret_cast<uint32_t *>(&h1);
-            }
-            const uint64_t s4 = f2_add(s01, s23);
-            l_sum += f2_lo(s4) + f2_hi(s4);
-            // P (bf16 pairs) into P buffer j & 1; PV_t(j - 2), its previous reader, has completed
-            {
+                    for (int cc = 0; cc < 32; ++cc) {
+                        if (!((vlo >> cc) & 1u)) sv[cc] = -INFINITY;
+                        if (!((vhi >> cc) & 1u)) sv[cc + 32] = -INFINITY;
+                    }
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 4) {
+                    mx0 = fmaxf(mx0, sv[cc]);
+                    mx1 = fmaxf(mx1, sv[cc + 1]);
+                    mx2 = fmaxf(mx2, sv[cc + 2]);
+                    mx3 = fmaxf(mx3, sv[cc + 3]);
+                }
+                const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                // lazy rescale: the reference moves only when the max exceeds it by more than 8 in
+                // base-2 units, so every P stays below 2^8
+                if (m_raw == -INFINITY ? mx != -INFINITY : (mx - m_raw) * c > 8.f) {
+                    const float alpha = m_raw == -INFINITY ? 0.f : fast_exp2((m_raw - mx) * c);
+                    m_raw = mx;
+                    if (j > 0) tmem_scale128(tO, alpha);  // O_t: tiles < j
+                    if (q == 1) {  // P of chunk 0 was computed against the old reference
+                        uint32_t q0[16], q1[16];
+                        tst_wait();
+                        tld16(tS, q0);
+                        tld16(tS + 16, q1);
+                        tld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&q0[e]));
+                            float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&q1[e]));
+                            __nv_bfloat162 g0 = __floats2bfloat162_rn(f0.x * alpha, f0.y * alpha);
+                            __nv_bfloat162 g1 = __floats2bfloat162_rn(f1.x * alpha, f1.y * alpha);
+                            q0[e] = *reinterpret_cast<uint32_t *>(&g0);
+                            q1[e] = *reinterpret_cast<uint32_t *>(&g1);
+                        }
+                        tst16(tS, q0);
+                        tst16(tS + 16, q1);
+                    }
+                    l_sum *= alpha;
+                    tile_sum *= alpha;
+                }
+                const float mc = m_raw == -INFINITY ? 0.f : m_raw * c;
+                // scale and row sums on the paired f32x2 pipe (two lanes of work per instruction)
+                const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(-mc, -mc);
+                uint64_t s01 = f2_pack(0.f, 0.f), s23 = s01;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 4) {
+                    const uint64_t a01 = f2_fma(f2_pack(sv[cc], sv[cc + 1]), c2, nm2);
+                    const uint64_t a23 = f2_fma(f2_pack(sv[cc + 2], sv[cc + 3]), c2, nm2);
+                    const float p0 = fast_exp2(f2_lo(a01)), p1 = fast_exp2(f2_hi(a01));
+                    const float p2 = fast_exp2(f2_lo(a23)), p3 = fast_exp2(f2_hi(a23));
+                    s01 = f2_add(s01, f2_pack(p0, p1));
+                    s23 = f2_add(s23, f2_pack(p2, p3));
+                    __nv_bfloat162 h0 = __floats2bfloat162_rn(p0, p1);
+                    __nv_bfloat162 h1 = __floats2bfloat162_rn(p2, p3);
+                    pk[cc / 2] = *reinterpret_cast<uint32_t *>(&h0);
+                    pk[cc / 2 + 1] = *reinterpret_cast<uint32_t *>(&h1);
+                }
+                const uint64_t s4 = f2_add(s01, s23);
+                tile_sum += f2_lo(s4) + f2_hi(s4);
+                // P of this chunk (keys 64q .. 64q + 63) over S columns already read: 32q .. 32q + 31
                 uint32_t (&p0)[16] = *reinterpret_cast<uint32_t(*)[16]>(pk);
                 uint32_t (&p1)[16] = *reinterpret_cast<uint32_t(*)[16]>(pk + 16);
-                tst16(tP + (j & 1) * 32, p0);
-                tst16(tP + (j & 1) * 32 + 16, p1);
-                tst_wait();
+                tst16(tS + q * 32, p0);
+                tst16(tS + q * 32 + 16, p1);
             }
+            l_sum += tile_sum;
+            tst_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.p_full[t][j & 1]);
+            if (lane == 0) mbar_arrive(&bars.p_full[t]);
             // M-tile 0's warpgroup zeroes the V rows past the last visible key of the ragged context
-            // tile and of the tree tile before their PV (P is 0 there, but 0 x NaN would not be).
+            // tile and of the tree tile before their PVs (P is 0 there, but 0 x NaN would not be).
             // Waiting on V(j)'s phase is safe here: that stage cannot move past tile j before the
             // PV that this warpgroup's P(j) gates.
             if (t == 0 && (j == jtail || j == nctx)) {

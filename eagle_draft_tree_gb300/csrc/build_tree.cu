@@ -94,6 +94,8 @@ __device__ __forceinline__ int tree_merge16(uint64_t (*buf)[kRowWarps][16], int 
 }
 
 __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
+    pdl_wait();
+    pdl_launch_next();
     __shared__ uint64_t s_lists[2][kRowWarps][16];
     __shared__ unsigned long long s_bound;  // CTA-wide lower bound of the slice's 16th key
     __shared__ float2 s_ms[kRowWarps];
@@ -282,6 +284,8 @@ struct SelectArgs {
 };
 
 __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) {
+    pdl_wait();
+    pdl_launch_next();
     __shared__ double s_lc[kMaxPool];     // [R*k] child log-confidences (R*k = P <= 1024)
     __shared__ int s_ctok[kMaxPool];      // [R*k] child tokens
     __shared__ double s_logv[kMaxPool];   // pool: log V
@@ -547,19 +551,9 @@ eagle_status launch_build(const eagle_tree_cfg &c, const float *draft, const int
     ra.c = kLog2e / c.tree_temp;
     ra.inv_t = 1.0 / double(c.tree_temp);
 
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(splits, R, c.batch);
-    cfg.blockDim = dim3(kRowThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = splits;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, row_topk_kernel, ra) != cudaSuccess) return EAGLE_ERR_CUDA;
+    if (launch_pdl(row_topk_kernel, dim3(splits, R, c.batch), dim3(kRowThreads), 0, stream, unsigned(splits), ra) !=
+        cudaSuccess)
+        return EAGLE_ERR_CUDA;
     note_launch();
 
     SelectArgs sa;
@@ -578,7 +572,8 @@ eagle_status launch_build(const eagle_tree_cfg &c, const float *draft, const int
     sa.k = c.topk;
     sa.m = c.keep;
     sa.R = R;
-    tree_select_kernel<<<c.batch, kSelThreads, 0, stream>>>(sa);
+    if (launch_pdl(tree_select_kernel, dim3(c.batch), dim3(kSelThreads), 0, stream, 1u, sa) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
     note_launch();
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }

@@ -230,6 +230,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
 
+    pdl_wait();
+    pdl_launch_next();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int mg = blockIdx.x % p.mgroups;
     const int unit = blockIdx.x / p.mgroups;
@@ -633,7 +635,9 @@ eagle_status tree_attention_tc_launch(const AttnTcParams &p, const void *q, cons
         attr = true;
     }
     const long grid = long(p.L) * p.B * p.Hkv * p.mgroups;
-    tree_attn_tc_kernel<<<unsigned(grid), kThreads, smem, stream>>>(qm, km, vm, ktm, vtm, p);
+    if (launch_pdl(tree_attn_tc_kernel, dim3(unsigned(grid)), dim3(kThreads), smem, stream, 1u, qm, km, vm, ktm, vtm, p) !=
+        cudaSuccess)
+        return EAGLE_ERR_CUDA;
     note_launch();
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }

@@ -359,6 +359,8 @@ __device__ __forceinline__ int draw_in_slice(const float (&w)[kE], uint64_t loca
 
 template <int CL>
 __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs a) {
+    pdl_wait();
+    pdl_launch_next();
     extern __shared__ __align__(16) float s_rows[];  // [2][kSliceMax]: the two held rows' slices
     __shared__ float4 s_wp[kWarpsPrep];              // per-warp partials of the current pass
     __shared__ float4 s_recv[2][CL];                 // the cluster's records of an exchange, by parity
@@ -761,6 +763,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
 }
 
 __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
+    pdl_wait();
+    pdl_launch_next();
     __shared__ int s_tok[64], s_par[64], s_row[64], s_fin[64], s_next[64];
     __shared__ int s_bad;
     const int b = blockIdx.x, tid = threadIdx.x;
@@ -872,19 +876,8 @@ cudaError_t launch_prep(const VerifyArgs &a, int clusters, int batch, cudaStream
         if (e != cudaSuccess) return e;
         ready.fetch_or(bit);
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(CL, clusters, batch);
-    cfg.blockDim = dim3(kPrepThreads, 1, 1);
-    cfg.dynamicSmemBytes = kPrepSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = CL;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, verify_prep_kernel<CL>, a);
+    return launch_pdl(verify_prep_kernel<CL>, dim3(CL, clusters, batch), dim3(kPrepThreads), kPrepSmem, stream,
+                      unsigned(CL), a);
 }
 }  // namespace
 
@@ -927,7 +920,7 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
                                   : launch_prep<16>(a, clusters, c.batch, stream);
     if (e != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();
-    verify_walk_kernel<<<c.batch, 64, 0, stream>>>(a);
+    if (launch_pdl(verify_walk_kernel, dim3(c.batch), dim3(64), 0, stream, 1u, a) != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }

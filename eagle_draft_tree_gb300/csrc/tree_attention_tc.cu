@@ -444,10 +444,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
                 // lazy rescale: the reference moves only when the max exceeds it by more than 8 in
-                // base-2 units, so every P stays below 2^8
-                if (m_raw == -INFINITY ? mx != -INFINITY : (mx - m_raw) * c > 8.f) {
-                    const float alpha = m_raw == -INFINITY ? 0.f : fast_exp2((m_raw - mx) * c);
-                    m_raw = mx;
+                // base-2 units, so every P stays below 2^8.  The TMEM accesses below are warp-wide
+                // (.sync.aligned), so the warp enters together when any row needs it; the other
+                // rows keep their reference and scale by 1.
+                const bool moves = m_raw == -INFINITY ? mx != -INFINITY : (mx - m_raw) * c > 8.f;
+                if (__any_sync(0xffffffffu, moves)) {
+                    const float alpha = !moves ? 1.f : m_raw == -INFINITY ? 0.f : fast_exp2((m_raw - mx) * c);
+                    if (moves) m_raw = mx;
                     if (j > 0) tmem_scale128(tO, alpha);  // O_t: tiles < j
                     if (q == 1) {  // P of chunk 0 was computed against the old reference
                         uint32_t q0[16], q1[16];

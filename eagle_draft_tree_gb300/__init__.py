@@ -23,7 +23,7 @@ from . import build as _build
 
 __all__ = [
     "EagleError", "Workspace", "load", "library_path", "build_tree", "tree_attention", "tree_verify",
-    "device_status", "last_launch_count", "TreeCfg", "AttnCfg", "VerifyCfg",
+    "device_status", "last_launch_count", "selftest_wait_timeout", "TreeCfg", "AttnCfg", "VerifyCfg",
 ]
 
 EAGLE_OK, EAGLE_ERR_INVALID_ARG, EAGLE_ERR_UNSUPPORTED, EAGLE_ERR_CUDA, EAGLE_ERR_TIMEOUT, EAGLE_ERR_DEVICE_INPUT = range(6)
@@ -69,6 +69,7 @@ _SIGS = {
     "eagle_get_device_status": (ctypes.c_int32, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
     "eagle_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "eagle_last_launch_count": (ctypes.c_int32, []),
+    "eagle_selftest_wait_timeout": (ctypes.c_int32, [_P, _P, _P]),
 }
 
 
@@ -103,6 +104,17 @@ def _status_string(s: int) -> str:
 def last_launch_count() -> int:
     """Kernel launches issued by the most recent entry-point call on this thread."""
     return int(load().eagle_last_launch_count())
+
+
+def selftest_wait_timeout(ws: "Workspace", stream=None) -> tuple[int, list[int]]:
+    """eagle_selftest_wait_timeout: a warp and a thread each wait on a barrier nothing completes.
+    Returns (the device status read back, [ns the warp waited, ns the thread waited])."""
+    ws.reserve(256, stream)
+    elapsed = torch.zeros(2, dtype=torch.int64, device=ws.device)
+    _check(load().eagle_selftest_wait_timeout(ws.ptr, _ptr(elapsed), _stream(stream)),
+           "eagle_selftest_wait_timeout")
+    st = ws.status(stream)
+    return st, [int(x) for x in elapsed.cpu()]
 
 
 def _check(status: int, what: str) -> None:

@@ -77,6 +77,26 @@ int check_verify(const eagle_verify_cfg *c) {
 
 using namespace eagle;
 
+// The bounded waits put to the test: warp 0 polls as a warp, lane 0 of warp 1 polls alone, both
+// on an mbarrier that nothing ever completes.  Each gives up at the deadline, records
+// EAGLE_ERR_TIMEOUT and stores how long it waited.
+static __global__ void wait_selftest_kernel(int32_t *status, uint64_t *elapsed_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const uint64_t t0 = global_ns();
+    bool got = true;
+    if (threadIdx.x < 32)
+        got = mbar_warp_wait_bounded(&bar, 0);
+    else if (threadIdx.x == 32)
+        got = mbar_wait_bounded(&bar, 0);
+    if (!got) set_status(status, EAGLE_ERR_TIMEOUT);
+    if ((threadIdx.x & 31) == 0) elapsed_ns[threadIdx.x >> 5] = global_ns() - t0;
+}
+
 extern "C" {
 
 size_t eagle_build_tree_workspace_size(const eagle_tree_cfg *cfg) {
@@ -165,5 +185,14 @@ const char *eagle_status_string(eagle_status s) {
 }
 
 int32_t eagle_last_launch_count(void) { return t_launches; }
+
+eagle_status eagle_selftest_wait_timeout(void *ws, uint64_t *elapsed_ns, cudaStream_t stream) {
+    if (!aligned256(ws) || !elapsed_ns) return EAGLE_ERR_INVALID_ARG;
+    reset_launches();
+    wait_selftest_kernel<<<1, 64, 0, stream>>>(static_cast<int32_t *>(ws), elapsed_ns);
+    if (cudaPeekAtLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
+    note_launch();
+    return EAGLE_OK;
+}
 
 }  // extern "C"

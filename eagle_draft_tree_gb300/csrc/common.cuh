@@ -136,11 +136,51 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Wait for phase `parity` of `bar` at most `limit` polls; false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit = 1u << 24) {
-    for (uint32_t it = 0; it < limit; ++it)
+
+// ---- bounded waits ----
+// Every wait in the library gives up after kWaitNs of wall-clock time (%globaltimer).  A poll
+// count alone would not bound it: try_wait may suspend the thread for a hardware-defined time
+// on each poll.  The timer is read once every 256 polls, so a wait that completes early never
+// touches it.
+constexpr uint64_t kWaitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+struct Deadline {
+    uint64_t start = 0;
+    // true once kWaitNs have passed since the first check; `it` is the poll count
+    __device__ __forceinline__ bool passed(uint32_t it) {
+        if ((it & 255u) != 255u) return false;
+        if (it >= (1u << 31)) return true;  // backstop, should the timer not advance
+        const uint64_t t = global_ns();
+        if (start == 0) {
+            start = t;
+            return false;
+        }
+        return t - start > kWaitNs;
+    }
+    // the same, agreed by the whole warp (`it` must be warp-uniform)
+    __device__ __forceinline__ bool passed_warp(uint32_t it) {
+        return (it & 255u) == 255u && __any_sync(0xffffffffu, passed(it));
+    }
+};
+// Wait for phase `parity` of `bar`; false when the deadline passed first.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    Deadline d;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-    return false;
+        if (d.passed(it)) return false;
+    }
+}
+// The same for a whole converged warp: every lane polls and the warp agrees by vote.
+__device__ __forceinline__ bool mbar_warp_wait_bounded(uint64_t *bar, uint32_t parity) {
+    Deadline d;
+    for (uint32_t it = 0;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if (d.passed_warp(it)) return false;
+    }
 }
 
 // Programmatic dependent launch.  Every kernel of the library is launched with programmatic stream

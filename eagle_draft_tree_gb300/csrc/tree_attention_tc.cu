@@ -26,9 +26,9 @@
 //              visible key of the ragged context tile and of the tree tile before their PV (P is 0
 //              there, but 0 x NaN would not be).
 //
-// Every mbarrier wait is bounded; a wait that runs out records EAGLE_ERR_TIMEOUT in the status
-// word, raises a CTA-wide abort flag that ends every role's loop, and the CTA still drains its
-// issued copies and MMAs (bounded) before releasing TMEM.
+// Every mbarrier wait gives up after one second; a wait that runs out records EAGLE_ERR_TIMEOUT in
+// the status word, raises a CTA-wide abort flag that ends every role's loop, and the CTA still
+// drains its issued copies and MMAs (bounded) before releasing TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -65,7 +65,6 @@ constexpr uint32_t kSmemBytes = kOffV + kVStages * kTileBytes;  // 224 KB
 // TMEM columns: O_0, O_1 (128 each) | S_0, S_1 (128 fp32 each; P_t over the first 64 of S_t)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 256;
-constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait counts as stuck
 
 __device__ __forceinline__ uint32_t sa(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
@@ -179,12 +178,14 @@ struct Bars {
     uint64_t drain;       // every MMA of the issuing warp completed
 };
 
-// Bounded wait; gives up (and raises the abort flag) when the CTA aborted or the limit ran out.
+// Bounded wait; gives up (and raises the abort flag) when the CTA aborted or the deadline passed.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                               int32_t *status) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    Deadline d;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255) == 255 && *abort_flag) return false;
+        if (d.passed(it)) break;
     }
     *abort_flag = 1;
     set_status(status, EAGLE_ERR_TIMEOUT);
@@ -195,9 +196,11 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 // diverges (a lane-0-only polling loop costs several hundred cycles to reconverge even when the
 // phase has long completed; this form costs a few dozen).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *status) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    Deadline d;
+    for (uint32_t it = 0;; ++it) {
         if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
         if ((it & 255) == 255 && __any_sync(0xffffffffu, *abort_flag != 0)) return false;
+        if (d.passed_warp(it)) break;
     }
     if ((threadIdx.x & 31) == 0) {
         *abort_flag = 1;
@@ -370,8 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // drain: every MMA issued by this warp has completed once `drain` completes
         umma_commit(&bars.drain);
-        for (uint32_t it = 0; it < kWaitLimit && !__all_sync(0xffffffffu, mbar_try_wait(&bars.drain, 0)); ++it) {
-        }
+        mbar_warp_wait_bounded(&bars.drain, 0);
     } else if (warp >= 4 && warp - 4 < 4 * tm) {
         // ---------------- softmax warpgroup t ----------------
         const int t = (warp - 4) >> 2;
@@ -555,13 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         // the last copy issued into each stage has landed (already true unless the CTA aborted)
         for (int j = k_issued > kKStages ? k_issued - kKStages : 0; j < k_issued; ++j)
-            for (uint32_t it = 0; it < kWaitLimit && !mbar_try_wait(&bars.k_full[j % kKStages], (j / kKStages) & 1);
-                 ++it) {
-            }
+            mbar_wait_bounded(&bars.k_full[j % kKStages], (j / kKStages) & 1);
         for (int j = v_issued > kVStages ? v_issued - kVStages : 0; j < v_issued; ++j)
-            for (uint32_t it = 0; it < kWaitLimit && !mbar_try_wait(&bars.v_full[j % kVStages], (j / kVStages) & 1);
-                 ++it) {
-            }
+            mbar_wait_bounded(&bars.v_full[j % kVStages], (j / kVStages) & 1);
     }
     __syncthreads();
     if (warp == 1) {

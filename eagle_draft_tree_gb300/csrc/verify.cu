@@ -469,8 +469,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     // A slice copy that does not land marks the CTA failed; the CTA still waits (bounded) for it
     // before it can leave, as the copy writes into its shared memory.
     auto wait_slice = [&](int i) {
-        bool got = false;
-        for (uint32_t it = 0; it < (1u << 22) && !got; ++it) got = __all_sync(0xffffffffu, mbar_try_wait(&s_lbar[i], 0));
+        const bool got = mbar_warp_wait_bounded(&s_lbar[i], 0);
         if (!got && lane == 0) {
             s_fail = 1;
             set_status(a.status, EAGLE_ERR_TIMEOUT);
@@ -506,10 +505,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         }
     };
     auto wait_posts = [&]() -> bool {  // warp 0
-        bool got = false;
-        if (!failed())
-            for (uint32_t it = 0; it < (1u << 22) && !got; ++it)
-                got = __all_sync(0xffffffffu, mbar_try_wait(&s_pbar, nposts & 1));
+        const bool got = !failed() && mbar_warp_wait_bounded(&s_pbar, nposts & 1);
         ++nposts;
         if (!got) fail();
         return got;
@@ -524,10 +520,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     };
     auto wait_recv = [&]() -> bool {  // the CL records of the current exchange are in s_recv
         const int slot = xch & 1;
-        bool got = false;
-        if (!failed())
-            for (uint32_t it = 0; it < (1u << 22) && !got; ++it)
-                got = __all_sync(0xffffffffu, mbar_try_wait(&s_rbar[slot], (xch >> 1) & 1));
+        const bool got = !failed() && mbar_warp_wait_bounded(&s_rbar[slot], (xch >> 1) & 1);
         ++xch;
         if (!got) fail();
         return got;

@@ -226,6 +226,13 @@ const char *eagle_status_string(eagle_status status);
  * (for launch accounting in benchmarks). */
 int32_t eagle_last_launch_count(void);
 
+/* Self-test of the device-side wait bound: one launch in which a warp and a single thread each
+ * wait on a barrier that nothing completes.  Both give up after the library's wait limit (one
+ * second), set EAGLE_ERR_TIMEOUT in the status word of `ws` (256-byte aligned, read it with
+ * eagle_get_device_status) and store the nanoseconds they waited into elapsed_ns[0] (the warp)
+ * and elapsed_ns[1] (the thread), a DEVICE buffer of two uint64.  The context stays usable. */
+eagle_status eagle_selftest_wait_timeout(void *ws, uint64_t *elapsed_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -182,6 +182,26 @@ __device__ __forceinline__ bool mbar_warp_wait_bounded(uint64_t *bar, uint32_t p
         if (d.passed_warp(it)) return false;
     }
 }
+// try_wait with acquire at cluster scope: for a phase completed by another CTA of the cluster
+// (st.async bytes, whose complete-tx releases at cluster scope).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_warp_wait_cluster_bounded(uint64_t *bar, uint32_t parity) {
+    Deadline d;
+    for (uint32_t it = 0;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait_cluster(bar, parity))) return true;
+        if (d.passed_warp(it)) return false;
+    }
+}
 
 // Programmatic dependent launch.  Every kernel of the library is launched with programmatic stream
 // serialisation, so it may start while the previous kernel in the stream is still running; it

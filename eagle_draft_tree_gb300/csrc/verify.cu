@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     };
     auto wait_recv = [&]() -> bool {  // the CL records of the current exchange are in s_recv
         const int slot = xch & 1;
-        const bool got = !failed() && mbar_warp_wait_bounded(&s_rbar[slot], (xch >> 1) & 1);
+        const bool got = !failed() && mbar_warp_wait_cluster_bounded(&s_rbar[slot], (xch >> 1) & 1);
         ++xch;
         if (!got) fail();
         return got;

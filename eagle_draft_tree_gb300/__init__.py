@@ -292,7 +292,7 @@ def tree_verify_static(target_logits: torch.Tensor, draft_logits: torch.Tensor, 
                        temperature: float, depth: int, topk: int, out: dict | None = None, with_ratio: bool = True,
                        stream=None) -> dict:
     """eagle_tree_verify_static: tree_verify with the library's static device scratch instead of a
-    caller workspace (same arguments and outputs; B * n <= 7272)."""
+    caller workspace (same arguments and outputs; up to 256 KB of scratch, e.g. 113 x 64 nodes)."""
     lib = load()
     B, n, V = target_logits.shape
     _need(target_logits, "target_logits", torch.float32)

@@ -19,16 +19,23 @@
 // the tree reduces to comparisons of uniforms with precomputed ratios.
 //
 //   verify_prep_kernel  one cluster of CL CTAs (8, or 16 for vocabularies above 131072) per node
-//                       with children, or per pair of leaves.  Each thread holds 32 consecutive
-//                       tokens of a row in registers: the node's target and draft rows, or the
-//                       two leaves' target rows.  Log-sum-exp, the S_j passes and the inverse-CDF
-//                       scan are register loops; each CTA reduces a pass to one record and pushes
-//                       it to every peer (st.async completing on the receiver's mbarrier), so a
-//                       pass costs one point-to-point exchange, not a cluster-wide barrier, and the
-//                       final draw reuses the records of the last exchange.  Per-node statistics
-//                       (row maxima, log normalisers, each child's c_j and S_j) go to the workspace.
+//                       with children (sampling; greedy: per pair of nodes).  Each thread holds 32
+//                       consecutive tokens of a row in registers: the node's target and draft rows.
+//                       Log-sum-exp, the S_j passes and the inverse-CDF scan are register loops;
+//                       each CTA reduces a pass to one record and pushes it to every peer
+//                       (st.async completing on the receiver's mbarrier), so a pass costs one
+//                       point-to-point exchange, not a cluster-wide barrier, and the final draw
+//                       reuses the records of the last exchange.  Per-node statistics (row
+//                       maxima, log normalisers, each child's c_j and S_j) and every such node's
+//                       final draw go to the workspace.
 //   verify_walk_kernel  one CTA per sequence: validates the tree, computes every child's accept
-//                       ratio in double precision (one thread per node), and walks the tree.
+//                       ratio in double precision (one thread per node), and walks the tree.  A
+//                       walk that ends at a leaf (every draft on its path accepted) leaves the
+//                       bonus token's slot to the next launch.
+//   the same prep kernel, bonus mode: one cluster per sequence draws the bonus token from the
+//                       target distribution of the leaf the walk ended at, if it did.  A leaf's
+//                       draw is needed by at most one walk, so it is made only for that leaf
+//                       instead of for every leaf up front.
 #include <atomic>
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
@@ -72,6 +79,7 @@ struct VerifyArgs {
     const float *uniforms;  // [B][n]
     NodeStat *stat;         // [B][n] workspace
     int32_t *final_tok;     // [B][n] workspace
+    int32_t *bonus;         // [B] workspace: leaf | out slot << 8 for the bonus draw, or -1
     float *out_ratio;       // optional
     int32_t *out_tokens, *out_len, *out_path;
     int32_t *status;
@@ -80,6 +88,7 @@ struct VerifyArgs {
     double inv_td;  // 1/T in double
     float c;        // log2(e)/T
     int greedy;
+    int bonus_mode;  // the prep kernel draws the bonus token of the leaf in `bonus`
 };
 
 // ---- cluster record exchange.  Each CTA reduces a pass to one 16-byte record and pushes it into
@@ -383,9 +392,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     const int32_t *par = a.parents + size_t(b) * n;
 
     // ---- work of this cluster.  Greedy: nodes 2y and 2y + 1 (argmax of two target rows).
-    // Sampling: node y when it has children; when y is a leaf, the cluster of an even-ranked leaf
-    // (in ascending order among the leaves) takes y and the next leaf, an odd-ranked leaf's exits.
-    const int y = blockIdx.y;
+    // Sampling: node y when it has children (a leaf's cluster exits).  Bonus mode: the leaf the
+    // walk ended at, if any (written by the walk, the launch before this one).
+    const int breq = a.bonus_mode ? __ldg(a.bonus + blockIdx.z) : -1;
+    if (a.bonus_mode && breq < 0) return;  // uniform for the cluster: nothing has started
+    const int y = a.bonus_mode ? (breq & 255) : int(blockIdx.y);
     const int nodeA = a.greedy ? 2 * y : y;
     const int nrow = a.greedy ? -1 : __ldg(a.node_row + size_t(b) * n + nodeA);
     // The barriers exist before anything else, and the cluster barrier that publishes them to the
@@ -418,16 +429,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         if (k1) s_kid[__popc(b0) + __popc(b1 & ((1u << lane) - 1u))] = lane + 32;
         if (lane == 0) {
             s_nk = __popc(b0) + __popc(b1);
-            int second = -1;  // sampling: the leaf paired with leaf y (-2: this cluster has no work)
-            if (!a.greedy && ((leaves >> y) & 1ull)) {
-                const int lrank = __popcll(leaves & ((1ull << y) - 1ull));
-                if (lrank & 1) {
-                    second = -2;
-                } else {
-                    const uint64_t after = leaves & ~((2ull << y) - 1ull);
-                    second = after ? __ffsll(static_cast<long long>(after)) - 1 : -1;
-                }
-            }
+            int second = -1;  // greedy: the paired node (-2: this cluster has no work)
+            if (!a.greedy && !a.bonus_mode && ((leaves >> y) & 1ull)) second = -2;
+            if (a.bonus_mode) s_nk = 0;  // the leaf's own target row only
             if (a.greedy) second = 2 * y + 1 < n ? 2 * y + 1 : -1;
             s_second = second;
             s_fail = 0;
@@ -438,8 +442,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     const int second = s_second;
     if (second == -2) return;  // uniform for the cluster: no exchange or copy has started
     const int J = a.greedy ? 0 : s_nk;
-    const bool pair = J == 0;  // a leaf pair (sampling) or a node pair (greedy)
-    const int nodeB = pair ? second : -1;
+    const int nodeB = a.greedy ? second : -1;  // greedy: the paired node
     const int rowq = J > 0 ? nrow : -1;
     const bool has_q = J > 0 && rowq >= 0 && rowq < a.R;
     const float *rowA = a.target + (size_t(b) * n + nodeA) * V + lo;
@@ -745,11 +748,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
                 xp[4 * e + 3] = v.w;
             }
         }
+        int32_t *slot = a.bonus_mode ? a.out_tokens + size_t(b) * (a.D + 1) + (breq >> 8) : nullptr;
         if (owner < 0) {
-            if (rank == 0 && tid == 0 && !s_fail) a.final_tok[size_t(b) * n + node] = 0;  // no positive mass
+            if (rank == 0 && tid == 0 && !s_fail) {  // no positive mass
+                a.final_tok[size_t(b) * n + node] = 0;
+                if (slot) *slot = 0;
+            }
         } else if (rank == owner) {
             const int found = draw_in_slice(xp, s_local[k], s_draw);
-            if (found >= 0 && !s_fail) a.final_tok[size_t(b) * n + node] = lo + found;
+            if (found >= 0 && !s_fail) {
+                a.final_tok[size_t(b) * n + node] = lo + found;
+                if (slot) *slot = lo + found;
+            }
         }
     }
     cluster_wait();  // no peer leaves while records it sent may still be landing here, or vice versa
@@ -758,7 +768,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
 __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
     pdl_wait();
     pdl_launch_next();
-    __shared__ int s_tok[64], s_par[64], s_row[64], s_fin[64], s_next[64];
+    __shared__ int s_tok[64], s_par[64], s_row[64], s_fin[64], s_next[64], s_kids[64];
     __shared__ int s_bad;
     const int b = blockIdx.x, tid = threadIdx.x;
     const int n = a.n, D = a.D;
@@ -773,6 +783,7 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
         s_fin[tid] = a.final_tok[o];
     }
     s_next[tid] = n;  // no accepted child (yet)
+    s_kids[tid] = 0;
     if (tid == 0) s_bad = 0;
     __syncthreads();
     bool bad = false;
@@ -783,6 +794,7 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
         bad |= tid == 0 ? p != -1 : (p < 0 || p >= tid);
     }
     if (bad) s_bad = 1;
+    if (!bad && tid > 0 && tid < n) s_kids[p] = 1;
     __syncthreads();
     if (!a.greedy && tid > 0 && tid < n && !s_bad && (s_row[p] < 0 || s_row[p] >= a.R)) s_bad = 1;
     __syncthreads();
@@ -824,6 +836,7 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
     int32_t *op = a.out_path + size_t(b) * D;
     for (int j = 0; j <= D; ++j) ot[j] = -1;
     for (int j = 0; j < D; ++j) op[j] = -1;
+    a.bonus[b] = -1;
     if (!ok) {
         set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
         a.out_len[b] = 0;
@@ -834,7 +847,14 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
         const int next = s_next[node];
         if (next >= n || len >= D) {
             if (next < n) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);  // tree deeper than D
-            ot[len++] = s_fin[node];
+            if (!a.greedy && !s_kids[node]) {
+                // a leaf: its draw from the target distribution is made by the bonus launch,
+                // which also writes the token into this slot
+                a.bonus[b] = node | (len << 8);
+                ++len;
+            } else {
+                ot[len++] = s_fin[node];
+            }
             break;
         }
         ot[len] = s_tok[next];
@@ -850,7 +870,7 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
 size_t tree_verify_workspace_bytes(const eagle_verify_cfg &c) {
     const int n = c.keep + 1;
     return kWsHeader + align_up(size_t(c.batch) * n * sizeof(NodeStat), 256) +
-           align_up(size_t(c.batch) * n * sizeof(int32_t), 256);
+           align_up(size_t(c.batch) * n * sizeof(int32_t), 256) + align_up(size_t(c.batch) * sizeof(int32_t), 256);
 }
 
 namespace {
@@ -890,6 +910,9 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
     a.status = reinterpret_cast<int32_t *>(w);
     a.stat = reinterpret_cast<NodeStat *>(w + kWsHeader);
     a.final_tok = reinterpret_cast<int32_t *>(w + kWsHeader + align_up(size_t(c.batch) * n * sizeof(NodeStat), 256));
+    a.bonus = reinterpret_cast<int32_t *>(reinterpret_cast<unsigned char *>(a.final_tok) +
+                                          align_up(size_t(c.batch) * n * sizeof(int32_t), 256));
+    a.bonus_mode = 0;
     a.out_ratio = out_ratio;
     a.out_tokens = out_tokens;
     a.out_len = out_len;
@@ -908,13 +931,18 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
     int slice = (c.vocab + cl - 1) / cl;
     slice = (slice + 3) & ~3;
     a.slice = slice;
-    const int clusters = a.greedy ? (n + 1) / 2 : n;  // sampling: one per node, odd-ranked leaves idle
-    const cudaError_t e = cl == 8 ? launch_prep<8>(a, clusters, c.batch, stream)
-                                  : launch_prep<16>(a, clusters, c.batch, stream);
+    const int clusters = a.greedy ? (n + 1) / 2 : n;  // sampling: one per node, leaves' clusters idle
+    cudaError_t e = cl == 8 ? launch_prep<8>(a, clusters, c.batch, stream) : launch_prep<16>(a, clusters, c.batch, stream);
     if (e != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();
     if (launch_pdl(verify_walk_kernel, dim3(c.batch), dim3(64), 0, stream, 1u, a) != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();
+    if (!a.greedy) {  // the bonus token of a walk that ended at a leaf
+        a.bonus_mode = 1;
+        e = cl == 8 ? launch_prep<8>(a, 1, c.batch, stream) : launch_prep<16>(a, 1, c.batch, stream);
+        if (e != cudaSuccess) return EAGLE_ERR_CUDA;
+        note_launch();
+    }
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
 

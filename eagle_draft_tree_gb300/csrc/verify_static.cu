@@ -9,12 +9,12 @@
 
 namespace {
 
-constexpr size_t kVerifyScratchBytes = size_t(256) << 10;  // 256 KB: B x n <= 7272 tree nodes
+constexpr size_t kVerifyScratchBytes = size_t(256) << 10;  // 256 KB: e.g. 113 sequences of 64 nodes
 constexpr int kMaxDevices = 64;
 
 // The scratch itself: file-scope device storage, zero-filled when the module is loaded.  Only its
 // first word (the device status word) is ever read before this call writes it, and that word
-// starts at zero; every other byte is written by the prep kernel before the walk reads it.
+// starts at zero; every other byte is written by a kernel of the call before another reads it.
 static __device__ __align__(256) unsigned char g_verify_scratch[kVerifyScratchBytes];
 
 // Per-device address of the scratch, looked up by the first call on each device.

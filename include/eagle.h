@@ -192,9 +192,10 @@ eagle_status eagle_tree_verify(const eagle_verify_cfg *cfg, const float *target_
 
 /*
  * eagle_tree_verify without a caller workspace: the same computation and outputs (the same
- * kernels run), with the scratch in the library's own static device storage of 256 KB, which
- * holds up to 7272 tree nodes in all (B * n; e.g. 113 sequences of 64 nodes); a configuration
- * needing more returns EAGLE_ERR_UNSUPPORTED before anything runs.  It exists for callers that cannot hand the library a device workspace:
+ * kernels run), with the scratch in the library's own static device storage of 256 KB: about
+ * 36 bytes per tree node and 4 per sequence (eagle_tree_verify_workspace_size), e.g. 113
+ * sequences of 64 nodes; a configuration needing more returns EAGLE_ERR_UNSUPPORTED before
+ * anything runs.  It exists for callers that cannot hand the library a device workspace:
  * a serving process that reserves all device memory for weights and the KV cache at start-up and
  * grants no further buffers, or a host framework whose plugin interface passes tensors but no
  * scratch.  The pages describe no such entry point; it is an interface convenience only.

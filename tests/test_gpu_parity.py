@@ -203,6 +203,27 @@ def test_tree_verify_low_noise_accepts_deep_paths():
     assert o["out_len"].max() >= 4
 
 
+@pytest.mark.parametrize("shape", [(4, 128256, 8, 10, 60), (3, 150000, 4, 4, 20), (6, 1000, 3, 4, 10)])
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_tree_verify_bonus_token_at_a_leaf(shape, T):
+    """Target rows equal to their draft rows make every accept ratio exactly 1, so every walk
+    accepts down to a leaf and ends with the bonus token drawn from that leaf's target
+    distribution (the draw made for that one leaf after the walk).  Both slice widths (8 and 16
+    CTAs per row) are covered."""
+    B, V, D, k, m = shape
+    wl = datagen.WORKLOADS["tiny_f32"].with_(batch=B, vocab=V, depth=D, topk=k, keep=m, noise=0.0)
+    g, o = _verify_case(wl, 77, T)
+    assert not compare_verify(g, o)
+    draft, root = _draft(wl, 77)
+    parents = oracle.build_tree(np_(draft), np_(root), D, k, m)["parents"]
+    for b in range(B):
+        L = int(g["out_len"][b])
+        path = [int(x) for x in g["out_path"][b][:L - 1]]
+        end = path[-1] if path else 0
+        assert end not in set(int(x) for x in parents[b]), f"sequence {b} did not end at a leaf"
+        assert int(g["out_tokens"][b][L - 1]) >= 0
+
+
 def test_tree_verify_bad_tree_sets_status():
     wl = datagen.WORKLOADS["tiny_f32"].with_(batch=2)
     draft, root = _draft(wl, 1)

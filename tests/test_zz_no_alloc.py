@@ -17,7 +17,7 @@ DEV = "cuda"
 
 def test_static_verify_rejects_configs_beyond_its_scratch():
     lib = eg.load()
-    # 120 sequences of 64 nodes need more than the 256 KB scratch (B * n <= 7272 fits)
+    # 120 sequences of 64 nodes need more than the 256 KB scratch (113 of 64 fit)
     big = eg.VerifyCfg(120, 1000, 8, 8, 63, 1.0)
     assert lib.eagle_tree_verify_workspace_size(ctypes.byref(big)) > (256 << 10)
     st = lib.eagle_tree_verify_static(ctypes.byref(big), *([None] * 10), None)

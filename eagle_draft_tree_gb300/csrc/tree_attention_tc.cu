@@ -107,13 +107,21 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(bar)) : "memory");
 }
-// One 4-D box: both 64-dim halves of kNkv rows of one KV head; lands as [half][row][128 B].
-__device__ __forceinline__ void tma_kv(const CUtensorMap *map, void *dst, uint64_t *bar, int row, int head) {
+// One 4-D box: both 64-dim halves of kNkv rows of one KV head; lands as [half][row][128 B].  The
+// KV cache is read once per call and is larger than L2, so its lines are marked evict-first:
+// the L2 keeps what the other kernels of a round reuse (their code, the draft rows, the tree).
+__device__ __forceinline__ void tma_kv(const CUtensorMap *map, void *dst, uint64_t *bar, int row, int head,
+                                       uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
-        "%5}], [%6];" ::"r"(sa(dst)),
-        "l"(map), "r"(0), "r"(row), "r"(0), "r"(head), "r"(sa(bar))
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4, %5}], [%6], %7;" ::"r"(sa(dst)),
+        "l"(map), "r"(0), "r"(row), "r"(0), "r"(head), "r"(sa(bar)), "l"(policy)
         : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 __device__ __forceinline__ void tma_3d(const CUtensorMap *map, void *dst, uint64_t *bar, int x, int y, int z) {
     asm volatile(
@@ -294,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_3d(&qmap, sm + t * kQTile + h * kQHalf, &bars.q_full, 64 * h, g * p.G, zq + t * (128 / p.G));
             const int zc = (l * p.B + b) * p.S_max;
             const int zt = (l * p.B + b) * p.n;
+            const uint64_t pol = l2_evict_first_policy();
             // fixed order K(j), V(j); each waits (blocking) for its stage's previous tile to be released
             for (int j = 0; j < ntiles; ++j) {
                 const int sk = j % kKStages, sv = j % kVStages;
@@ -301,13 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 mbar_expect_tx(&bars.k_full[sk], kTileBytes);
                 tma_kv(j == nctx ? &ktmap : &kmap, sm + kOffK + sk * kTileBytes, &bars.k_full[sk],
-                       j == nctx ? zt : zc + j * kNkv, g);
+                       j == nctx ? zt : zc + j * kNkv, g, pol);
                 ++k_issued;
                 if (j >= kVStages && !wait_or_abort(&bars.v_empty[sv], ((j / kVStages) - 1) & 1, abort_flag, p.status))
                     break;
                 mbar_expect_tx(&bars.v_full[sv], kTileBytes);
                 tma_kv(j == nctx ? &vtmap : &vmap, sm + kOffV + sv * kTileBytes, &bars.v_full[sv],
-                       j == nctx ? zt : zc + j * kNkv, g);
+                       j == nctx ? zt : zc + j * kNkv, g, pol);
                 ++v_issued;
             }
         }

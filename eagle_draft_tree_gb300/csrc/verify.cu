@@ -59,15 +59,19 @@ constexpr size_t kPrepSmem = 2 * size_t(kSliceMax) * sizeof(float);  // both row
 constexpr int kMaxNodes = 64;
 constexpr double kFxInv = 1.0 / 4503599627370496.0;  // fixed-point unit of weight sums: 2^-52
 
-// Per-node statistics the prep kernel leaves for the walk, in the forms the prep computes them
-// (the walk converts them to double).  Row statistics (mp, mq, lnsp, lnsq) belong to a node with
-// children; (cj, sj) to a node as a child: its parent's rejection chain state when this child is
-// tested.
+// Per-node statistics the prep kernel leaves for the walk.  Row statistics (mp, mq, lnsp, lnsq)
+// belong to a node with children; (cj, sj) to a node as a child: its parent's rejection chain
+// state when this child is tested.  Child j (sibling index) is accepted when
+// u < (p0/q0 - c_j)+ / S_j at its token, i.e. u S_j + c_j < p0/q0 (S_j = 0 accepts), decided
+// exactly in 2^-52 units.  When a chain stops at the first accepted child, the prep makes the
+// tests itself and leaves each child's verdict in the top bits of sj.
 struct NodeStat {
     float mp, mq;      // row maxima (logit units)
     float lnsp, lnsq;  // ln of the normaliser sum_t exp((x_t - max) / T), target and draft rows
-    uint64_t cj, sj;   // c_j, S_j of the parent's chain at this child's sibling index, in 2^-52 units
+    uint64_t cj, sj;   // c_j, S_j (<= 2^52) in 2^-52 units; sj bits 62-63: the prep's verdict
 };
+constexpr int kVerdictShift = 62;  // 0: not tested by the prep, 1: rejected, 2: accepted
+constexpr uint64_t kSjMask = (1ull << kVerdictShift) - 1;
 static_assert(sizeof(NodeStat) == 32, "NodeStat layout");
 
 struct VerifyArgs {
@@ -89,6 +93,8 @@ struct VerifyArgs {
     float c;        // log2(e)/T
     int greedy;
     int bonus_mode;  // the prep kernel draws the bonus token of the leaf in `bonus`
+    int full_chain;  // every child tested (its ratio is an output); else a chain stops at the
+                     // first accepted child
 };
 
 // ---- cluster record exchange.  Each CTA reduces a pass to one 16-byte record and pushes it into
@@ -224,6 +230,17 @@ __device__ __forceinline__ uint64_t scale_fx(uint64_t total, float u) {
     if (sh >= 128) return 0;
     if (sh >= 64) return hi >> (sh - 64);
     return (hi << (64 - sh)) | (lo >> sh);
+}
+
+// p0/q0 in 2^-52 units, clamped at 2^11 (c_j <= 64 and u S_j < 1, so the clamp never decides a
+// test); NaN and non-positive ratios give 0.
+__device__ __forceinline__ uint64_t ratio_fx(double rr) {
+    const double v = rr * 4503599627370496.0;  // 2^52
+    return v >= 9223372036854775808.0 ? (1ull << 63) : (v > 0.0 ? __double2ull_rz(v) : 0ull);
+}
+// The accept test u < (p0/q0 - c)+ / S, as u S + c < p0/q0 in 2^-52 units (S = 0 accepts).
+__device__ __forceinline__ bool accept_fx(float u, uint64_t c, uint64_t S, uint64_t rrfx) {
+    return S == 0 || scale_fx(S, u) + c < rrfx;
 }
 
 // Warp-wide merge of (max, scaled sum) pairs: M = max over the lanes, S = sum of s 2^((m - M) c)
@@ -377,6 +394,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     __shared__ __align__(8) uint64_t s_pbar;     // every warp's partial of the current pass posted
     __shared__ __align__(8) uint64_t s_lbar[2];  // a row slice landed
     __shared__ int s_kid[kMaxNodes];             // children of the node (sampling), ascending
+    __shared__ uint64_t s_rrfx[kMaxNodes];       // each child's p0/q0 at its token, 2^-52 units
+    __shared__ float s_uk[kMaxNodes];            // each child's uniform
+    __shared__ int s_dec[2];                     // the accept test of the current child, by parity
+    __shared__ __align__(8) uint64_t s_decbar;   // s_dec written
     __shared__ int s_nk, s_fail, s_second;
     __shared__ int s_own[2];
     __shared__ uint64_t s_local[2];
@@ -408,6 +429,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         mbar_init(&s_pbar, kWarpsPrep);
         mbar_init(&s_lbar[0], 1);
         mbar_init(&s_lbar[1], 1);
+        mbar_init(&s_decbar, 1);
         fence_barrier_init();
     }
     cluster_arrive();
@@ -445,6 +467,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     const int nodeB = a.greedy ? second : -1;  // greedy: the paired node
     const int rowq = J > 0 ? nrow : -1;
     const bool has_q = J > 0 && rowq >= 0 && rowq < a.R;
+    // warp 4: the children's logits at their tokens, loaded now for the accept tests
+    float kx = 0.f, ky = 0.f;
+    int ktok = -1;
+    if (warp == 4 && has_q)
+        for (int jj = lane; jj < J && jj < 32; jj += 32) {
+            ktok = __ldg(a.tokens + size_t(b) * n + s_kid[jj]);
+            if (ktok >= 0 && ktok < V) {
+                kx = __ldg(a.target + (size_t(b) * n + nodeA) * V + ktok);
+                ky = __ldg(a.draft + (size_t(b) * a.R + rowq) * V + ktok);
+            }
+        }
     const float *rowA = a.target + (size_t(b) * n + nodeA) * V + lo;
     const float *rowB = nullptr;
     if (nodeB >= 0) rowB = a.target + (size_t(b) * n + nodeB) * V + lo;
@@ -599,6 +632,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     // ---- row statistics of both held rows.  Values become 2^((x - m) c) against the thread's max
     // m, so the probabilities later cost one multiply each (no second exponential).
     float mA, mB = -INFINITY, sB = 0.f;
+    float4 gst;  // the rows' global (max, sum) statistics
     const float sA = exp_run(xp, mA, c);
     if (rowB) sB = exp_run(xq, mB, c);
     cluster_wait();  // every peer's barriers exist
@@ -626,6 +660,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
                 s_local[k] = loc;
             }
         }
+        gst = g;
         if (warp == 3 && lane == 0 && rank == 0 && J > 0 && !s_fail) {
             NodeStat *st = a.stat + size_t(b) * n + nodeA;
             st->mp = g.x;
@@ -649,15 +684,37 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     // distribution).  c_j and S_j are fixed-point integers, the same in every thread; each pass
     // uses c_{j+1} rounded to float.  When the last pass moves c, its per-rank sums are exactly
     // the final draw's per-rank weights: the residual below is formed with the same float c.
+    // Child j is tested with c_j and S_j, known before pass j; pass j is issued first and the
+    // test is made while its exchange is in flight.  Unless every ratio is wanted, the chain stops
+    // at the first accepted child: the walk takes that child, and the node's final draw (made
+    // only when every child is rejected) is not needed.
+    // warp 4: every child's p0/q0 at its token, in double precision from the row statistics:
+    // exp(((x - Mp) / T - ln Sp) - ((y - Mq) / T - ln Sq)), its fixed-point image, and its uniform
+    // (lanes past 32 children load their logits here)
+    auto child_ratios = [&]() {
+        const double lnsp = double(logf(gst.y)), lnsq = gst.w > 0.f ? double(logf(gst.w)) : 0.0;
+        for (int jj = lane; jj < J; jj += 32) {
+            const int kid = s_kid[jj];
+            if (jj >= 32) {
+                ktok = __ldg(a.tokens + size_t(b) * n + kid);
+                if (ktok >= 0 && ktok < V) {
+                    kx = __ldg(a.target + (size_t(b) * n + nodeA) * V + ktok);
+                    ky = __ldg(a.draft + (size_t(b) * a.R + rowq) * V + ktok);
+                }
+            }
+            double rr = NAN;
+            if (ktok >= 0 && ktok < V)
+                rr = exp(((double(kx) - double(gst.x)) * a.inv_td - lnsp) - ((double(ky) - double(gst.z)) * a.inv_td - lnsq));
+            s_rrfx[jj] = ratio_fx(rr);
+            s_uk[jj] = __ldg(a.uniforms + size_t(b) * n + kid);
+        }
+        __syncwarp();
+    };
     uint64_t cj = 0, Sj = 1ull << 52;
     float cnf = 1.f;  // c_1 = c_0 + S_0
     bool decided = !has_q;
+    bool accepted = false;  // a child was accepted and the chain stopped there
     for (int j = 0; j < J && has_q; ++j) {
-        if (rank == 0 && tid == 0 && !s_fail) {  // the child tested at step j
-            NodeStat *st = a.stat + size_t(b) * n + s_kid[j];
-            st->cj = cj;
-            st->sj = Sj;
-        }
         // the last pass forms exact chunk weights (they may become the final draw's); earlier
         // passes need only the sum: one float sum per thread
         uint64_t part;
@@ -675,9 +732,44 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
             part = to_fx((t0 + t1) + (t2 + t3));
         }
         post(fx_rec(warp_sum_fx(part)));
+        // The accept test of child j, made by one lane of warp 4 while the pass's exchange runs
+        // (double precision stays off the other warps: the FP64 pipe is narrow), published
+        // through s_dec and s_decbar; every warp reads it after the exchange.  The inputs are the
+        // same in every CTA, so every CTA of the cluster takes the same decision.
+        if (warp == 4) {
+            if (j == 0 && !a.full_chain) child_ratios();
+            if (lane == 0 && a.full_chain) {  // the walk makes every test
+                if (rank == 0 && !s_fail) {
+                    NodeStat *st = a.stat + size_t(b) * n + s_kid[j];
+                    st->cj = cj;
+                    st->sj = Sj;
+                }
+            } else if (lane == 0) {
+                // u < (p0/q0 - c_j)+ / S_j, i.e. u S_j + c_j < p0/q0, exactly in 2^-52 units (an
+                // empty residual, S_j = 0, accepts)
+                const bool acc = accept_fx(s_uk[j], cj, Sj, s_rrfx[j]);
+                s_dec[j & 1] = acc;
+                if (rank == 0 && !s_fail) {
+                    NodeStat *st = a.stat + size_t(b) * n + s_kid[j];
+                    st->cj = cj;
+                    st->sj = Sj | (uint64_t(acc ? 2 : 1) << kVerdictShift);
+                    if (acc)
+                        for (int k2 = j + 1; k2 < J; ++k2) a.stat[size_t(b) * n + s_kid[k2]].sj = 0;  // not tested
+                }
+                mbar_arrive(&s_decbar);
+            }
+            __syncwarp();
+        }
         if (warp == 0 && wait_posts()) send(fx_rec(fold_posts()));
         const int slot = xch & 1;
-        const uint64_t g = recv_fx();
+        const uint64_t g = recv_fx();  // received in every case: the exchanges stay paired
+        if (!a.full_chain) {
+            if (!mbar_warp_wait_bounded(&s_decbar, j & 1)) fail();
+            if (*reinterpret_cast<volatile int *>(&s_dec[j & 1])) {
+                accepted = true;
+                break;
+            }
+        }
         const bool moved = g > 0;
         if (moved) {
             cj += Sj;
@@ -699,12 +791,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     }
     // residual weights of a node with children: (p0 - c_J q)+, with c_J as the pass that set it
     // rounded it
-    if (has_q) {
+    if (has_q && !accepted) {
         const float cjf = fx_to_float(cj);
 #pragma unroll
         for (int e = 0; e < kE; ++e) xp[e] = fmaxf(fmaf(-cjf, xq[e], xp[e]), 0.f);
     }
-    if (has_q && !decided) {
+    if (has_q && !decided && !accepted) {
         // the last pass left c unchanged: one more exchange for the residual's per-rank weights
         post(fx_rec(warp_sum_fx(weight_fx(xp))));
         if (warp == 0) {
@@ -733,7 +825,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         for (int e = 0; e < kChunks; ++e)
             *reinterpret_cast<float4 *>(dst + chunk_tok(e)) = make_float4(xq[4 * e], xq[4 * e + 1], xq[4 * e + 2], xq[4 * e + 3]);
     }
-    for (int k = 0; k < (nodeB >= 0 ? 2 : 1); ++k) {
+    for (int k = 0; k < (accepted ? 0 : nodeB >= 0 ? 2 : 1); ++k) {
         const int owner = s_own[k];
         const int node = k ? nodeB : nodeA;
         if (k == 1) {
@@ -768,12 +860,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
 __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
     pdl_wait();
     pdl_launch_next();
-    __shared__ int s_tok[64], s_par[64], s_row[64], s_fin[64], s_next[64], s_kids[64];
+    __shared__ int s_tok[64], s_row[64], s_fin[64], s_next[64], s_kids[64];
     __shared__ int s_bad;
     const int b = blockIdx.x, tid = threadIdx.x;
     const int n = a.n, D = a.D;
     int t = 0, p = -1;
     float u = 0.f;
+    NodeStat cs = {};
     if (tid < n) {  // every load of the node's own inputs at once
         const size_t o = size_t(b) * n + tid;
         t = a.tokens[o];
@@ -781,6 +874,7 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
         u = a.uniforms[o];
         s_row[tid] = a.node_row[o];
         s_fin[tid] = a.final_tok[o];
+        if (!a.greedy && tid > 0) cs = a.stat[o];
     }
     s_next[tid] = n;  // no accepted child (yet)
     s_kids[tid] = 0;
@@ -789,7 +883,6 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
     bool bad = false;
     if (tid < n) {
         s_tok[tid] = t;
-        s_par[tid] = p;
         bad = t < 0 || t >= a.V;
         bad |= tid == 0 ? p != -1 : (p < 0 || p >= tid);
     }
@@ -798,31 +891,27 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
     __syncthreads();
     if (!a.greedy && tid > 0 && tid < n && !s_bad && (s_row[p] < 0 || s_row[p] >= a.R)) s_bad = 1;
     __syncthreads();
-    // accept ratio of every child (one thread per node, double precision).  With the parent's
-    // row statistics, p0 / q0 = exp(((x - Mp) - (y - Mq)) / T - ln Sp + ln Sq) at the child's
-    // token; the child tested after j rejected siblings has ratio (p0 / q0 - c_j)+ / S_j
-    // (p0 / q0 itself for j = 0), as p_j / q = (p0 - c_j q)+ / (S_j q).
+    // every child's accept test: the ratio (p0 / q0 - c_j)+ / S_j at its token after j rejected
+    // siblings (p0 / q0 itself for j = 0, as p_j / q = (p0 - c_j q)+ / (S_j q)) against its
+    // uniform.  A chain that stopped at its first accepted child was tested by the prep (the
+    // verdict is in sj); with every ratio wanted, each child's is computed here, one thread per
+    // node, in double precision from its parent's row statistics.
     const bool ok = !s_bad;
     bool acc = false;
     if (tid < n) {
         float r = NAN;
-        if (!a.greedy && ok && tid > 0) {
-            int sib = 0;
-            for (int j = p + 1; j < tid; ++j) sib += s_par[j] == p;
+        if (!a.greedy && ok && tid > 0 && !a.full_chain) {
+            acc = (cs.sj >> kVerdictShift) == 2;
+        } else if (!a.greedy && ok && tid > 0) {
             const NodeStat ps = a.stat[size_t(b) * n + p];
-            const NodeStat cs = a.stat[size_t(b) * n + tid];
             const double x = a.target[(size_t(b) * n + p) * a.V + t];
             const double yv = a.draft[(size_t(b) * a.R + s_row[p]) * a.V + t];
-            const double lp = (x - double(ps.mp)) * a.inv_td - double(ps.lnsp);
-            const double lq = (yv - double(ps.mq)) * a.inv_td - double(ps.lnsq);
-            const double rr = exp(lp - lq);
-            if (sib == 0) {
-                r = float(rr);
-            } else {
-                const double sj = double(cs.sj) * kFxInv;
-                r = sj > 0.0 ? float(fmax(rr - double(cs.cj) * kFxInv, 0.0) / sj) : INFINITY;
-            }
-            acc = u < r;
+            const double rr = exp(((x - double(ps.mp)) * a.inv_td - double(ps.lnsp)) -
+                                  ((yv - double(ps.mq)) * a.inv_td - double(ps.lnsq)));
+            const uint64_t sj = cs.sj & kSjMask;
+            const double sjd = double(sj) * kFxInv;
+            r = cs.cj == 0 ? float(rr) : (sjd > 0.0 ? float(fmax(rr - double(cs.cj) * kFxInv, 0.0) / sjd) : INFINITY);
+            acc = accept_fx(u, cs.cj, sj, ratio_fx(rr));
         } else if (a.greedy && ok && tid > 0) {
             acc = t == s_fin[p];
         }
@@ -913,6 +1002,7 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
     a.bonus = reinterpret_cast<int32_t *>(reinterpret_cast<unsigned char *>(a.final_tok) +
                                           align_up(size_t(c.batch) * n * sizeof(int32_t), 256));
     a.bonus_mode = 0;
+    a.full_chain = out_ratio != nullptr;
     a.out_ratio = out_ratio;
     a.out_tokens = out_tokens;
     a.out_len = out_len;

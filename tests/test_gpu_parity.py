@@ -163,16 +163,16 @@ def test_tree_attention_bad_context_sets_status():
 
 # ---------------------------------------------------------------- verify
 
-def _verify_case(wl, seed, T):
+def _verify_case(wl, seed, T, with_ratio=True):
     draft, root = _draft(wl, seed)
     o_tree = oracle.build_tree(np_(draft), np_(root), wl.depth, wl.topk, wl.keep)
     sig = datagen.noise_sigmas(wl, seed)
     target = datagen.target_logits(draft, torch.from_numpy(o_tree["node_row"]).to(DEV), sig, seed)
     u = datagen.uniforms(wl.batch, wl.nodes, seed, DEV)
     tree = oracle_tree_tensors(o_tree, DEV)
-    g = eg.tree_verify(target, draft, tree, u, temperature=T, depth=wl.depth, topk=wl.topk)
+    g = eg.tree_verify(target, draft, tree, u, temperature=T, depth=wl.depth, topk=wl.topk, with_ratio=with_ratio)
     torch.cuda.synchronize()
-    g = {k: np_(v) for k, v in g.items()}
+    g = {k: np_(v) for k, v in g.items() if v is not None}
     o = oracle.tree_verify(np_(target), np_(draft), o_tree["tokens"], o_tree["parents"], o_tree["node_row"], np_(u),
                            T, wl.depth + 1)
     return g, o
@@ -184,11 +184,14 @@ VERIFY_SHAPES = [(4, 1000, 3, 4, 10), (2, 32000, 6, 10, 50), (2, 128256, 8, 10, 
 
 @pytest.mark.parametrize("shape", VERIFY_SHAPES)
 @pytest.mark.parametrize("T", [1.0, 0.7, 0.0])
-def test_tree_verify_matches_oracle(shape, T):
+@pytest.mark.parametrize("with_ratio", [True, False], ids=["ratios", "first-accept"])
+def test_tree_verify_matches_oracle(shape, T, with_ratio):
+    """With every child's ratio requested the prep tests every child; without, a node's chain
+    stops at its first accepted child.  The committed tokens and path are the same either way."""
     B, V, D, k, m = shape
     wl = datagen.WORKLOADS["tiny_f32"].with_(batch=B, vocab=V, depth=D, topk=k, keep=m)
     for seed in (0, 1):
-        g, o = _verify_case(wl, 40 + seed, T)
+        g, o = _verify_case(wl, 40 + seed, T, with_ratio)
         log = []
         excused = compare_verify(g, o, log)
         assert len(excused) <= max(1, B // 8), log
@@ -205,14 +208,15 @@ def test_tree_verify_low_noise_accepts_deep_paths():
 
 @pytest.mark.parametrize("shape", [(4, 128256, 8, 10, 60), (3, 150000, 4, 4, 20), (6, 1000, 3, 4, 10)])
 @pytest.mark.parametrize("T", [1.0, 0.7])
-def test_tree_verify_bonus_token_at_a_leaf(shape, T):
+@pytest.mark.parametrize("with_ratio", [True, False], ids=["ratios", "first-accept"])
+def test_tree_verify_bonus_token_at_a_leaf(shape, T, with_ratio):
     """Target rows equal to their draft rows make every accept ratio exactly 1, so every walk
     accepts down to a leaf and ends with the bonus token drawn from that leaf's target
     distribution (the draw made for that one leaf after the walk).  Both slice widths (8 and 16
     CTAs per row) are covered."""
     B, V, D, k, m = shape
     wl = datagen.WORKLOADS["tiny_f32"].with_(batch=B, vocab=V, depth=D, topk=k, keep=m, noise=0.0)
-    g, o = _verify_case(wl, 77, T)
+    g, o = _verify_case(wl, 77, T, with_ratio)
     assert not compare_verify(g, o)
     draft, root = _draft(wl, 77)
     parents = oracle.build_tree(np_(draft), np_(root), D, k, m)["parents"]

@@ -38,16 +38,19 @@ def test_workload_round(name):
     u = datagen.uniforms(wl.batch, wl.nodes, seed, DEV)
     tree = oracle_tree_tensors(o_tree, DEV)
     target_np, u_np = np_(target), np_(u)
+    # (with every ratio requested, and without, as the benchmark calls it)
     for T in ([wl.temperature, 0.0] if name == "llama31_8b" else [wl.temperature]):
-        gv = eg.tree_verify(target, draft, tree, u, temperature=T, depth=wl.depth, topk=wl.topk, ws=ws)
-        torch.cuda.synchronize()
-        gv = {k: np_(v) for k, v in gv.items()}
         ov = oracle.tree_verify(target_np, draft_np, o_tree["tokens"], o_tree["parents"], o_tree["node_row"], u_np,
                                 T, wl.depth + 1)
-        vlog = []
-        compare_verify(gv, ov, vlog)
-        assert len(vlog) <= max(1, wl.batch // 16), vlog
-        assert ws.status() == eg.EAGLE_OK
+        for with_ratio in (True, False):
+            gv = eg.tree_verify(target, draft, tree, u, temperature=T, depth=wl.depth, topk=wl.topk, ws=ws,
+                                with_ratio=with_ratio)
+            torch.cuda.synchronize()
+            gv = {k: np_(v) for k, v in gv.items() if v is not None}
+            vlog = []
+            compare_verify(gv, ov, vlog)
+            assert len(vlog) <= max(1, wl.batch // 16), vlog
+            assert ws.status() == eg.EAGLE_OK
     del target, target_np
 
     # attention over every layer at full size; oracle on sampled rows

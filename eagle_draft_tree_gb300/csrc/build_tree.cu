@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     __shared__ int s_ptok[kMaxPool];      // pool: token
     __shared__ unsigned char s_dep[kMaxPool];
     __shared__ int s_slot[16];
-    __shared__ int s_hist[256];
+    __shared__ int s_hist[2][256];  // by pass parity: a pass clears the next pass's buffer
     __shared__ uint64_t s_prefix;
     __shared__ uint64_t s_gather[32];
     __shared__ int s_remaining, s_bcount;
@@ -306,10 +306,27 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = a.k, R = a.R, D = a.D, m = a.m;
 
-    // the rows' children (written by row_topk_kernel)
-    for (int i = tid; i < R * k; i += kSelThreads) {
-        s_lc[i] = a.row_lc[size_t(b) * R * k + i];
-        s_ctok[i] = a.row_tok[size_t(b) * R * k + i];
+    // the rows' children (written by row_topk_kernel): every load in flight before the first store
+    {
+        constexpr int kPer = kMaxPool / kSelThreads;
+        double lcv[kPer];
+        int tkv[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int i = tid + u * kSelThreads;
+            if (i < R * k) {
+                lcv[u] = a.row_lc[size_t(b) * R * k + i];
+                tkv[u] = a.row_tok[size_t(b) * R * k + i];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int i = tid + u * kSelThreads;
+            if (i < R * k) {
+                s_lc[i] = lcv[u];
+                s_ctok[i] = tkv[u];
+            }
+        }
     }
     __syncthreads();
     // depth 1: the root's children (row 0)
@@ -326,19 +343,27 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     // depths 2..D: the k best nodes of the previous depth are expanded; frontier slot = rank
     int lb = 0, cnt = k, np = k;
     for (int f = 1; f <= D - 1; ++f) {
-        for (int e = lb + tid; e < lb + cnt; e += kSelThreads) {
-            const uint64_t v = s_key[e];
+        // rank of each candidate of the previous depth: two adjacent threads per candidate, each
+        // counting the keys above it in one half of the candidates (the loop is warp-uniform)
+        const int half = (cnt + 1) >> 1;
+        for (int base = 0; base < cnt; base += kSelThreads / 2) {
+            const int ei = base + (tid >> 1);
+            const bool act = ei < cnt;
+            const int e = lb + ei;
+            const uint64_t v = act ? s_key[e] : ~0ull;
+            const int o0 = lb + (tid & 1) * half, o1 = min(o0 + half, lb + cnt);
             int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent chains of shared loads
-            int o = lb;
-            for (; o + 4 <= lb + cnt; o += 4) {
+            int o = o0;
+            for (; o + 4 <= o1; o += 4) {
                 r0 += s_key[o] > v;
                 r1 += s_key[o + 1] > v;
                 r2 += s_key[o + 2] > v;
                 r3 += s_key[o + 3] > v;
             }
-            for (; o < lb + cnt; ++o) r0 += s_key[o] > v;
-            const int rank = (r0 + r1) + (r2 + r3);
-            if (rank < k) {
+            for (; o < o1; ++o) r0 += s_key[o] > v;
+            const int part = (r0 + r1) + (r2 + r3);
+            const int rank = part + __shfl_xor_sync(0xffffffffu, part, 1);
+            if (act && !(tid & 1) && rank < k) {
                 s_slot[rank] = e;
                 s_row[e] = 1 + (f - 1) * k + rank;
             }
@@ -375,11 +400,11 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         s_remaining = m;
         s_bcount = 0x7fffffff;
     }
+    s_hist[0][tid] = 0;  // kSelThreads == 256 buckets
     __syncthreads();
     uint64_t hmask = 0;
-    for (int shift = 56; shift >= 0; shift -= 8) {
-        s_hist[tid] = 0;  // kSelThreads == 256 buckets
-        __syncthreads();
+    for (int shift = 56, cur = 0; shift >= 0; shift -= 8, cur ^= 1) {
+        s_hist[cur ^ 1][tid] = 0;  // the previous pass's buffer, read before its closing barrier
         const uint64_t prefix = s_prefix;
         for (int e0 = 0; e0 < np; e0 += kSelThreads) {  // whole warps take part in the match
             const int e = e0 + tid;
@@ -387,14 +412,14 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
             const bool in = e < np && (key & hmask) == prefix;
             const unsigned dig = in ? unsigned((key >> shift) & 255) : 256u + unsigned(lane);
             const unsigned grp = __match_any_sync(0xffffffffu, dig);
-            if (in && lane == __ffs(grp) - 1) atomicAdd(&s_hist[dig], __popc(grp));
+            if (in && lane == __ffs(grp) - 1) atomicAdd(&s_hist[cur][dig], __popc(grp));
         }
         __syncthreads();
         if (warp == 0) {
             // buckets from the top: lane l owns buckets 255-8l .. 248-8l
             int cntl = 0;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) cntl += s_hist[255 - 8 * lane - q];
+            for (int q = 0; q < 8; ++q) cntl += s_hist[cur][255 - 8 * lane - q];
             int incl = cntl;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -407,7 +432,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
                 int acc = excl;
                 for (int q = 0; q < 8; ++q) {
                     const int bucket = 255 - 8 * lane - q;
-                    const int h = s_hist[bucket];
+                    const int h = s_hist[cur][bucket];
                     if (acc + h >= need) {
                         s_prefix = prefix | (uint64_t(bucket) << shift);
                         s_remaining = need - acc;

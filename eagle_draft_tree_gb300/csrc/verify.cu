@@ -433,7 +433,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         fence_barrier_init();
     }
     cluster_arrive();
-    if (warp == 0) {
+    if (a.bonus_mode) {  // the leaf's own target row only: no tree to scan
+        if (tid == 0) {
+            s_nk = 0;
+            s_second = -1;
+            s_fail = 0;
+            s_own[0] = s_own[1] = -1;
+        }
+    } else if (warp == 0) {
         // every node's "has children" bit, and the children of node y, from the <= 64 parents
         const int p0 = lane < n ? __ldg(par + lane) : -1;
         const int p1 = lane + 32 < n ? __ldg(par + lane + 32) : -1;
@@ -452,8 +459,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         if (lane == 0) {
             s_nk = __popc(b0) + __popc(b1);
             int second = -1;  // greedy: the paired node (-2: this cluster has no work)
-            if (!a.greedy && !a.bonus_mode && ((leaves >> y) & 1ull)) second = -2;
-            if (a.bonus_mode) s_nk = 0;  // the leaf's own target row only
+            if (!a.greedy && ((leaves >> y) & 1ull)) second = -2;
             if (a.greedy) second = 2 * y + 1 < n ? 2 * y + 1 : -1;
             s_second = second;
             s_fail = 0;

@@ -240,6 +240,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
 
     # end to end: per-round inputs from pinned host memory, the three calls, results back to host
     e2e = run_e2e(eg, lib, wl, sets[0], outs, ws, stream, dev, min(K, args.e2e_steps), world)
+    commit = run_kv_commit(eg, lib, wl, sets[0], outs, ws, stream, dev)
 
     bytes_ = datagen.bytes_of(wl, ctx_total=float(sets[0].attn["ctx_len"].sum().item()))
     peaks = _peaks()
@@ -265,6 +266,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
                            "gbs": metric_bytes / (ms / K * 1e-3) / 1e9,
                            "frac": metric_bytes / (ms / K * 1e-3) / 1e9 / peaks["hbm_gbs"]},
         "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "mean_committed": mean_len,
+        "kv_commit": commit,
     }
     return res
 
@@ -350,6 +352,41 @@ def run_e2e(eg, lib, wl, rd: Round, outs, ws, stream, dev, steps, world) -> dict
             "d2h_bytes_per_step": d2h, "steps": steps,
             "pipeline": "inputs copied on a second stream in the order the calls need them; two device "
                         "input sets alternate between rounds"}
+
+
+def run_kv_commit(eg, lib, wl, rd: Round, outs, ws, stream, dev, calls: int = 200) -> dict:
+    """eagle_kv_commit after the round (not part of the round's metric): the committed nodes' keys
+    and values appended to a cache with room for them (the round's own cache is full).  Timed
+    with CUDA events over `calls` launches of the same commit."""
+    a = rd.attn
+    L, B, n, Hkv, d = a["k_tree"].shape
+    ctx = a["ctx_len"]
+    S = int(ctx.max().item()) + wl.depth + 8
+    kc = torch.zeros((L, B, S, Hkv, d), dtype=a["k_tree"].dtype, device=dev)
+    vc = torch.zeros_like(kc)
+    new_ctx = torch.empty_like(ctx)
+    cfg = eg.AttnCfg(B, L, n, Hkv, Hkv, d, S, eg.EAGLE_DTYPE_BF16 if kc.dtype == torch.bfloat16 else eg.EAGLE_DTYPE_F32,
+                     0.0)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    cargs = (ctypes.byref(cfg), wl.depth, P(a["k_tree"]), P(a["v_tree"]), P(outs["out_path"]), P(outs["out_len"]),
+             P(ctx), P(kc), P(vc), P(new_ctx), ws.ptr, ctypes.c_size_t(ws.nbytes), ctypes.c_void_p(stream.cuda_stream))
+    for _ in range(3):
+        if lib.eagle_kv_commit(*cargs) != 0:
+            raise RuntimeError("eagle_kv_commit failed")
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(calls):
+        lib.eagle_kv_commit(*cargs)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if ws.status(stream) != 0:
+        raise RuntimeError("device status not OK after the KV commits")
+    us = e0.elapsed_time(e1) / calls * 1e3
+    rows = int(outs["out_len"].sum().item())
+    moved = 2 * 2 * L * rows * Hkv * d * kc.element_size()  # K and V, read and written
+    return {"us": us, "rows_per_sequence": rows / B, "bytes_moved": moved, "gbs": moved / (us * 1e-6) / 1e9,
+            "note": "not in the round's metric; latency-bound (a few KB per layer and sequence)"}
 
 
 def attention_source_hash() -> str:

@@ -23,7 +23,7 @@ from . import build as _build
 
 __all__ = [
     "EagleError", "Workspace", "load", "library_path", "build_tree", "tree_attention", "tree_verify",
-    "device_status", "last_launch_count", "selftest_wait_timeout", "TreeCfg", "AttnCfg", "VerifyCfg",
+    "device_status", "last_launch_count", "selftest_wait_timeout", "kv_commit", "TreeCfg", "AttnCfg", "VerifyCfg",
 ]
 
 EAGLE_OK, EAGLE_ERR_INVALID_ARG, EAGLE_ERR_UNSUPPORTED, EAGLE_ERR_CUDA, EAGLE_ERR_TIMEOUT, EAGLE_ERR_DEVICE_INPUT = range(6)
@@ -70,6 +70,8 @@ _SIGS = {
     "eagle_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "eagle_last_launch_count": (ctypes.c_int32, []),
     "eagle_selftest_wait_timeout": (ctypes.c_int32, [_P, _P, _P]),
+    "eagle_kv_commit_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnCfg)]),
+    "eagle_kv_commit": (ctypes.c_int32, [ctypes.POINTER(AttnCfg), ctypes.c_int32] + [_P] * 9 + [ctypes.c_size_t, _P]),
 }
 
 
@@ -251,6 +253,45 @@ def tree_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                                   ctypes.c_size_t(ws.nbytes), _stream(stream))
     _check(st, "eagle_tree_attention")
     return out
+
+
+def kv_commit(k_tree: torch.Tensor, v_tree: torch.Tensor, out_path: torch.Tensor, out_len: torch.Tensor,
+              ctx_len: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              new_ctx_len: torch.Tensor | None = None, ws: Workspace | None = None, stream=None) -> torch.Tensor:
+    """eagle_kv_commit: append each sequence's root and accepted path (out_path [B,D], out_len [B]
+    from tree_verify) from k/v_tree [L,B,n,Hkv,d] to k/v_cache [L,B,S_max,Hkv,d] in place at
+    positions ctx_len[b] ...; returns new_ctx_len i32 [B] = ctx_len + out_len."""
+    lib = load()
+    L, B, n, Hkv, d = k_tree.shape
+    S_max = k_cache.shape[2]
+    dt = k_tree.dtype
+    if dt not in (torch.bfloat16, torch.float32):
+        raise TypeError("K/V must be bfloat16 or float32")
+    _need(k_tree, "k_tree", dt)
+    _need(v_tree, "v_tree", dt, (L, B, n, Hkv, d))
+    _need(k_cache, "k_cache", dt, (L, B, S_max, Hkv, d))
+    _need(v_cache, "v_cache", dt, (L, B, S_max, Hkv, d))
+    _need(out_path, "out_path", torch.int32)
+    _need(out_len, "out_len", torch.int32, (B,))
+    _need(ctx_len, "ctx_len", torch.int32, (B,))
+    D = out_path.shape[1]
+    if out_path.shape != (B, D):
+        raise ValueError("out_path must be [B, D]")
+    cfg = AttnCfg(B, L, n, Hkv, Hkv, d, S_max, EAGLE_DTYPE_BF16 if dt == torch.bfloat16 else EAGLE_DTYPE_F32, 0.0)
+    if new_ctx_len is None:
+        new_ctx_len = torch.empty_like(ctx_len)
+    else:
+        _need(new_ctx_len, "new_ctx_len", torch.int32, (B,))
+    ws = ws or Workspace(device=k_tree.device)
+    need = lib.eagle_kv_commit_workspace_size(ctypes.byref(cfg))
+    if need == 0:
+        _check(EAGLE_ERR_UNSUPPORTED, "eagle_kv_commit")
+    ws.reserve(need, stream)
+    st = lib.eagle_kv_commit(ctypes.byref(cfg), D, _ptr(k_tree), _ptr(v_tree), _ptr(out_path), _ptr(out_len),
+                             _ptr(ctx_len), _ptr(k_cache), _ptr(v_cache), _ptr(new_ctx_len), ws.ptr,
+                             ctypes.c_size_t(ws.nbytes), _stream(stream))
+    _check(st, "eagle_kv_commit")
+    return new_ctx_len
 
 
 def tree_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor, tree: dict, uniforms: torch.Tensor,

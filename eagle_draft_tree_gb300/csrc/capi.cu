@@ -22,6 +22,9 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
                                 const float *uniforms, int32_t *out_tokens, int32_t *out_len, int32_t *out_path,
                                 float *out_ratio, void *ws, cudaStream_t stream);
 size_t verify_max_vocab();
+eagle_status kv_commit_launch(const eagle_attn_cfg &c, int depth, const void *k_tree, const void *v_tree,
+                              const int32_t *out_path, const int32_t *out_len, const int32_t *ctx_len,
+                              void *k_cache, void *v_cache, int32_t *new_ctx_len, void *ws, cudaStream_t stream);
 
 static thread_local int32_t t_launches = 0;
 void note_launch() { ++t_launches; }
@@ -155,6 +158,29 @@ eagle_status eagle_tree_verify(const eagle_verify_cfg *cfg, const float *target_
     if (!aligned256(ws) || ws_bytes < tree_verify_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
     return tree_verify_launch(*cfg, target_logits, draft_logits, tokens, parents, node_row, uniforms, out_tokens,
                               out_len, out_path, out_ratio, ws, stream);
+}
+
+size_t eagle_kv_commit_workspace_size(const eagle_attn_cfg *cfg) {
+    if (check_attn(cfg)) return 0;
+    return kWsHeader;
+}
+
+eagle_status eagle_kv_commit(const eagle_attn_cfg *cfg, int32_t depth, const void *k_tree, const void *v_tree,
+                             const int32_t *out_path, const int32_t *out_len, const int32_t *ctx_len, void *k_cache,
+                             void *v_cache, int32_t *new_ctx_len, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    reset_launches();
+    if (int e = check_attn(cfg)) return e;
+    if (depth < 0 || depth > 63) return EAGLE_ERR_INVALID_ARG;
+    if (cfg->layers > 65535 || cfg->batch > 65535) return EAGLE_ERR_UNSUPPORTED;
+    if (!k_tree || !v_tree || !out_path || !out_len || !ctx_len || !k_cache || !v_cache || !new_ctx_len || !ws)
+        return EAGLE_ERR_INVALID_ARG;
+    if (new_ctx_len == ctx_len) return EAGLE_ERR_INVALID_ARG;  // every CTA of a sequence reads ctx_len
+    if (!aligned256(ws) || ws_bytes < kWsHeader) return EAGLE_ERR_INVALID_ARG;
+    const uintptr_t any = reinterpret_cast<uintptr_t>(k_tree) | reinterpret_cast<uintptr_t>(v_tree) |
+                          reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
+    if (any & 15u) return EAGLE_ERR_INVALID_ARG;
+    return kv_commit_launch(*cfg, depth, k_tree, v_tree, out_path, out_len, ctx_len, k_cache, v_cache, new_ctx_len,
+                            ws, stream);
 }
 
 eagle_status eagle_workspace_init(void *ws, size_t bytes, cudaStream_t stream) {

@@ -26,6 +26,8 @@
  *                         sample only after every candidate was rejected), and the hubwiz
  *                         article's sections 1-2 (p = target, q = draft; a bonus token when every
  *                         draft token on the path is accepted; temperature applied to both).
+ *   eagle_kv_commit       appends the committed nodes' keys and values to each KV cache, which
+ *                         sets up the next round (the same pages; see the entry point below).
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers; tensors are dense row-major with the shapes given
@@ -156,6 +158,34 @@ eagle_status eagle_tree_attention(const eagle_attn_cfg *cfg, const void *q, cons
                                   const void *v_cache, const int32_t *ctx_len, const void *k_tree,
                                   const void *v_tree, const uint64_t *mask, void *out, void *ws, size_t ws_bytes,
                                   cudaStream_t stream);
+
+/* Workspace bytes needed by eagle_kv_commit (the status header only; 0 for an invalid cfg). */
+size_t eagle_kv_commit_workspace_size(const eagle_attn_cfg *cfg);
+
+/*
+ * Append each sequence's committed tree nodes to its KV cache, for every layer.  Defined by:
+ * "LLM speculative decoding explained" (hubwiz.com) sections 1 and 5 (a round commits the accepted
+ * draft tokens and one more; the tree pass computed every node's keys and values at position
+ * ctx + depth) and the EAGLE notes' section 3.3 (the accepted path).
+ *   cfg          the attention configuration of the round (B, L, n, Hkv, d, S_max, dtype).
+ *   depth        D: the width of out_path.
+ *   k_tree, v_tree  [L][B][n][Hkv][d]  the round's tree keys and values (as given to
+ *                   eagle_tree_attention).
+ *   out_path     i32 [B][D], out_len i32 [B]: as eagle_tree_verify writes them.
+ *   ctx_len      i32 [B]  context lengths of the round.
+ *   k_cache, v_cache  [L][B][S_max][Hkv][d]: sequence b gains the root (node 0) at position
+ *                   ctx_len[b], then path entries 0 .. out_len[b] - 2 at ctx_len[b] + 1 ...:
+ *                   out_len[b] rows.  The last committed token has no keys or values yet (it is
+ *                   the next round's root).  Other positions are not touched.
+ *   new_ctx_len  i32 [B]  ctx_len[b] + out_len[b] (must not alias ctx_len).
+ * Element type: cfg->dtype.  Device-side check: a sequence whose out_len exceeds D + 1, whose path
+ * holds an id outside [1, n), or whose new length exceeds S_max sets EAGLE_ERR_DEVICE_INPUT and
+ * keeps its cache and length; out_len 0 (a refused tree) is a no-op.  The K/V pointers must be
+ * 16-byte aligned.
+ */
+eagle_status eagle_kv_commit(const eagle_attn_cfg *cfg, int32_t depth, const void *k_tree, const void *v_tree,
+                             const int32_t *out_path, const int32_t *out_len, const int32_t *ctx_len, void *k_cache,
+                             void *v_cache, int32_t *new_ctx_len, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Workspace bytes needed by eagle_tree_verify. */
 size_t eagle_tree_verify_workspace_size(const eagle_verify_cfg *cfg);

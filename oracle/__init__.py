@@ -64,7 +64,9 @@ def _bind(path: str):
     lib.orc_tree_attention.argtypes = [I, I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, P, I, I, I]
     lib.orc_tree_attention_rows.argtypes = [I, I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, P, I, P, I]
     lib.orc_tree_verify.argtypes = [I, I, I, I, I, D, P, P, P, P, P, P, P, P, P, P, P, I]
-    for f in (lib.orc_build_tree, lib.orc_tree_attention, lib.orc_tree_attention_rows, lib.orc_tree_verify):
+    lib.orc_kv_commit.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
+    for f in (lib.orc_build_tree, lib.orc_tree_attention, lib.orc_tree_attention_rows, lib.orc_tree_verify,
+              lib.orc_kv_commit):
         f.restype = I
     return lib
 
@@ -118,6 +120,9 @@ class Oracle:
 
     def tree_verify(self, *a, **kw):
         return tree_verify(*a, _lib=self._lib(), **kw)
+
+    def kv_commit(self, *a, **kw):
+        return kv_commit(*a, _lib=self._lib(), **kw)
 
 
 def build_tree(draft_logits, root_token, depth: int, topk: int, keep: int, tree_temp: float = 1.0,
@@ -227,3 +232,28 @@ def tree_verify(target_logits, draft_logits, tokens, parents, node_row, uniforms
                                  _threads(nthreads))
     _check(st, "tree_verify")
     return out
+
+
+def kv_commit(k_tree, v_tree, out_path, out_len, ctx_len, k_cache, v_cache, _lib=None):
+    """Append each sequence's root and accepted path to its KV cache ([EAGLE-3 blog] sections 1
+    and 5; the reading is at ``orc_kv_commit`` in the C file).
+
+    k_tree/v_tree [L,B,n,Hkv,d] and k_cache/v_cache [L,B,S_max,Hkv,d]: float32, or uint16 holding
+    bf16 bits (the bytes are copied); out_path int32 [B,D]; out_len, ctx_len int32 [B].  The
+    input caches are not modified.  Returns (k_cache', v_cache', new_ctx_len int32 [B], ok): ok
+    is False when some sequence's commit was refused (that sequence is left as it was)."""
+    kt, vt = np.ascontiguousarray(k_tree), np.ascontiguousarray(v_tree)
+    kc, vc = np.array(k_cache, copy=True, order="C"), np.array(v_cache, copy=True, order="C")
+    assert kt.dtype == vt.dtype == kc.dtype == vc.dtype and kt.dtype in (np.float32, np.uint16)
+    L, B, n, Hkv, d = kt.shape
+    S_max = kc.shape[2]
+    assert kc.shape == (L, B, S_max, Hkv, d) and vc.shape == kc.shape and vt.shape == kt.shape
+    path = _c(out_path, np.int32).reshape(B, -1)
+    D = path.shape[1]
+    ln, ctx = _c(out_len, np.int32).reshape(B), _c(ctx_len, np.int32).reshape(B)
+    new_ctx = np.zeros(B, np.int32)
+    st = (_lib or _load()).orc_kv_commit(L, B, n, Hkv, d, S_max, D, kt.dtype.itemsize, _ptr(kt), _ptr(vt),
+                                         _ptr(path), _ptr(ln), _ptr(ctx), _ptr(kc), _ptr(vc), _ptr(new_ctx))
+    if st not in (ORC_OK, ORC_BAD_ARG):
+        _check(st, "kv_commit")
+    return kc, vc, new_ctx, st == ORC_OK

@@ -623,4 +623,52 @@ int orc_tree_verify(int B, int V, int R, int n, int max_commit, double T, const 
     return status;
 }
 
+/* ------------------------------------------------------------------------------------------ */
+/* KV commit of the accepted path                                                             */
+/* ------------------------------------------------------------------------------------------ */
+
+/* After a round the committed tokens extend each sequence ([EAGLE-3 blog] section 1: the
+ * accepted drafts and one more token; section 5: the tree pass computed every node's keys and
+ * values at position ctx + depth).  Reading: the cache gains the root (node 0, position ctx_b)
+ * and then the accepted nodes in path order (path entry i at position ctx_b + 1 + i), i.e. the
+ * out_len[b] nodes root, path[0 .. out_len[b] - 2]; the last committed token has no keys or
+ * values yet (it is the next round's root), so the new length is ctx_b + out_len[b].  A
+ * sequence with out_len 0 (nothing committed) keeps its cache and length.  A sequence whose
+ * count exceeds D + 1, whose path holds an id outside [1, n), or whose new length exceeds S_max
+ * is also left as it was, and the call returns ORC_BAD_ARG.  Copies are bytewise (esize bytes
+ * per element), one row of Hkv * d elements at a time. */
+int orc_kv_commit(int L, int B, int n, int Hkv, int d, int S_max, int D, int esize, const void *k_tree,
+                  const void *v_tree, const int32_t *out_path, const int32_t *out_len, const int32_t *ctx_len,
+                  void *k_cache, void *v_cache, int32_t *new_ctx_len)
+{
+    if (L < 1 || B < 1 || n < 1 || Hkv < 1 || d < 1 || S_max < 1 || D < 0 || (esize != 2 && esize != 4))
+        return ORC_BAD_ARG;
+    const size_t row = (size_t)Hkv * d * esize;
+    int status = ORC_OK;
+    for (int b = 0; b < B; ++b) {
+        const int ctx = ctx_len[b], len = out_len[b];
+        new_ctx_len[b] = ctx;
+        if (len == 0) continue;
+        int ok = len >= 1 && len <= D + 1 && ctx >= 0 && ctx + len <= S_max;
+        for (int i = 0; ok && i < len - 1; ++i) {
+            const int node = out_path[(size_t)b * D + i];
+            if (node < 1 || node >= n) ok = 0;
+        }
+        if (!ok) {
+            status = ORC_BAD_ARG;
+            continue;
+        }
+        for (int l = 0; l < L; ++l)
+            for (int i = 0; i < len; ++i) {
+                const int node = i == 0 ? 0 : out_path[(size_t)b * D + i - 1];
+                const size_t src = (((size_t)l * B + b) * n + node) * row;
+                const size_t dst = (((size_t)l * B + b) * S_max + ctx + i) * row;
+                memcpy((char *)k_cache + dst, (const char *)k_tree + src, row);
+                memcpy((char *)v_cache + dst, (const char *)v_tree + src, row);
+            }
+        new_ctx_len[b] = ctx + len;
+    }
+    return status;
+}
+
 int orc_version(void) { return 1; }

@@ -11,6 +11,7 @@ from scipy.stats import chisquare
 import oracle
 from tests.test_oracle_attention import _inputs, _mask_from_parents, _sdpa
 from tests.test_oracle_build import _brute_force_tree
+from tests.test_oracle_kv_commit import commit_matches_golden
 from tests.test_oracle_verify import _iid_trials, _logits
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "eagle_oracle.c")
@@ -104,6 +105,17 @@ MUTANTS = {
     # attention: a node does not see itself
     "no_self": ("if (!((mrow[j / 64] >> (j % 64)) & 1ull)) continue;\n        size_t koff",
                 "if (!((mrow[j / 64] >> (j % 64)) & 1ull) || j == i) continue;\n        size_t koff", "attention"),
+    # KV commit: the root is not appended (the path starts at position ctx)
+    "commit_skips_root": ("const int node = i == 0 ? 0 : out_path[(size_t)b * D + i - 1];",
+                          "const int node = i == len - 1 ? 0 : out_path[(size_t)b * D + i];", "commit"),
+    # KV commit: rows written one position late
+    "commit_position_shifted": ("const size_t dst = (((size_t)l * B + b) * S_max + ctx + i) * row;",
+                                "const size_t dst = (((size_t)l * B + b) * S_max + ctx + i + 1) * row;", "commit"),
+    # KV commit: the new length leaves out the root
+    "commit_length_short": ("new_ctx_len[b] = ctx + len;", "new_ctx_len[b] = ctx + len - 1;", "commit"),
+    # KV commit: keys taken from the tree's values
+    "commit_k_from_v": ("memcpy((char *)k_cache + dst, (const char *)k_tree + src, row);",
+                        "memcpy((char *)k_cache + dst, (const char *)v_tree + src, row);", "commit"),
 }
 
 
@@ -116,6 +128,8 @@ def test_pins_reject_mutant(name):
             assert _chi_square_pvalue(orc) < 1e-6
         elif part == "build":
             assert not _build_matches_brute_force(orc)
+        elif part == "commit":
+            assert not commit_matches_golden(orc)
         else:
             assert not _chain_matches_causal(orc)
 
@@ -124,3 +138,4 @@ def test_pins_accept_real_oracle():
     assert _chi_square_pvalue(oracle) > 1e-3
     assert _build_matches_brute_force(oracle)
     assert _chain_matches_causal(oracle)
+    assert commit_matches_golden(oracle)

@@ -241,6 +241,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
     # end to end: per-round inputs from pinned host memory, the three calls, results back to host
     e2e = run_e2e(eg, lib, wl, sets[0], outs, ws, stream, dev, min(K, args.e2e_steps), world)
     commit = run_kv_commit(eg, lib, wl, sets[0], outs, ws, stream, dev)
+    draft_attn = run_draft_attention(eg, lib, wl, ws, stream, dev)
 
     bytes_ = datagen.bytes_of(wl, ctx_total=float(sets[0].attn["ctx_len"].sum().item()))
     peaks = _peaks()
@@ -266,7 +267,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
                            "gbs": metric_bytes / (ms / K * 1e-3) / 1e9,
                            "frac": metric_bytes / (ms / K * 1e-3) / 1e9 / peaks["hbm_gbs"]},
         "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "mean_committed": mean_len,
-        "kv_commit": commit,
+        "kv_commit": commit, "draft_attention": draft_attn,
     }
     return res
 
@@ -387,6 +388,49 @@ def run_kv_commit(eg, lib, wl, rd: Round, outs, ws, stream, dev, calls: int = 20
     moved = 2 * 2 * L * rows * Hkv * d * kc.element_size()  # K and V, read and written
     return {"us": us, "rows_per_sequence": rows / B, "bytes_moved": moved, "gbs": moved / (us * 1e-6) / 1e9,
             "note": "not in the round's metric; latency-bound (a few KB per layer and sequence)"}
+
+
+def run_draft_attention(eg, lib, wl, ws, stream, dev, calls: int = 200) -> dict:
+    """Tree attention at the draft model's shape (not part of the round's metric): one decoder
+    layer with the workload's heads, one sequence at its context length, the tree as a draft step
+    sees it (n = 1 + k, 1 + 3k, 1 + 6k nodes).  Timed with CUDA events over `calls` launches."""
+    res = {}
+    g = torch.Generator(device=dev).manual_seed(5)
+    ctx = int(wl.ctx)
+    S = ctx + 64
+    kc = torch.randn((1, 1, S, wl.heads_kv, wl.head_dim), generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn_like(kc)
+    ctx_t = torch.tensor([ctx], dtype=torch.int32, device=dev)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    for n in (1 + wl.topk, 1 + 3 * wl.topk, 1 + 6 * wl.topk):
+        if n > 64:
+            continue
+        q = torch.randn((1, 1, n, wl.heads_q, wl.head_dim), generator=g, device=dev).to(torch.bfloat16)
+        kt = torch.randn((1, 1, n, wl.heads_kv, wl.head_dim), generator=g, device=dev).to(torch.bfloat16)
+        vt = torch.randn_like(kt)
+        mask = torch.tensor([[(1 << (i + 1)) - 1 for i in range(n)]], dtype=torch.int64, device=dev)
+        out = torch.empty_like(q)
+        cfg = eg.AttnCfg(1, 1, n, wl.heads_q, wl.heads_kv, wl.head_dim, S, eg.EAGLE_DTYPE_BF16, 0.0)
+        need = lib.eagle_tree_attention_workspace_size(ctypes.byref(cfg))
+        ws.reserve(need)
+        args = (ctypes.byref(cfg), P(q), P(kc), P(vc), P(ctx_t), P(kt), P(vt), P(mask), P(out), ws.ptr,
+                ctypes.c_size_t(ws.nbytes), ctypes.c_void_p(stream.cuda_stream))
+        for _ in range(5):
+            if lib.eagle_tree_attention(*args) != 0:
+                raise RuntimeError("eagle_tree_attention failed")
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(calls):
+            lib.eagle_tree_attention(*args)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[f"n{n}_us"] = e0.elapsed_time(e1) / calls * 1e3
+    if ws.status(stream) != 0:
+        raise RuntimeError("device status not OK after the draft-shape attention")
+    res["shape"] = f"L=1 B=1 Hq={wl.heads_q} Hkv={wl.heads_kv} d={wl.head_dim} ctx={ctx}"
+    res["note"] = "not in the round's metric; the unit's context is split over several CTAs and merged"
+    return res
 
 
 def attention_source_hash() -> str:

@@ -32,6 +32,9 @@ struct AttnTcParams {
     int32_t *status;
     int L, B, n, Hq, Hkv, G, S_max, rows, mgroups;
     float scale_log2;
+    int splits;
+    float *part_o;
+    float *part_ml;
 };
 bool tree_attention_tc_supported(int head_dim, int dtype, int G, int S_max);
 eagle_status tree_attention_tc_launch(const AttnTcParams &p, const void *q, const void *k_cache, const void *v_cache,
@@ -390,7 +393,33 @@ eagle_status launch_f32(const AttnArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
-size_t tree_attention_workspace_bytes(const eagle_attn_cfg &) { return kWsHeader; }
+// Context split of the tensor-core kernel: when the (layer, sequence, KV head, row group) units
+// fill less than half of the GPU's 152 SMs (a draft model's single layer, one sequence), each
+// unit's context tiles are shared among several CTAs whose partial results a merge kernel
+// combines exactly; the workspace then holds the partials.
+int attn_tc_splits(const eagle_attn_cfg &c) {
+    if (c.dtype != EAGLE_DTYPE_BF16 || c.head_dim != 128 || c.heads_kv < 1 || c.heads_q % c.heads_kv) return 1;
+    const long rows = long(c.heads_q / c.heads_kv) * c.nodes;
+    const long units = long(c.layers) * c.batch * c.heads_kv * ((rows + 255) / 256);
+    if (units * 2 > 152) return 1;
+    const long nctx = (long(c.max_seq) + 127) / 128;
+    long s = 152 / units;
+    if (s > nctx / 2) s = nctx / 2;  // at least two tiles a split: the partials and the merge stay small
+    if (s > 32) s = 32;
+    return s < 2 ? 1 : int(s);
+}
+
+size_t attn_tc_partial_rows(const eagle_attn_cfg &c, int splits) {
+    const long rows = long(c.heads_q / c.heads_kv) * c.nodes;
+    return size_t(c.layers) * c.batch * c.heads_kv * ((rows + 255) / 256) * splits * 256;
+}
+
+size_t tree_attention_workspace_bytes(const eagle_attn_cfg &c) {
+    const int splits = attn_tc_splits(c);
+    if (splits == 1) return kWsHeader;
+    const size_t prow = attn_tc_partial_rows(c, splits);
+    return kWsHeader + align_up(prow * 2 * sizeof(float), 256) + align_up(prow * 128 * sizeof(float), 256);
+}
 
 eagle_status tree_attention_launch(const eagle_attn_cfg &c, const void *q, const void *k_cache, const void *v_cache,
                                    const int32_t *ctx_len, const void *k_tree, const void *v_tree,
@@ -433,6 +462,15 @@ eagle_status tree_attention_launch(const eagle_attn_cfg &c, const void *q, const
             tp.rows = a.rows;
             tp.mgroups = (a.rows + 255) / 256;
             tp.scale_log2 = a.scale_log2;
+            tp.splits = attn_tc_splits(c);
+            tp.part_ml = nullptr;
+            tp.part_o = nullptr;
+            if (tp.splits > 1) {
+                unsigned char *w = static_cast<unsigned char *>(ws);
+                const size_t prow = attn_tc_partial_rows(c, tp.splits);
+                tp.part_ml = reinterpret_cast<float *>(w + kWsHeader);
+                tp.part_o = reinterpret_cast<float *>(w + kWsHeader + align_up(prow * 2 * sizeof(float), 256));
+            }
             const eagle_status st = tree_attention_tc_launch(tp, q, k_cache, v_cache, k_tree, v_tree, stream);
             if (st != EAGLE_ERR_UNSUPPORTED) return st;
         }

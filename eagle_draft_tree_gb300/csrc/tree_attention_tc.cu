@@ -47,6 +47,9 @@ struct AttnTcParams {  // same layout as the declaration in tree_attention.cu
     int32_t *status;
     int L, B, n, Hq, Hkv, G, S_max, rows, mgroups;
     float scale_log2;
+    int splits;     // context splits per unit (1: each CTA writes its rows' output itself)
+    float *part_o;  // splits > 1: [unit][split][mgroup][256 rows][128] unnormalised partial O
+    float *part_ml; // splits > 1: [unit][split][mgroup][256 rows][2] (max in base-2 units, sum)
 };
 
 namespace {
@@ -231,6 +234,9 @@ __device__ __forceinline__ void tmem_scale128(uint32_t taddr, float alpha) {
     }
 }
 
+// kSplit: the unit's context is shared among p.splits CTAs, each writing a partial result for
+// tree_attn_merge_kernel (a separate instance, so the unsplit kernel carries none of it).
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap ktmap,
@@ -244,8 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
     pdl_launch_next();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int splits = kSplit ? p.splits : 1;
     const int mg = blockIdx.x % p.mgroups;
-    const int unit = blockIdx.x / p.mgroups;
+    const int split = kSplit ? (blockIdx.x / p.mgroups) % splits : 0;
+    const int unit = blockIdx.x / (p.mgroups * splits);
     const int g = unit % p.Hkv;
     const int b = (unit / p.Hkv) % p.B;
     const int l = unit / (p.Hkv * p.B);
@@ -257,8 +265,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row0 = mg * 256;                          // first query row of this CTA
     const int tm = min(2, (p.rows - row0 + 127) / 128);  // M-tiles in this CTA (1 or 2)
     const int nctx = (ctx + kNkv - 1) / kNkv;            // context tiles
-    const int ntiles = nctx + 1;                         // + the tree tile
     const int jtail = (ctx % kNkv) ? nctx - 1 : -1;      // the ragged context tile, if any
+    // This CTA's share of the unit's tiles: context tiles [c0, c1), and the tree tile in the last
+    // split.  Stages, phases and the first-tile test count local tiles j = 0 .. ntiles - 1; the
+    // coordinates and the masking use the global tile gtile(j).
+    const int tps = kSplit ? (nctx + splits - 1) / splits : nctx;
+    const int c0 = kSplit ? min(split * tps, nctx) : 0, c1 = kSplit ? min(c0 + tps, nctx) : nctx;
+    const bool has_tree = !kSplit || split == splits - 1;
+    const int ntiles = (c1 - c0) + (has_tree ? 1 : 0);
+    auto gtile = [&](int j) { return kSplit ? (j < c1 - c0 ? c0 + j : nctx) : j; };
+    const size_t pbase = (size_t(unit * splits + split) * p.mgroups + mg) * 256;  // partial rows
+    if (kSplit && ntiles == 0) {  // a split with no tile (short context): an empty partial, uniform for the CTA
+        for (int i = tid; i < 256; i += kThreads) {
+            p.part_ml[(pbase + i) * 2] = -INFINITY;
+            p.part_ml[(pbase + i) * 2 + 1] = 0.f;
+        }
+        return;
+    }
 
     if (tid == 0) {
         s_abort = 0;
@@ -308,15 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int sk = j % kKStages, sv = j % kVStages;
                 if (j >= kKStages && !wait_or_abort(&bars.k_empty[sk], ((j / kKStages) - 1) & 1, abort_flag, p.status))
                     break;
+                const int jg = gtile(j);
                 mbar_expect_tx(&bars.k_full[sk], kTileBytes);
-                tma_kv(j == nctx ? &ktmap : &kmap, sm + kOffK + sk * kTileBytes, &bars.k_full[sk],
-                       j == nctx ? zt : zc + j * kNkv, g, pol);
+                tma_kv(jg == nctx ? &ktmap : &kmap, sm + kOffK + sk * kTileBytes, &bars.k_full[sk],
+                       jg == nctx ? zt : zc + jg * kNkv, g, pol);
                 ++k_issued;
                 if (j >= kVStages && !wait_or_abort(&bars.v_empty[sv], ((j / kVStages) - 1) & 1, abort_flag, p.status))
                     break;
                 mbar_expect_tx(&bars.v_full[sv], kTileBytes);
-                tma_kv(j == nctx ? &vtmap : &vmap, sm + kOffV + sv * kTileBytes, &bars.v_full[sv],
-                       j == nctx ? zt : zc + j * kNkv, g, pol);
+                tma_kv(jg == nctx ? &vtmap : &vmap, sm + kOffV + sv * kTileBytes, &bars.v_full[sv],
+                       jg == nctx ? zt : zc + jg * kNkv, g, pol);
                 ++v_issued;
             }
         }
@@ -355,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sv = j % kVStages, jn = j + 1;
             // V(j) landed (and cleaned, for the ragged and the tree tile), P_0(j) written
             ok = warp_wait(&bars.v_full[sv], (j / kVStages) & 1, abort_flag, p.status) &&
-                 (j != jtail || warp_wait(&bars.v_clean[0], 0, abort_flag, p.status)) &&
-                 (j != nctx || warp_wait(&bars.v_clean[1], 0, abort_flag, p.status)) &&
+                 (gtile(j) != jtail || warp_wait(&bars.v_clean[0], 0, abort_flag, p.status)) &&
+                 (gtile(j) != nctx || warp_wait(&bars.v_clean[1], 0, abort_flag, p.status)) &&
                  warp_wait(&bars.p_full[0], j & 1, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
@@ -409,8 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const bool tree = j == nctx;
-            const int kvalid = tree ? p.n : min(kNkv, ctx - j * kNkv);
+            const int jg = gtile(j);
+            const bool tree = jg == nctx;
+            const int kvalid = tree ? p.n : min(kNkv, ctx - jg * kNkv);
             float tile_sum = 0.f;
 #pragma unroll 1
             for (int q = 0; q < 2; ++q) {  // 64-key chunks
@@ -518,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // tile and of the tree tile before their PVs (P is 0 there, but 0 x NaN would not be).
             // Waiting on V(j)'s phase is safe here: that stage cannot move past tile j before the
             // PV that this warpgroup's P(j) gates.
-            if (t == 0 && (j == jtail || j == nctx)) {
+            if (t == 0 && (jg == jtail || jg == nctx)) {
                 if (!warp_wait(&bars.v_full[j % kVStages], (j / kVStages) & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
@@ -532,11 +557,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars.v_clean[j == nctx ? 1 : 0]);
+                if (lane == 0) mbar_arrive(&bars.v_clean[jg == nctx ? 1 : 0]);
             }
         }
-        // epilogue: O / l to global, bf16
-        if (ok && warp_wait(&bars.o_done[t], 0, abort_flag, p.status)) {
+        // epilogue: O / l to global, bf16; with a context split, the unnormalised partial O and the
+        // row's (max in base-2 units, sum) for the merge
+        if (kSplit && ok && warp_wait(&bars.o_done[t], 0, abort_flag, p.status)) {
+            tc_fence_after();
+            const size_t pr = pbase + t * 128 + rho;
+            float4 *po = reinterpret_cast<float4 *>(p.part_o + pr * 128);
+#pragma unroll
+            for (int cc = 0; cc < 128; cc += 16) {
+                uint32_t o[16];
+                tld16(tO + cc, o);
+                tld_wait();
+                if (valid)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        po[cc / 4 + e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                                     __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+            }
+            if (valid) {
+                p.part_ml[pr * 2] = m_raw == -INFINITY ? -INFINITY : m_raw * c;
+                p.part_ml[pr * 2 + 1] = l_sum;
+            }
+        } else if (!kSplit && ok && warp_wait(&bars.o_done[t], 0, abort_flag, p.status)) {
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
             __nv_bfloat16 *orow = p.out + ((((size_t)l * p.B + b) * p.n + node) * p.Hq + g * p.G + gh) * 128;
@@ -576,6 +621,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
     }
+}
+
+// The merge of a context split: one warp per query row, each lane four of its 128 outputs.  With
+// partial (m_s, l_s, O_s) per split (O_s = sum 2^(s c - m_s) v over the split's keys), the row's
+// output is sum_s w_s O_s / sum_s w_s l_s, w_s = 2^(m_s - max_s m_s).
+__global__ void __launch_bounds__(256) tree_attn_merge_kernel(AttnTcParams p) {
+    pdl_wait();
+    pdl_launch_next();
+    const long wid = (long(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long total = long(p.L) * p.B * p.Hkv * p.rows;
+    if (wid >= total) return;
+    const int r = int(wid % p.rows);
+    const long unit = wid / p.rows;
+    const int g = int(unit % p.Hkv), b = int((unit / p.Hkv) % p.B), l = int(unit / (long(p.Hkv) * p.B));
+    const int ctx = p.ctx_len[b];
+    if (ctx < 0 || ctx > p.S_max) return;  // flagged by the main kernel; the rows stay unwritten
+    const int mg = r / 256, rin = r % 256;
+    auto prow = [&](int s) { return ((size_t(unit) * p.splits + s) * p.mgroups + mg) * 256 + rin; };
+    // lane s < splits: split s's (max, sum), all loaded at once; the weights by warp reduction
+    float ms = -INFINITY, ls = 0.f;
+    if (lane < p.splits) {
+        const float2 v = reinterpret_cast<const float2 *>(p.part_ml)[prow(lane)];
+        ms = v.x;
+        ls = v.y;
+    }
+    float M = ms;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
+    float lsum = w * ls;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    // every split's four outputs of this lane, eight loads in flight at a time
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < p.splits; s0 += 8) {
+        float4 o[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            o[u] = s0 + u < p.splits ? reinterpret_cast<const float4 *>(p.part_o + prow(s0 + u) * 128)[lane]
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float ws = __shfl_sync(0xffffffffu, w, (s0 + u) & 31);
+            acc.x += ws * o[u].x;
+            acc.y += ws * o[u].y;
+            acc.z += ws * o[u].z;
+            acc.w += ws * o[u].w;
+        }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const int node = r / p.G, gh = r % p.G;
+    __nv_bfloat16 *orow = p.out + ((((size_t)l * p.B + b) * p.n + node) * p.Hq + g * p.G + gh) * 128;
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2 *>(orow)[lane] =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -639,16 +741,27 @@ eagle_status tree_attention_tc_launch(const AttnTcParams &p, const void *q, cons
     static bool attr = false;
     const size_t smem = kSmemBytes + 1024;
     if (!attr) {
-        if (cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(tree_attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(tree_attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
+                cudaSuccess)
             return EAGLE_ERR_CUDA;
         attr = true;
     }
-    const long grid = long(p.L) * p.B * p.Hkv * p.mgroups;
-    if (launch_pdl(tree_attn_tc_kernel, dim3(unsigned(grid)), dim3(kThreads), smem, stream, 1u, qm, km, vm, ktm, vtm, p) !=
-        cudaSuccess)
-        return EAGLE_ERR_CUDA;
+    const long grid = long(p.L) * p.B * p.Hkv * p.mgroups * p.splits;
+    const cudaError_t e = p.splits > 1 ? launch_pdl(tree_attn_tc_kernel<true>, dim3(unsigned(grid)), dim3(kThreads), smem,
+                                                    stream, 1u, qm, km, vm, ktm, vtm, p)
+                                       : launch_pdl(tree_attn_tc_kernel<false>, dim3(unsigned(grid)), dim3(kThreads),
+                                                    smem, stream, 1u, qm, km, vm, ktm, vtm, p);
+    if (e != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();
+    if (p.splits > 1) {
+        const long warps = long(p.L) * p.B * p.Hkv * p.rows;
+        if (launch_pdl(tree_attn_merge_kernel, dim3(unsigned((warps + 7) / 8)), dim3(256), 0, stream, 1u, p) !=
+            cudaSuccess)
+            return EAGLE_ERR_CUDA;
+        note_launch();
+    }
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
 

@@ -119,3 +119,11 @@ def test_binding_refuses_cpu_tensors():
     r = torch.zeros((1,), dtype=torch.int32)
     with pytest.raises((ValueError, RuntimeError, AssertionError)):
         eg.build_tree(x, r, depth=3, topk=4, keep=10, ws=object())
+
+
+def test_context_split_is_planned_only_for_small_unit_counts():
+    lib = eg.load()
+    small = eg.AttnCfg(1, 1, 61, 32, 8, 128, 2048, eg.EAGLE_DTYPE_BF16, 0.0)   # 8 units: split
+    full = eg.AttnCfg(1, 32, 61, 32, 8, 128, 2048, eg.EAGLE_DTYPE_BF16, 0.0)   # 256 units: none
+    assert lib.eagle_tree_attention_workspace_size(ctypes.byref(small)) > 256
+    assert lib.eagle_tree_attention_workspace_size(ctypes.byref(full)) == 256

@@ -242,6 +242,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
     e2e = run_e2e(eg, lib, wl, sets[0], outs, ws, stream, dev, min(K, args.e2e_steps), world)
     commit = run_kv_commit(eg, lib, wl, sets[0], outs, ws, stream, dev)
     draft_attn = run_draft_attention(eg, lib, wl, ws, stream, dev)
+    static = run_static_tree(eg, lib, wl, ws, stream, dev)
 
     bytes_ = datagen.bytes_of(wl, ctx_total=float(sets[0].attn["ctx_len"].sum().item()))
     peaks = _peaks()
@@ -267,7 +268,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
                            "gbs": metric_bytes / (ms / K * 1e-3) / 1e9,
                            "frac": metric_bytes / (ms / K * 1e-3) / 1e9 / peaks["hbm_gbs"]},
         "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "mean_committed": mean_len,
-        "kv_commit": commit, "draft_attention": draft_attn,
+        "kv_commit": commit, "draft_attention": draft_attn, "static_tree": static,
     }
     return res
 
@@ -430,6 +431,43 @@ def run_draft_attention(eg, lib, wl, ws, stream, dev, calls: int = 200) -> dict:
         raise RuntimeError("device status not OK after the draft-shape attention")
     res["shape"] = f"L=1 B=1 Hq={wl.heads_q} Hkv={wl.heads_kv} d={wl.head_dim} ctx={ctx}"
     res["note"] = "not in the round's metric; the unit's context is split over several CTAs and merged"
+    return res
+
+
+def run_static_tree(eg, lib, wl, ws, stream, dev, calls: int = 200) -> dict:
+    """eagle_build_static_tree (not part of the round's metric): the chain of the workload's depth
+    and a 21-node template (the root with 4 children, each with 4), at the workload's batch and
+    vocabulary.  Timed with CUDA events over `calls` launches."""
+    res = {}
+    B, V = wl.batch, wl.vocab
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    for name, tmpl in (("chain", eg.chain_template(wl.depth)), ("tree_4x4", [-1] + [0] * 4 + [i for i in (1, 2, 3, 4) for _ in range(4)])):
+        R = len(set(tmpl[1:]))
+        draft = datagen.draft_logits(B, R, V, 3, dev)
+        root = datagen.root_tokens(B, V, 3, dev)
+        n = len(tmpl)
+        o = {k: torch.empty((B, n), dtype=torch.int32, device=dev) for k in ("tokens", "parents", "depths", "node_row")}
+        mask = torch.empty((B, n), dtype=torch.int64, device=dev)
+        logv = torch.empty((B, n), dtype=torch.float32, device=dev)
+        cfg = eg.static_tree_cfg(B, V, tmpl, 1.0)
+        ws.reserve(lib.eagle_build_static_tree_workspace_size(ctypes.byref(cfg)))
+        args = (ctypes.byref(cfg), P(draft), P(root), P(o["tokens"]), P(o["parents"]), P(o["depths"]),
+                P(o["node_row"]), P(mask), P(logv), ws.ptr, ctypes.c_size_t(ws.nbytes),
+                ctypes.c_void_p(stream.cuda_stream))
+        for _ in range(5):
+            if lib.eagle_build_static_tree(*args) != 0:
+                raise RuntimeError("eagle_build_static_tree failed")
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(calls):
+            lib.eagle_build_static_tree(*args)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[f"{name}_n{n}_us"] = e0.elapsed_time(e1) / calls * 1e3
+    if ws.status(stream) != 0:
+        raise RuntimeError("device status not OK after the static builds")
+    res["note"] = f"not in the round's metric; B={B} V={V}, draft rows L2-warm across calls"
     return res
 
 

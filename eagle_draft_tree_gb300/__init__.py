@@ -23,7 +23,8 @@ from . import build as _build
 
 __all__ = [
     "EagleError", "Workspace", "load", "library_path", "build_tree", "tree_attention", "tree_verify",
-    "device_status", "last_launch_count", "selftest_wait_timeout", "kv_commit", "TreeCfg", "AttnCfg", "VerifyCfg",
+    "device_status", "last_launch_count", "selftest_wait_timeout", "kv_commit", "build_static_tree",
+    "StaticTreeCfg", "static_tree_cfg", "chain_template", "TreeCfg", "AttnCfg", "VerifyCfg",
 ]
 
 EAGLE_OK, EAGLE_ERR_INVALID_ARG, EAGLE_ERR_UNSUPPORTED, EAGLE_ERR_CUDA, EAGLE_ERR_TIMEOUT, EAGLE_ERR_DEVICE_INPUT = range(6)
@@ -52,6 +53,25 @@ class VerifyCfg(ctypes.Structure):
                 ("topk", ctypes.c_int32), ("keep", ctypes.c_int32), ("temperature", ctypes.c_float)]
 
 
+class StaticTreeCfg(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("vocab", ctypes.c_int32), ("nodes", ctypes.c_int32),
+                ("tree_temp", ctypes.c_float), ("parents", ctypes.c_int8 * 64)]
+
+
+def static_tree_cfg(batch: int, vocab: int, template_parents, tree_temp: float = 1.0) -> StaticTreeCfg:
+    """The C struct for a template of parent indices (parents[0] = -1, parents[i] < i)."""
+    tp = [int(x) for x in template_parents]
+    if not 1 <= len(tp) <= 64:
+        raise ValueError("a template has 1 to 64 nodes")
+    arr = (ctypes.c_int8 * 64)(*(tp + [-1] * (64 - len(tp))))
+    return StaticTreeCfg(batch, vocab, len(tp), tree_temp, arr)
+
+
+def chain_template(depth: int) -> list[int]:
+    """The chain of `depth` draft tokens below the root: parents -1, 0, 1, ..., depth - 1."""
+    return [-1] + list(range(depth))
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -71,6 +91,8 @@ _SIGS = {
     "eagle_last_launch_count": (ctypes.c_int32, []),
     "eagle_selftest_wait_timeout": (ctypes.c_int32, [_P, _P, _P]),
     "eagle_kv_commit_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnCfg)]),
+    "eagle_build_static_tree_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(StaticTreeCfg)]),
+    "eagle_build_static_tree": (ctypes.c_int32, [ctypes.POINTER(StaticTreeCfg)] + [_P] * 9 + [ctypes.c_size_t, _P]),
     "eagle_kv_commit": (ctypes.c_int32, [ctypes.POINTER(AttnCfg), ctypes.c_int32] + [_P] * 9 + [ctypes.c_size_t, _P]),
 }
 
@@ -252,6 +274,39 @@ def tree_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
                                   _ptr(k_tree), _ptr(v_tree), _ptr(mask), _ptr(out), ws.ptr,
                                   ctypes.c_size_t(ws.nbytes), _stream(stream))
     _check(st, "eagle_tree_attention")
+    return out
+
+
+def build_static_tree(draft_logits: torch.Tensor, root_token: torch.Tensor, template_parents, tree_temp: float = 1.0,
+                      ws: Workspace | None = None, out: dict | None = None, with_logv: bool = True,
+                      stream=None) -> dict:
+    """eagle_build_static_tree: a static tree (EAGLE-1) or chain from a template of parent
+    indices.  draft_logits f32 [B,R,V] (R = template nodes with children, in index order), root
+    tokens i32 [B] -> the same dict as build_tree (n = len(template_parents))."""
+    lib = load()
+    B, R, V = draft_logits.shape
+    cfg = static_tree_cfg(B, V, template_parents, tree_temp)
+    n = cfg.nodes
+    internal = len({int(p) for p in template_parents[1:]})
+    if R != internal:
+        raise ValueError(f"draft_logits must have one row per template node with children ({internal}), got {R}")
+    _need(draft_logits, "draft_logits", torch.float32)
+    _need(root_token, "root_token", torch.int32, (B,))
+    dev = draft_logits.device
+    if out is None:
+        out = {k: torch.empty((B, n), dtype=torch.int32, device=dev) for k in ("tokens", "parents", "depths", "node_row")}
+        out["mask"] = torch.empty((B, n), dtype=torch.int64, device=dev)
+        out["node_logv"] = torch.empty((B, n), dtype=torch.float32, device=dev) if with_logv else None
+    ws = ws or Workspace(device=dev)
+    need = lib.eagle_build_static_tree_workspace_size(ctypes.byref(cfg))
+    if need == 0:
+        _check(EAGLE_ERR_UNSUPPORTED, "eagle_build_static_tree")
+    ws.reserve(need, stream)
+    st = lib.eagle_build_static_tree(ctypes.byref(cfg), _ptr(draft_logits), _ptr(root_token), _ptr(out["tokens"]),
+                                     _ptr(out["parents"]), _ptr(out["depths"]), _ptr(out["node_row"]),
+                                     _ptr(out["mask"]), _ptr(out.get("node_logv")), ws.ptr, ctypes.c_size_t(ws.nbytes),
+                                     _stream(stream))
+    _check(st, "eagle_build_static_tree")
     return out
 
 

@@ -544,17 +544,106 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
 
 int kmax_for(int k) { return k <= 4 ? 4 : (k <= 8 ? 8 : 16); }
 
+// ---- static tree (EAGLE-1) and chain: a template of parent indices shared by the batch -------
+// Page: "EAGLE: Speculative Sampling Requires Rethinking Feature Uncertainty", appendix A.1 (a
+// fixed draft tree; greedy: a node's children are the top tokens of the draft distribution at
+// it) and section 4.3.1 (the chain).  The template node p with children reads draft row
+// row(p) = the number of such nodes before it; its children, in ascending index, take that row's
+// tokens of rank 0, 1, ... (value desc, ties to the lower id).  log V = the sum of the
+// log-confidences along the path.
+struct StaticArgs {
+    const int32_t *row_tok;  // [B][R][k]
+    const double *row_lc;    // [B][R][k]
+    const int32_t *root_token;
+    int32_t *tokens, *parents, *depths, *node_row;
+    uint64_t *mask;
+    float *node_logv;
+    int32_t *status;
+    int n, k, R, V;
+    int8_t tmpl[64];  // parents[i]; tmpl[0] = -1
+};
+
+__global__ void __launch_bounds__(64) static_tree_kernel(StaticArgs a) {
+    pdl_wait();
+    pdl_launch_next();
+    __shared__ int s_internal[64], s_row[64], s_tok[64];
+    __shared__ double s_lc[64];
+    const int b = blockIdx.x, i = threadIdx.x, n = a.n;
+    const int p = i < n ? a.tmpl[i] : -1;
+    bool internal = false;
+    for (int j = i + 1; j < n; ++j) internal |= a.tmpl[j] == i;
+    s_internal[i] = internal;
+    __syncthreads();
+    int row = -1;
+    if (internal) {
+        row = 0;
+        for (int j = 0; j < i; ++j) row += s_internal[j];
+    }
+    s_row[i] = row;
+    __syncthreads();
+    if (i == 0) {
+        const int32_t rt = a.root_token[b];
+        if (rt < 0 || rt >= a.V) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
+        s_tok[0] = rt;
+        s_lc[0] = 0.0;
+    } else if (i < n) {
+        int rank = 0;  // this node among its parent's children, in ascending index
+        for (int j = p + 1; j < i; ++j) rank += a.tmpl[j] == p;
+        const size_t o = (size_t(b) * a.R + s_row[p]) * a.k + rank;
+        s_tok[i] = a.row_tok[o];
+        s_lc[i] = a.row_lc[o];
+    }
+    __syncthreads();
+    if (i >= n) return;
+    double logv = 0.0;
+    uint64_t bits = 1ull;
+    int depth = 0;
+    for (int q = i; q > 0; q = a.tmpl[q]) {
+        logv += s_lc[q];
+        bits |= 1ull << q;
+        ++depth;
+    }
+    const size_t o = size_t(b) * n + i;
+    a.tokens[o] = s_tok[i];
+    a.parents[o] = p;
+    a.depths[o] = depth;
+    a.node_row[o] = s_row[i];
+    a.mask[o] = bits;
+    if (a.node_logv) a.node_logv[o] = float(logv);
+}
+
 // One wave of CTAs: rows are split over a cluster only while the grid stays within the SM count
 // (each CTA streams its slice with loads of the next batch in flight).
-int splits_for(const eagle_tree_cfg &c) {
-    const int R = 1 + (c.depth - 1) * c.topk;
-    const long rows = long(c.batch) * R;
+int splits_for_rows(long rows, int vocab) {
     long sp = 152 / rows;
     const long per = long(kRowThreads) * kRowVals;
-    const long useful = (c.vocab + per - 1) / per;  // no empty CTAs
+    const long useful = (vocab + per - 1) / per;  // no empty CTAs
     if (sp > useful) sp = useful;
     if (sp > kMaxSplits) sp = kMaxSplits;
     return sp < 1 ? 1 : int(sp);
+}
+
+// a1 over R rows of B sequences: each row's k children (token, fp64 log-confidence at tree_temp)
+eagle_status row_topk_launch(const float *draft, int B, int R, int V, int k, float tree_temp, int32_t *row_tok,
+                             double *row_lc, cudaStream_t stream) {
+    const int splits = splits_for_rows(long(B) * R, V);
+    int chunk = (V + splits - 1) / splits;
+    chunk = (chunk + 3) & ~3;
+    RowArgs ra;
+    ra.x = draft;
+    ra.row_tok = row_tok;
+    ra.row_lc = row_lc;
+    ra.V = V;
+    ra.R = R;
+    ra.k = k;
+    ra.chunk = chunk;
+    ra.c = kLog2e / tree_temp;
+    ra.inv_t = 1.0 / double(tree_temp);
+    if (launch_pdl(row_topk_kernel, dim3(splits, R, B), dim3(kRowThreads), 0, stream, unsigned(splits), ra) !=
+        cudaSuccess)
+        return EAGLE_ERR_CUDA;
+    note_launch();
+    return EAGLE_OK;
 }
 
 template <int KMAX>
@@ -562,28 +651,14 @@ eagle_status launch_build(const eagle_tree_cfg &c, const float *draft, const int
                           int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv,
                           unsigned char *ws, cudaStream_t stream) {
     const int R = 1 + (c.depth - 1) * c.topk;
-    const int splits = splits_for(c);
-    int chunk = (c.vocab + splits - 1) / splits;
-    chunk = (chunk + 3) & ~3;
-    RowArgs ra;
-    ra.x = draft;
-    ra.row_tok = reinterpret_cast<int32_t *>(ws + kWsHeader);
-    ra.row_lc = reinterpret_cast<double *>(ws + kWsHeader + align_up(size_t(c.batch) * R * c.topk * 4, 256));
-    ra.V = c.vocab;
-    ra.R = R;
-    ra.k = c.topk;
-    ra.chunk = chunk;
-    ra.c = kLog2e / c.tree_temp;
-    ra.inv_t = 1.0 / double(c.tree_temp);
-
-    if (launch_pdl(row_topk_kernel, dim3(splits, R, c.batch), dim3(kRowThreads), 0, stream, unsigned(splits), ra) !=
-        cudaSuccess)
-        return EAGLE_ERR_CUDA;
-    note_launch();
+    int32_t *row_tok = reinterpret_cast<int32_t *>(ws + kWsHeader);
+    double *row_lc = reinterpret_cast<double *>(ws + kWsHeader + align_up(size_t(c.batch) * R * c.topk * 4, 256));
+    if (eagle_status e = row_topk_launch(draft, c.batch, R, c.vocab, c.topk, c.tree_temp, row_tok, row_lc, stream))
+        return e;
 
     SelectArgs sa;
-    sa.row_tok = ra.row_tok;
-    sa.row_lc = ra.row_lc;
+    sa.row_tok = row_tok;
+    sa.row_lc = row_lc;
     sa.root_token = root;
     sa.tokens = tokens;
     sa.parents = parents;
@@ -604,6 +679,43 @@ eagle_status launch_build(const eagle_tree_cfg &c, const float *draft, const int
 }
 
 }  // namespace
+
+size_t static_tree_workspace_bytes(const eagle_static_tree_cfg &c, int R, int k) {
+    const size_t ent = size_t(c.batch) * (R > 0 ? R : 1) * (k > 0 ? k : 1);
+    return kWsHeader + align_up(ent * 4, 256) + align_up(ent * 8, 256);
+}
+
+eagle_status build_static_tree_launch(const eagle_static_tree_cfg &c, int R, int k, const float *draft,
+                                      const int32_t *root, int32_t *tokens, int32_t *parents, int32_t *depths,
+                                      int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
+                                      cudaStream_t stream) {
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    const size_t ent = size_t(c.batch) * (R > 0 ? R : 1) * (k > 0 ? k : 1);
+    StaticArgs a;
+    a.row_tok = reinterpret_cast<int32_t *>(w + kWsHeader);
+    a.row_lc = reinterpret_cast<double *>(w + kWsHeader + align_up(ent * 4, 256));
+    if (R > 0) {
+        if (eagle_status e = row_topk_launch(draft, c.batch, R, c.vocab, k, c.tree_temp, const_cast<int32_t *>(a.row_tok),
+                                             const_cast<double *>(a.row_lc), stream))
+            return e;
+    }
+    a.root_token = root;
+    a.tokens = tokens;
+    a.parents = parents;
+    a.depths = depths;
+    a.node_row = node_row;
+    a.mask = mask;
+    a.node_logv = node_logv;
+    a.status = reinterpret_cast<int32_t *>(w);
+    a.n = c.nodes;
+    a.k = k > 0 ? k : 1;
+    a.R = R > 0 ? R : 1;
+    a.V = c.vocab;
+    for (int i = 0; i < 64; ++i) a.tmpl[i] = i < c.nodes ? c.parents[i] : int8_t(-1);
+    if (launch_pdl(static_tree_kernel, dim3(c.batch), dim3(64), 0, stream, 1u, a) != cudaSuccess) return EAGLE_ERR_CUDA;
+    note_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
+}
 
 size_t build_tree_workspace_bytes(const eagle_tree_cfg &c) {
     const int R = 1 + (c.depth - 1) * c.topk;

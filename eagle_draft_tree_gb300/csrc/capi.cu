@@ -22,6 +22,11 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
                                 const float *uniforms, int32_t *out_tokens, int32_t *out_len, int32_t *out_path,
                                 float *out_ratio, void *ws, cudaStream_t stream);
 size_t verify_max_vocab();
+size_t static_tree_workspace_bytes(const eagle_static_tree_cfg &c, int R, int k);
+eagle_status build_static_tree_launch(const eagle_static_tree_cfg &c, int R, int k, const float *draft,
+                                      const int32_t *root, int32_t *tokens, int32_t *parents, int32_t *depths,
+                                      int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
+                                      cudaStream_t stream);
 eagle_status kv_commit_launch(const eagle_attn_cfg &c, int depth, const void *k_tree, const void *v_tree,
                               const int32_t *out_path, const int32_t *out_len, const int32_t *ctx_len,
                               void *k_cache, void *v_cache, int32_t *new_ctx_len, void *ws, cudaStream_t stream);
@@ -62,6 +67,29 @@ int check_attn(const eagle_attn_cfg *c) {
     const long rows = long(c->heads_q / c->heads_kv) * c->nodes;
     const long grid = long(c->layers) * c->batch * c->heads_kv * ((rows + 63) / 64);
     if (grid > 0x7fffffffL) return EAGLE_ERR_UNSUPPORTED;
+    return 0;
+}
+
+// 0 = ok, else an eagle status; R = template nodes with children, k = most children of one node
+int check_static(const eagle_static_tree_cfg *c, int *R, int *k) {
+    if (!c) return EAGLE_ERR_INVALID_ARG;
+    if (c->batch < 1 || c->vocab < 1 || c->nodes < 1 || !(c->tree_temp > 0.f)) return EAGLE_ERR_INVALID_ARG;
+    if (c->nodes > 64) return EAGLE_ERR_UNSUPPORTED;
+    if (c->batch > 65535) return EAGLE_ERR_UNSUPPORTED;
+    if (c->parents[0] != -1) return EAGLE_ERR_INVALID_ARG;
+    int kids[64] = {0};
+    for (int i = 1; i < c->nodes; ++i) {
+        if (c->parents[i] < 0 || c->parents[i] >= i) return EAGLE_ERR_INVALID_ARG;
+        ++kids[c->parents[i]];
+    }
+    int r = 0, km = 0;
+    for (int i = 0; i < c->nodes; ++i) {
+        r += kids[i] > 0;
+        km = kids[i] > km ? kids[i] : km;
+    }
+    if (km > 16 || km > c->vocab) return EAGLE_ERR_UNSUPPORTED;
+    *R = r;
+    *k = km;
     return 0;
 }
 
@@ -158,6 +186,26 @@ eagle_status eagle_tree_verify(const eagle_verify_cfg *cfg, const float *target_
     if (!aligned256(ws) || ws_bytes < tree_verify_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
     return tree_verify_launch(*cfg, target_logits, draft_logits, tokens, parents, node_row, uniforms, out_tokens,
                               out_len, out_path, out_ratio, ws, stream);
+}
+
+size_t eagle_build_static_tree_workspace_size(const eagle_static_tree_cfg *cfg) {
+    int R = 0, k = 0;
+    if (check_static(cfg, &R, &k)) return 0;
+    return static_tree_workspace_bytes(*cfg, R, k);
+}
+
+eagle_status eagle_build_static_tree(const eagle_static_tree_cfg *cfg, const float *draft_logits,
+                                     const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
+                                     int32_t *node_row, uint64_t *mask, float *node_logv, void *ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+    reset_launches();
+    int R = 0, k = 0;
+    if (int e = check_static(cfg, &R, &k)) return e;
+    if ((R > 0 && !draft_logits) || !root_token || !tokens || !parents || !depths || !node_row || !mask || !ws)
+        return EAGLE_ERR_INVALID_ARG;
+    if (!aligned256(ws) || ws_bytes < static_tree_workspace_bytes(*cfg, R, k)) return EAGLE_ERR_INVALID_ARG;
+    return build_static_tree_launch(*cfg, R, k, draft_logits, root_token, tokens, parents, depths, node_row, mask,
+                                    node_logv, ws, stream);
 }
 
 size_t eagle_kv_commit_workspace_size(const eagle_attn_cfg *cfg) {

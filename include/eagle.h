@@ -12,6 +12,8 @@
  *                         tokens" (global top-m by value, shallower first on ties; the kept set
  *                         stays a connected tree) and "Tree Attention Mask" (flatten to one
  *                         sequence; a token sees only its ancestors).
+ *   eagle_build_static_tree  a static draft tree (EAGLE-1) or a chain from a caller's template:
+ *                         the same outputs as eagle_build_tree (see the entry point below).
  *   eagle_tree_attention  tree-masked grouped-query attention of the flattened tree against the
  *                         cached context, for every layer.  Defined by: "LLM speculative decoding
  *                         explained" (hubwiz.com), section 5 (the flattened tree is scored in one
@@ -107,6 +109,15 @@ typedef struct {
     float temperature; /* T > 0: speculative sampling at T;  T == 0: greedy     */
 } eagle_verify_cfg;
 
+/* A static draft tree (EAGLE-1) or chain: one template of parent indices for every sequence. */
+typedef struct {
+    int32_t batch;      /* B                                                         */
+    int32_t vocab;      /* V                                                         */
+    int32_t nodes;      /* n <= 64 template nodes; node 0 is the root                */
+    float tree_temp;    /* temperature of the draft confidences (log V), > 0         */
+    int8_t parents[64]; /* parents[0] = -1, parents[i] in [0, i) for 1 <= i < n      */
+} eagle_static_tree_cfg;
+
 /* ---------------------------------------------------------------------------------------- */
 
 /* Workspace bytes needed by eagle_build_tree for this configuration (0 if the config is
@@ -134,6 +145,32 @@ size_t eagle_build_tree_workspace_size(const eagle_tree_cfg *cfg);
 eagle_status eagle_build_tree(const eagle_tree_cfg *cfg, const float *draft_logits, const int32_t *root_token,
                               int32_t *tokens, int32_t *parents, int32_t *depths, int32_t *node_row,
                               uint64_t *mask, float *node_logv, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes needed by eagle_build_static_tree (0 for an invalid or unsupported cfg). */
+size_t eagle_build_static_tree_workspace_size(const eagle_static_tree_cfg *cfg);
+
+/*
+ * A static draft tree or a chain, as EAGLE-1 drafts them.  Defined by: "EAGLE: Speculative
+ * Sampling Requires Rethinking Feature Uncertainty" (papercache.org), appendix A.1 (a fixed tree;
+ * in the greedy setting a node's children are the top tokens of the draft distribution at it)
+ * and section 4.3.1 (the chain: one child per node).  The pages draw the tree only as a figure,
+ * so its shape is the caller's template (cfg->parents).
+ *   draft_logits f32 [B][R][V]  R = the number of template nodes with children; row r of a
+ *                               sequence belongs to the r-th such node in ascending index.
+ *   root_token   i32 [B]
+ * Outputs as eagle_build_tree (n = cfg->nodes): a node's children, in ascending index, take its
+ * row's tokens of rank 0, 1, ... (value desc, ties to the lower token id); node_row[i] is node
+ * i's own row or -1; node_logv[i] is the sum of log-confidences x/T - logsumexp(x/T) along the
+ * path; masks are ancestor-or-self bits.  A chain of depth D is the template
+ * parents = {-1, 0, 1, ..., D - 1}.
+ * Host-side checks: the template (parents[0] = -1, parents[i] in [0, i)), n <= 64, at most 16
+ * children per node and at most V.  Device-side: a root token outside [0, V) sets
+ * EAGLE_ERR_DEVICE_INPUT.
+ */
+eagle_status eagle_build_static_tree(const eagle_static_tree_cfg *cfg, const float *draft_logits,
+                                     const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
+                                     int32_t *node_row, uint64_t *mask, float *node_logv, void *ws, size_t ws_bytes,
+                                     cudaStream_t stream);
 
 /* Workspace bytes needed by eagle_tree_attention. */
 size_t eagle_tree_attention_workspace_size(const eagle_attn_cfg *cfg);

@@ -65,8 +65,9 @@ def _bind(path: str):
     lib.orc_tree_attention_rows.argtypes = [I, I, I, I, I, I, I, I, D, P, P, P, P, P, P, P, P, I, P, I]
     lib.orc_tree_verify.argtypes = [I, I, I, I, I, D, P, P, P, P, P, P, P, P, P, P, P, I]
     lib.orc_kv_commit.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
+    lib.orc_build_static_tree.argtypes = [I, I, I, P, D, P, P, P, P, P, P, P, P]
     for f in (lib.orc_build_tree, lib.orc_tree_attention, lib.orc_tree_attention_rows, lib.orc_tree_verify,
-              lib.orc_kv_commit):
+              lib.orc_kv_commit, lib.orc_build_static_tree):
         f.restype = I
     return lib
 
@@ -123,6 +124,9 @@ class Oracle:
 
     def kv_commit(self, *a, **kw):
         return kv_commit(*a, _lib=self._lib(), **kw)
+
+    def build_static_tree(self, *a, **kw):
+        return build_static_tree(*a, _lib=self._lib(), **kw)
 
 
 def build_tree(draft_logits, root_token, depth: int, topk: int, keep: int, tree_temp: float = 1.0,
@@ -257,3 +261,26 @@ def kv_commit(k_tree, v_tree, out_path, out_len, ctx_len, k_cache, v_cache, _lib
     if st not in (ORC_OK, ORC_BAD_ARG):
         _check(st, "kv_commit")
     return kc, vc, new_ctx, st == ORC_OK
+
+
+def build_static_tree(draft_logits, root_token, template_parents, tree_temp: float = 1.0, _lib=None):
+    """Static tree or chain from a template ([EAGLE-1 notes] A.1, 4.3.1; the reading is at
+    ``orc_build_static_tree`` in the C file).  draft_logits float32 [B, R, V] with R = the template
+    nodes that have children; root_token int32 [B].  Returns tokens/parents/depths/node_row int32
+    [B, n], mask uint64 [B, n, 1], node_logv float64 [B, n]."""
+    x = _c(draft_logits, np.float32)
+    B, R, V = x.shape
+    tmpl = np.ascontiguousarray(template_parents, np.int32)
+    n = tmpl.shape[0]
+    root = _c(root_token, np.int32).reshape(B)
+    out = {k: np.zeros((B, n), np.int32) for k in ("tokens", "parents", "depths", "node_row")}
+    out["mask"] = np.zeros((B, n, 1), np.uint64)
+    out["node_logv"] = np.zeros((B, n), np.float64)
+    internal = len(set(int(p) for p in tmpl[1:]))
+    if R != internal:
+        raise OracleError(f"build_static_tree: {R} draft rows for {internal} template nodes with children")
+    st = (_lib or _load()).orc_build_static_tree(B, V, n, _ptr(tmpl), float(tree_temp), _ptr(x), _ptr(root),
+                                                 _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["depths"]),
+                                                 _ptr(out["node_row"]), _ptr(out["mask"]), _ptr(out["node_logv"]))
+    _check(st, "build_static_tree")
+    return out

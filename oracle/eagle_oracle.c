@@ -624,6 +624,66 @@ int orc_tree_verify(int B, int V, int R, int n, int max_commit, double T, const 
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* Static tree and chain  ([EAGLE-1 notes] appendix A.1, section 4.3.1)                        */
+/* ------------------------------------------------------------------------------------------ */
+
+/* EAGLE-1 drafts a fixed tree: in the greedy setting a node's children are the top tokens of the
+ * draft distribution at that node (appendix A.1); the chain of section 4.3.1 has one child per
+ * node.  The tree is drawn only as a figure, so it is a template here (reading): tmpl[0] = -1,
+ * tmpl[i] in [0, i).  The template nodes with children own the draft rows, in ascending index
+ * (row r = the r-th such node); node p's children, in ascending index, take ranks 0, 1, ... of
+ * its row's tokens under (value desc, id asc).  log V of a node is the sum of the
+ * log-confidences (x/T - logsumexp(x/T) of the row) along its path; the root has 0. */
+int orc_build_static_tree(int B, int V, int n, const int32_t *tmpl, double tree_temp, const float *draft,
+                          const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
+                          int32_t *node_row, uint64_t *mask, double *node_logv)
+{
+    if (B < 1 || V < 1 || n < 1 || n > 64 || !(tree_temp > 0.0) || tmpl[0] != -1) return ORC_BAD_ARG;
+    int kids[64] = {0}, row_of[64];
+    for (int i = 1; i < n; ++i) {
+        if (tmpl[i] < 0 || tmpl[i] >= i) return ORC_BAD_ARG;
+        ++kids[tmpl[i]];
+    }
+    int R = 0;
+    for (int i = 0; i < n; ++i) {
+        if (kids[i] > V) return ORC_BAD_ARG;
+        row_of[i] = kids[i] > 0 ? R++ : -1;
+    }
+    int top[64][64];
+    double lse[64];
+    for (int b = 0; b < B; ++b) {
+        for (int p = 0; p < n; ++p)
+            if (row_of[p] >= 0) {
+                const float *row = draft + ((size_t)b * R + row_of[p]) * V;
+                lse[p] = row_logsumexp(row, V, tree_temp);
+                row_topk(row, V, kids[p], top[p]);
+            }
+        int32_t *tok = tokens + (size_t)b * n, *par = parents + (size_t)b * n, *dep = depths + (size_t)b * n;
+        int32_t *nr = node_row + (size_t)b * n;
+        uint64_t *mk = mask + (size_t)b * n;
+        double *lv = node_logv + (size_t)b * n;
+        tok[0] = root_token[b];
+        par[0] = -1;
+        dep[0] = 0;
+        lv[0] = 0.0;
+        mk[0] = 1ull;
+        for (int i = 0; i < n; ++i) nr[i] = row_of[i];
+        for (int i = 1; i < n; ++i) {  /* parents come first, so their values are already set */
+            const int p = tmpl[i];
+            int rank = 0;
+            for (int j = p + 1; j < i; ++j) rank += tmpl[j] == p;
+            const float *row = draft + ((size_t)b * R + row_of[p]) * V;
+            tok[i] = top[p][rank];
+            par[i] = p;
+            dep[i] = dep[p] + 1;
+            lv[i] = lv[p] + ((double)row[tok[i]] / tree_temp - lse[p]);
+            mk[i] = mk[p] | (1ull << i);
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* KV commit of the accepted path                                                             */
 /* ------------------------------------------------------------------------------------------ */
 

@@ -127,3 +127,20 @@ def test_context_split_is_planned_only_for_small_unit_counts():
     full = eg.AttnCfg(1, 32, 61, 32, 8, 128, 2048, eg.EAGLE_DTYPE_BF16, 0.0)   # 256 units: none
     assert lib.eagle_tree_attention_workspace_size(ctypes.byref(small)) > 256
     assert lib.eagle_tree_attention_workspace_size(ctypes.byref(full)) == 256
+
+
+@pytest.mark.parametrize("parents,code", [
+    ([-1, 0, 0, 1], None),
+    ([0, 0], eg.EAGLE_ERR_INVALID_ARG),           # the root has a parent
+    ([-1, 0, 3, 1], eg.EAGLE_ERR_INVALID_ARG),    # a parent after its child
+    ([-1] + [0] * 17, eg.EAGLE_ERR_UNSUPPORTED),  # 17 children of one node
+])
+def test_static_tree_host_validation(parents, code):
+    lib = eg.load()
+    cfg = eg.static_tree_cfg(2, 1000, parents, 1.0)
+    size = lib.eagle_build_static_tree_workspace_size(ctypes.byref(cfg))
+    st = lib.eagle_build_static_tree(ctypes.byref(cfg), *([None] * 9), 0, None)
+    if code is None:
+        assert size >= 256 and st == eg.EAGLE_ERR_INVALID_ARG  # valid template, null buffers
+    else:
+        assert size == 0 and st == code

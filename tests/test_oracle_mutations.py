@@ -12,6 +12,7 @@ import oracle
 from tests.test_oracle_attention import _inputs, _mask_from_parents, _sdpa
 from tests.test_oracle_build import _brute_force_tree
 from tests.test_oracle_kv_commit import commit_matches_golden
+from tests.test_oracle_static_tree import static_invariants_hold, static_matches_golden
 from tests.test_oracle_verify import _iid_trials, _logits
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "eagle_oracle.c")
@@ -105,6 +106,15 @@ MUTANTS = {
     # attention: a node does not see itself
     "no_self": ("if (!((mrow[j / 64] >> (j % 64)) & 1ull)) continue;\n        size_t koff",
                 "if (!((mrow[j / 64] >> (j % 64)) & 1ull) || j == i) continue;\n        size_t koff", "attention"),
+    # static tree: siblings take the ranks in reverse order
+    "static_rank_reversed": ("tok[i] = top[p][rank];", "tok[i] = top[p][kids[p] - 1 - rank];", "static"),
+    # static tree: a child reads its own row instead of its parent's
+    "static_own_row": ("const float *row = draft + ((size_t)b * R + row_of[p]) * V;\n            tok[i]",
+                       "const float *row = draft + ((size_t)b * R + (row_of[i] >= 0 ? row_of[i] : row_of[p])) * V;\n            tok[i]",
+                       "static"),
+    # static tree: log V not cumulative along the path
+    "static_value_not_cumulative": ("lv[i] = lv[p] + ((double)row[tok[i]] / tree_temp - lse[p]);",
+                                    "lv[i] = ((double)row[tok[i]] / tree_temp - lse[p]);", "static"),
     # KV commit: the root is not appended (the path starts at position ctx)
     "commit_skips_root": ("const int node = i == 0 ? 0 : out_path[(size_t)b * D + i - 1];",
                           "const int node = i == len - 1 ? 0 : out_path[(size_t)b * D + i];", "commit"),
@@ -130,6 +140,8 @@ def test_pins_reject_mutant(name):
             assert not _build_matches_brute_force(orc)
         elif part == "commit":
             assert not commit_matches_golden(orc)
+        elif part == "static":
+            assert not (static_matches_golden(orc) and static_invariants_hold(orc))
         else:
             assert not _chain_matches_causal(orc)
 
@@ -139,3 +151,4 @@ def test_pins_accept_real_oracle():
     assert _build_matches_brute_force(oracle)
     assert _chain_matches_causal(oracle)
     assert commit_matches_golden(oracle)
+    assert static_matches_golden(oracle) and static_invariants_hold(oracle)

@@ -66,8 +66,10 @@ def _bind(path: str):
     lib.orc_tree_verify.argtypes = [I, I, I, I, I, D, P, P, P, P, P, P, P, P, P, P, P, I]
     lib.orc_kv_commit.argtypes = [I, I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
     lib.orc_build_static_tree.argtypes = [I, I, I, P, D, P, P, P, P, P, P, P, P]
+    lib.orc_build_tree_ex.argtypes = [I, I, I, I, I, D, P, P, P, P, P, P, P, P, P, P, P, P, P, I]
+    lib.orc_build_static_tree_ex.argtypes = [I, I, I, P, D, P, P, P, P, P, P, P, P, P, P]
     for f in (lib.orc_build_tree, lib.orc_tree_attention, lib.orc_tree_attention_rows, lib.orc_tree_verify,
-              lib.orc_kv_commit, lib.orc_build_static_tree):
+              lib.orc_kv_commit, lib.orc_build_static_tree, lib.orc_build_tree_ex, lib.orc_build_static_tree_ex):
         f.restype = I
     return lib
 
@@ -130,29 +132,44 @@ class Oracle:
 
 
 def build_tree(draft_logits, root_token, depth: int, topk: int, keep: int, tree_temp: float = 1.0,
-               nthreads: int | None = None, _lib=None):
+               nthreads: int | None = None, child_u=None, frontier: bool = False, _lib=None):
     """EAGLE-2 dynamic draft tree ([EAGLE-2 notes] Expanding / Rerank / Tree Attention Mask).
 
     draft_logits: float32 [B, R, V], R = 1 + (depth-1)*topk.  root_token: int32 [B].
+    child_u: None for top-k children (greedy), else float32 [B, R, topk] uniforms: the children of
+    row r are topk inverse-CDF draws from softmax(x_r / tree_temp) ([EAGLE-1 notes] A.1,
+    non-greedy), in draw order.
     Returns dict of tokens/parents/depths/node_row int32 [B, n], mask uint64 [B, n, W],
-    node_logv float64 [B, n], margin float64 [B] (smallest relative key gap at a selection).
+    node_logv float64 [B, n], margin float64 [B] (smallest relative key gap at a selection),
+    draw_gap float64 [B] (smallest distance of a uniform to the CDF step deciding its draw; inf
+    without draws) and, with ``frontier``, front_tok/front_par int32 [B, depth-1, topk]: the
+    frontier of depths 1..depth-1 in slot order and each node's parent slot (-1 at depth 1).
     """
     x = _c(draft_logits, np.float32)
     B, R, V = x.shape
     assert R == 1 + (depth - 1) * topk, "draft rows must be 1 + (D-1)k"
     root = _c(root_token, np.int32).reshape(B)
+    u = None if child_u is None else _c(child_u, np.float32).reshape(B, R, topk)
     n = keep + 1
     W = (n + 63) // 64
     out = dict(
         tokens=np.zeros((B, n), np.int32), parents=np.zeros((B, n), np.int32),
         depths=np.zeros((B, n), np.int32), node_row=np.zeros((B, n), np.int32),
         mask=np.zeros((B, n, W), np.uint64), node_logv=np.zeros((B, n), np.float64),
-        margin=np.zeros(B, np.float64))
-    st = (_lib or _load()).orc_build_tree(B, V, depth, topk, keep, float(tree_temp), _ptr(x), _ptr(root),
-                                _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["depths"]),
-                                _ptr(out["node_row"]), _ptr(out["mask"]), _ptr(out["node_logv"]),
-                                _ptr(out["margin"]), _threads(nthreads))
+        margin=np.zeros(B, np.float64), draw_gap=np.zeros(B, np.float64))
+    ft = fp = None
+    if frontier:
+        ft = np.zeros((B, max(depth - 1, 1), topk), np.int32)
+        fp = np.zeros_like(ft)
+    st = (_lib or _load()).orc_build_tree_ex(B, V, depth, topk, keep, float(tree_temp), _ptr(x), _ptr(u),
+                                             _ptr(root), _ptr(out["tokens"]), _ptr(out["parents"]),
+                                             _ptr(out["depths"]), _ptr(out["node_row"]), _ptr(out["mask"]),
+                                             _ptr(out["node_logv"]), _ptr(out["margin"]), _ptr(out["draw_gap"]),
+                                             _ptr(ft), _ptr(fp), _threads(nthreads))
     _check(st, "build_tree")
+    if frontier:
+        out["front_tok"] = ft[:, :depth - 1]
+        out["front_par"] = fp[:, :depth - 1]
     return out
 
 
@@ -263,11 +280,14 @@ def kv_commit(k_tree, v_tree, out_path, out_len, ctx_len, k_cache, v_cache, _lib
     return kc, vc, new_ctx, st == ORC_OK
 
 
-def build_static_tree(draft_logits, root_token, template_parents, tree_temp: float = 1.0, _lib=None):
+def build_static_tree(draft_logits, root_token, template_parents, tree_temp: float = 1.0, child_u=None,
+                      _lib=None):
     """Static tree or chain from a template ([EAGLE-1 notes] A.1, 4.3.1; the reading is at
     ``orc_build_static_tree`` in the C file).  draft_logits float32 [B, R, V] with R = the template
-    nodes that have children; root_token int32 [B].  Returns tokens/parents/depths/node_row int32
-    [B, n], mask uint64 [B, n, 1], node_logv float64 [B, n]."""
+    nodes that have children; root_token int32 [B].  child_u: None (top-k children) or float32
+    [B, R, kmax] uniforms, kmax = the most children of one template node (sampled children,
+    [EAGLE-1 notes] A.1 non-greedy).  Returns tokens/parents/depths/node_row int32 [B, n], mask
+    uint64 [B, n, 1], node_logv float64 [B, n], draw_gap float64 [B]."""
     x = _c(draft_logits, np.float32)
     B, R, V = x.shape
     tmpl = np.ascontiguousarray(template_parents, np.int32)
@@ -276,11 +296,17 @@ def build_static_tree(draft_logits, root_token, template_parents, tree_temp: flo
     out = {k: np.zeros((B, n), np.int32) for k in ("tokens", "parents", "depths", "node_row")}
     out["mask"] = np.zeros((B, n, 1), np.uint64)
     out["node_logv"] = np.zeros((B, n), np.float64)
+    out["draw_gap"] = np.zeros(B, np.float64)
     internal = len(set(int(p) for p in tmpl[1:]))
     if R != internal:
         raise OracleError(f"build_static_tree: {R} draft rows for {internal} template nodes with children")
-    st = (_lib or _load()).orc_build_static_tree(B, V, n, _ptr(tmpl), float(tree_temp), _ptr(x), _ptr(root),
-                                                 _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["depths"]),
-                                                 _ptr(out["node_row"]), _ptr(out["mask"]), _ptr(out["node_logv"]))
+    u = None
+    if child_u is not None:
+        kmax = int(np.bincount(tmpl[1:], minlength=n).max()) if n > 1 else 1
+        u = _c(child_u, np.float32).reshape(B, R, kmax)
+    st = (_lib or _load()).orc_build_static_tree_ex(B, V, n, _ptr(tmpl), float(tree_temp), _ptr(x), _ptr(u),
+                                                    _ptr(root), _ptr(out["tokens"]), _ptr(out["parents"]),
+                                                    _ptr(out["depths"]), _ptr(out["node_row"]), _ptr(out["mask"]),
+                                                    _ptr(out["node_logv"]), _ptr(out["draw_gap"]))
     _check(st, "build_static_tree")
     return out

@@ -26,7 +26,9 @@
  * Readings where the pages are silent (the same list is kept in the design notes):
  *   - V_i is compared in log space: log V_i = sum of log-confidences (equal to the product).
  *   - Confidence = the draft row's softmax at the tree temperature (1 by default).
- *   - Children of a row = its k largest logits, ties to the lower token id.
+ *   - Children of a row = its k largest logits, ties to the lower token id (greedy).  When
+ *     sampling ([EAGLE-1 notes] appendix A.1, non-greedy): k independent inverse-CDF draws from
+ *     the row's q = softmax(x/T), with replacement, one caller uniform per draw, in draw order.
  *   - Frontier at depth f (1..D-1) = the k depth-f nodes of largest (log V desc, creation asc);
  *     frontier slot s is expanded with draft row 1 + (f-1)k + s.  Row 0 expands the root.
  *   - Creation index: depth-1 children 0..k-1 in child-rank order, then per depth, per frontier
@@ -101,6 +103,36 @@ static int row_argmax(const float *x, int V)
     return best;
 }
 
+static int inverse_cdf(const double *p, int V, double u, double *gap);
+
+/* The children of one draft row in the non-greedy setting ([EAGLE-1 notes] appendix A.1: k
+ * tokens are sampled instead of the top k).  Reading: k independent draws from the row's draft
+ * distribution q = softmax(x/T), with replacement (a token may be drawn twice), draw j by
+ * inverse CDF over ascending token id with the caller's uniform u[j]; the children keep draw
+ * order.  q_buf: V doubles of scratch.  *gap is lowered to the smallest distance of a u[j] to the
+ * CDF step that decided its draw. */
+static void row_sample(const float *x, int V, double T, int k, const float *u, int *out, double *q_buf,
+                       double *gap)
+{
+    const double lse = row_logsumexp(x, V, T);
+    for (int t = 0; t < V; ++t) q_buf[t] = exp((double)x[t] / T - lse);
+    for (int j = 0; j < k; ++j) {
+        double g = INFINITY;
+        out[j] = inverse_cdf(q_buf, V, (double)u[j], &g);
+        if (g < *gap) *gap = g;
+    }
+}
+
+/* A row's k children: the top k (u == NULL) or k draws (u = the row's k uniforms). */
+static void row_children(const float *x, int V, double T, int k, const float *u, int *out, double *q_buf,
+                         double *gap)
+{
+    if (u)
+        row_sample(x, V, T, k, u, out, q_buf, gap);
+    else
+        row_topk(x, V, k, out);
+}
+
 static double bf16_to_double(uint16_t h)
 {
     uint32_t u = ((uint32_t)h) << 16;
@@ -163,9 +195,10 @@ static double key_gap(const cand_t *a, const cand_t *b)
  *   outputs of length n = m + 1 (mask: n * W words, W = ceil(n/64)).
  *   margin: smallest relative key gap at any selection boundary that decides the result.
  */
-static int build_one(int V, int D, int k, int m, double Tt, const float *x, int32_t root_tok,
+static int build_one(int V, int D, int k, int m, double Tt, const float *x, const float *u, int32_t root_tok,
                      int32_t *tokens, int32_t *parents, int32_t *depths, int32_t *node_row,
-                     uint64_t *mask, double *node_logv, double *margin)
+                     uint64_t *mask, double *node_logv, double *margin, double *draw_gap,
+                     int32_t *front_tok, int32_t *front_par)
 {
     const int R = 1 + (D - 1) * k;
     const int P = k + (D - 1) * k * k;
@@ -177,14 +210,19 @@ static int build_one(int V, int D, int k, int m, double Tt, const float *x, int3
     cand_t **order = (cand_t **)calloc((size_t)P, sizeof(cand_t *));
     int *kids = (int *)calloc((size_t)k, sizeof(int));
     int *flat = (int *)calloc((size_t)P, sizeof(int));
-    if (!pool || !order || !kids || !flat) { free(pool); free(order); free(kids); free(flat); return ORC_BAD_ARG; }
+    double *qbuf = u ? (double *)calloc((size_t)V, sizeof(double)) : NULL;
+    double dgap = INFINITY;
+    if (!pool || !order || !kids || !flat || (u && !qbuf)) {
+        free(pool); free(order); free(kids); free(flat); free(qbuf);
+        return ORC_BAD_ARG;
+    }
 
     /* depth 1: the root's children from row 0 */
     int np = 0;
     {
         const float *row = x;
         double lse = row_logsumexp(row, V, Tt);
-        row_topk(row, V, k, kids);
+        row_children(row, V, Tt, k, u, kids, qbuf, &dgap);
         for (int r = 0; r < k; ++r) {
             cand_t *c = &pool[np];
             c->logv = (double)row[kids[r]] / Tt - lse; /* log confidence; log V_parent(root) = 0 */
@@ -207,12 +245,18 @@ static int build_one(int V, int D, int k, int m, double Tt, const float *x, int3
             if (g < gap_min) gap_min = g;
         }
         int next_begin = np;
+        /* the frontier of depth f in slot order, with each node's parent slot at depth f - 1 */
+        for (int s = 0; front_tok && s < nf; ++s) {
+            front_tok[(size_t)(f - 1) * k + s] = order[s]->token;
+            front_par[(size_t)(f - 1) * k + s] =
+                order[s]->parent < 0 ? -1 : pool[order[s]->parent].row - 1 - (f - 2) * k;
+        }
         for (int s = 0; s < nf; ++s) {
             cand_t *par = order[s];
             par->row = 1 + (f - 1) * k + s;
             const float *row = x + (size_t)par->row * V;
             double lse = row_logsumexp(row, V, Tt);
-            row_topk(row, V, k, kids);
+            row_children(row, V, Tt, k, u ? u + (size_t)par->row * k : NULL, kids, qbuf, &dgap);
             for (int r = 0; r < k; ++r) {
                 cand_t *c = &pool[np];
                 c->logv = par->logv + ((double)row[kids[r]] / Tt - lse);
@@ -269,6 +313,8 @@ static int build_one(int V, int D, int k, int m, double Tt, const float *x, int3
         mask[(size_t)i * W + i / 64] |= 1ull << (i % 64);
     }
     *margin = gap_min;
+    if (draw_gap) *draw_gap = dgap;
+    free(qbuf);
     free(kept);
     free(pool);
     free(order);
@@ -277,33 +323,51 @@ static int build_one(int V, int D, int k, int m, double Tt, const float *x, int3
     return status;
 }
 
-/* Batched build.  draft_logits [B][R][V]; outputs [B][n] (mask [B][n][W]). */
-int orc_build_tree(int B, int V, int D, int k, int m, double tree_temp, const float *draft_logits,
-                   const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
-                   int32_t *node_row, uint64_t *mask, double *node_logv, double *margin, int nthreads)
+/* Batched build.  draft_logits [B][R][V]; outputs [B][n] (mask [B][n][W]).
+ * child_u: NULL for top-k children, else [B][R][k] uniforms in [0, 1) (sampled children).
+ * draw_gap [B] (optional): smallest distance of a uniform to the CDF step deciding its draw.
+ * front_tok, front_par [B][D-1][k] (optional, both or neither): the frontier of each depth
+ * f = 1..D-1 in slot order (slot s is expanded with row 1 + (f-1)k + s) and each frontier
+ * node's parent slot at depth f - 1 (-1 at depth 1: the parent is the root). */
+int orc_build_tree_ex(int B, int V, int D, int k, int m, double tree_temp, const float *draft_logits,
+                      const float *child_u, const int32_t *root_token, int32_t *tokens, int32_t *parents,
+                      int32_t *depths, int32_t *node_row, uint64_t *mask, double *node_logv, double *margin,
+                      double *draw_gap, int32_t *front_tok, int32_t *front_par, int nthreads)
 {
     if (B < 0 || V < 1 || D < 1 || k < 1 || k > V || m < 1 || !(tree_temp > 0)) return ORC_BAD_ARG;
+    if ((front_tok == NULL) != (front_par == NULL)) return ORC_BAD_ARG;
     const int P = k + (D - 1) * k * k;
     if (m > P) return ORC_BAD_ARG;
     const int R = 1 + (D - 1) * k;
     const int n = m + 1;
     const int W = (n + 63) / 64;
+    const size_t F = (size_t)(D > 1 ? D - 1 : 1) * k;
     int status = ORC_OK;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
 #pragma omp parallel for schedule(dynamic) reduction(max : status)
 #endif
     for (int b = 0; b < B; ++b) {
-        double mg = INFINITY;
-        int s = build_one(V, D, k, m, tree_temp, draft_logits + (size_t)b * R * V, root_token[b],
+        double mg = INFINITY, dg = INFINITY;
+        int s = build_one(V, D, k, m, tree_temp, draft_logits + (size_t)b * R * V,
+                          child_u ? child_u + (size_t)b * R * k : NULL, root_token[b],
                           tokens + (size_t)b * n, parents + (size_t)b * n, depths + (size_t)b * n,
                           node_row + (size_t)b * n, mask + (size_t)b * n * W, node_logv + (size_t)b * n,
-                          &mg);
+                          &mg, &dg, front_tok ? front_tok + b * F : NULL, front_par ? front_par + b * F : NULL);
         if (margin) margin[b] = mg;
+        if (draw_gap) draw_gap[b] = dg;
         if (s > status) status = s;
     }
     (void)nthreads;
     return status;
+}
+
+int orc_build_tree(int B, int V, int D, int k, int m, double tree_temp, const float *draft_logits,
+                   const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
+                   int32_t *node_row, uint64_t *mask, double *node_logv, double *margin, int nthreads)
+{
+    return orc_build_tree_ex(B, V, D, k, m, tree_temp, draft_logits, NULL, root_token, tokens, parents, depths,
+                             node_row, mask, node_logv, margin, NULL, NULL, NULL, nthreads);
 }
 
 /* ------------------------------------------------------------------------------------------ */
@@ -634,9 +698,13 @@ int orc_tree_verify(int B, int V, int R, int n, int max_commit, double T, const 
  * (row r = the r-th such node); node p's children, in ascending index, take ranks 0, 1, ... of
  * its row's tokens under (value desc, id asc).  log V of a node is the sum of the
  * log-confidences (x/T - logsumexp(x/T) of the row) along its path; the root has 0. */
-int orc_build_static_tree(int B, int V, int n, const int32_t *tmpl, double tree_temp, const float *draft,
-                          const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
-                          int32_t *node_row, uint64_t *mask, double *node_logv)
+/* Sampled children (child_u != NULL, [B][R][kmax] with kmax = the most children of one template
+ * node): node p's children, in ascending index, are draws 0, 1, ... of its row (row_sample),
+ * draw j with child_u[b][row(p)][j].  draw_gap [B] (optional) as in orc_build_tree_ex. */
+int orc_build_static_tree_ex(int B, int V, int n, const int32_t *tmpl, double tree_temp, const float *draft,
+                             const float *child_u, const int32_t *root_token, int32_t *tokens, int32_t *parents,
+                             int32_t *depths, int32_t *node_row, uint64_t *mask, double *node_logv,
+                             double *draw_gap)
 {
     if (B < 1 || V < 1 || n < 1 || n > 64 || !(tree_temp > 0.0) || tmpl[0] != -1) return ORC_BAD_ARG;
     int kids[64] = {0}, row_of[64];
@@ -644,20 +712,26 @@ int orc_build_static_tree(int B, int V, int n, const int32_t *tmpl, double tree_
         if (tmpl[i] < 0 || tmpl[i] >= i) return ORC_BAD_ARG;
         ++kids[tmpl[i]];
     }
-    int R = 0;
+    int R = 0, kmax = 0;
     for (int i = 0; i < n; ++i) {
         if (kids[i] > V) return ORC_BAD_ARG;
         row_of[i] = kids[i] > 0 ? R++ : -1;
+        if (kids[i] > kmax) kmax = kids[i];
     }
     int top[64][64];
     double lse[64];
+    double *qbuf = child_u ? (double *)calloc((size_t)V, sizeof(double)) : NULL;
+    if (child_u && !qbuf) return ORC_BAD_ARG;
     for (int b = 0; b < B; ++b) {
+        double dg = INFINITY;
         for (int p = 0; p < n; ++p)
             if (row_of[p] >= 0) {
                 const float *row = draft + ((size_t)b * R + row_of[p]) * V;
                 lse[p] = row_logsumexp(row, V, tree_temp);
-                row_topk(row, V, kids[p], top[p]);
+                row_children(row, V, tree_temp, kids[p],
+                             child_u ? child_u + ((size_t)b * R + row_of[p]) * kmax : NULL, top[p], qbuf, &dg);
             }
+        if (draw_gap) draw_gap[b] = dg;
         int32_t *tok = tokens + (size_t)b * n, *par = parents + (size_t)b * n, *dep = depths + (size_t)b * n;
         int32_t *nr = node_row + (size_t)b * n;
         uint64_t *mk = mask + (size_t)b * n;
@@ -680,7 +754,16 @@ int orc_build_static_tree(int B, int V, int n, const int32_t *tmpl, double tree_
             mk[i] = mk[p] | (1ull << i);
         }
     }
+    free(qbuf);
     return ORC_OK;
+}
+
+int orc_build_static_tree(int B, int V, int n, const int32_t *tmpl, double tree_temp, const float *draft,
+                          const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
+                          int32_t *node_row, uint64_t *mask, double *node_logv)
+{
+    return orc_build_static_tree_ex(B, V, n, tmpl, tree_temp, draft, NULL, root_token, tokens, parents, depths,
+                                    node_row, mask, node_logv, NULL);
 }
 
 /* ------------------------------------------------------------------------------------------ */

@@ -12,6 +12,7 @@ import oracle
 from tests.test_oracle_attention import _inputs, _mask_from_parents, _sdpa
 from tests.test_oracle_build import _brute_force_tree
 from tests.test_oracle_kv_commit import commit_matches_golden
+from tests.test_oracle_sampled_children import frontier_consistent, sampled_matches_golden
 from tests.test_oracle_static_tree import static_invariants_hold, static_matches_golden
 from tests.test_oracle_verify import _iid_trials, _logits
 
@@ -126,6 +127,22 @@ MUTANTS = {
     # KV commit: keys taken from the tree's values
     "commit_k_from_v": ("memcpy((char *)k_cache + dst, (const char *)k_tree + src, row);",
                         "memcpy((char *)k_cache + dst, (const char *)v_tree + src, row);", "commit"),
+    # sampled children: q formed without the tree temperature
+    "sample_ignores_temperature": ("q_buf[t] = exp((double)x[t] / T - lse);", "q_buf[t] = exp((double)x[t] - lse);",
+                                   "sampled"),
+    # sampled children: draws take the uniforms in reverse order
+    "sample_draw_order_reversed": ("out[j] = inverse_cdf(q_buf, V, (double)u[j], &g);",
+                                   "out[j] = inverse_cdf(q_buf, V, (double)u[k - 1 - j], &g);", "sampled"),
+    # sampled children: a drawn token cannot come up again (without replacement, unnormalised)
+    "sample_without_replacement": ("        if (g < *gap) *gap = g;\n    }\n}\n\n/* A row's k children",
+                                   "        if (g < *gap) *gap = g;\n        q_buf[out[j]] = 0.0;\n    }\n}\n\n/* A row's k children",
+                                   "sampled"),
+    # sampled children: the CDF walked from the top (1 - u)
+    "sample_cdf_from_top": ("out[j] = inverse_cdf(q_buf, V, (double)u[j], &g);",
+                            "out[j] = inverse_cdf(q_buf, V, 1.0 - (double)u[j], &g);", "sampled"),
+    # frontier outputs: parent slot off by one
+    "frontier_parent_slot_shifted": ("pool[order[s]->parent].row - 1 - (f - 2) * k;",
+                                     "pool[order[s]->parent].row - (f - 2) * k;", "sampled"),
 }
 
 
@@ -140,6 +157,8 @@ def test_pins_reject_mutant(name):
             assert not _build_matches_brute_force(orc)
         elif part == "commit":
             assert not commit_matches_golden(orc)
+        elif part == "sampled":
+            assert not (sampled_matches_golden(orc) and frontier_consistent(orc))
         elif part == "static":
             assert not (static_matches_golden(orc) and static_invariants_hold(orc))
         else:
@@ -152,3 +171,4 @@ def test_pins_accept_real_oracle():
     assert _chain_matches_causal(oracle)
     assert commit_matches_golden(oracle)
     assert static_matches_golden(oracle) and static_invariants_hold(oracle)
+    assert sampled_matches_golden(oracle) and frontier_consistent(oracle)

@@ -243,6 +243,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
     commit = run_kv_commit(eg, lib, wl, sets[0], outs, ws, stream, dev)
     draft_attn = run_draft_attention(eg, lib, wl, ws, stream, dev)
     static = run_static_tree(eg, lib, wl, ws, stream, dev)
+    sampled_build = run_sampled_build(eg, lib, wl, ws, stream, dev)
 
     bytes_ = datagen.bytes_of(wl, ctx_total=float(sets[0].attn["ctx_len"].sum().item()))
     peaks = _peaks()
@@ -268,7 +269,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
                            "gbs": metric_bytes / (ms / K * 1e-3) / 1e9,
                            "frac": metric_bytes / (ms / K * 1e-3) / 1e9 / peaks["hbm_gbs"]},
         "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "mean_committed": mean_len,
-        "kv_commit": commit, "draft_attention": draft_attn, "static_tree": static,
+        "kv_commit": commit, "draft_attention": draft_attn, "static_tree": static, "sampled_build": sampled_build,
     }
     return res
 
@@ -468,6 +469,63 @@ def run_static_tree(eg, lib, wl, ws, stream, dev, calls: int = 200) -> dict:
     if ws.status(stream) != 0:
         raise RuntimeError("device status not OK after the static builds")
     res["note"] = f"not in the round's metric; B={B} V={V}, draft rows L2-warm across calls"
+    return res
+
+
+def run_sampled_build(eg, lib, wl, ws, stream, dev, calls: int = 100) -> dict:
+    """The dynamic build with sampled children (eagle_build_tree_sampled) and as a stepwise build
+    (eagle_build_begin, D - 1 eagle_build_expand, eagle_build_finalize), beside the greedy
+    one-call build, on the workload's rows (not part of the round's metric).  CUDA events over
+    `calls` builds each."""
+    B, V, D, k, m = wl.batch, wl.vocab, wl.depth, wl.topk, wl.keep
+    R = 1 + (D - 1) * k
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None  # noqa: E731
+    draft = datagen.draft_logits(B, R, V, 5, dev)
+    cu = datagen.child_uniforms(B, R, k, 5, dev)
+    root = datagen.root_tokens(B, V, 5, dev)
+    rows = [draft[:, :1].contiguous()] + [draft[:, 1 + (f - 1) * k:1 + f * k].contiguous() for f in range(1, D)]
+    us = [cu[:, :1].contiguous()] + [cu[:, 1 + (f - 1) * k:1 + f * k].contiguous() for f in range(1, D)]
+    n = m + 1
+    o = {key: torch.empty((B, n), dtype=torch.int32, device=dev) for key in ("tokens", "parents", "depths", "node_row")}
+    mask = torch.empty((B, n), dtype=torch.int64, device=dev)
+    logv = torch.empty((B, n), dtype=torch.float32, device=dev)
+    ft = torch.empty((B, k), dtype=torch.int32, device=dev)
+    fp = torch.empty((B, k), dtype=torch.int32, device=dev)
+    cfg = eg.tree_cfg(B, V, D, k, m, 1.0)
+    ws.reserve(lib.eagle_build_tree_workspace_size(ctypes.byref(cfg)))
+    s = ctypes.c_void_p(stream.cuda_stream)
+    wsz = ctypes.c_size_t(ws.nbytes)
+    outs = (P(o["tokens"]), P(o["parents"]), P(o["depths"]), P(o["node_row"]), P(mask), P(logv))
+
+    def greedy():
+        return lib.eagle_build_tree(ctypes.byref(cfg), P(draft), P(root), *outs, ws.ptr, wsz, s)
+
+    def sampled():
+        return lib.eagle_build_tree_sampled(ctypes.byref(cfg), P(draft), P(cu), P(root), *outs, ws.ptr, wsz, s)
+
+    def stepwise():
+        st = lib.eagle_build_begin(ctypes.byref(cfg), P(rows[0]), P(us[0]), ws.ptr, wsz, P(ft), P(fp), s)
+        for f in range(1, D):
+            st = st or lib.eagle_build_expand(ctypes.byref(cfg), f, P(rows[f]), P(us[f]), ws.ptr, wsz, P(ft), P(fp), s)
+        return st or lib.eagle_build_finalize(ctypes.byref(cfg), P(root), ws.ptr, wsz, *outs, s)
+
+    res = {}
+    for name, fn in (("greedy_us", greedy), ("sampled_us", sampled), ("stepwise_sampled_us", stepwise)):
+        for _ in range(5):
+            if fn() != 0:
+                raise RuntimeError(f"{name}: build call failed")
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(calls):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = e0.elapsed_time(e1) / calls * 1e3
+    if ws.status(stream) != 0:
+        raise RuntimeError("device status not OK after the sampled builds")
+    res["note"] = (f"not in the round's metric; B={B} V={V} D={D} k={k} m={m}; the stepwise build is "
+                   f"{2 * D} launches with no draft model between them; draft rows L2-warm across calls")
     return res
 
 

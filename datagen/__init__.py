@@ -11,7 +11,8 @@ Workload recipe (each value below is a reading of the workload descriptions, sta
   * target row of tree node i = draft row node_row[i] (a fresh draft-like row when the node was
     never expanded) + N(0, sigma^2) noise, sigma per workload (per sequence for the serving mix);
   * q, K, V (cache and tree) ~ N(0, 1), rounded once to the stored dtype;
-  * uniforms ~ U(0, 1) in float32; root tokens uniform over the vocabulary;
+  * uniforms ~ U(0, 1) in float32 (verify tests and sampled-children draws, separate streams);
+    root tokens uniform over the vocabulary;
   * context lengths fixed per workload, or uniform integers in [512, 8192] for the serving mix.
 """
 from __future__ import annotations
@@ -78,6 +79,7 @@ WORKLOAD_ORDER = ["tiny_f32", "llama31_8b", "vicuna_13b", "llama2_70b_b4", "serv
 # Per-tensor stream offsets so every tensor of a seed has its own generator stream.
 _S_DRAFT, _S_PLANT, _S_ROOT, _S_TGT, _S_TPLANT, _S_TNOISE, _S_SIG = 11, 12, 13, 21, 22, 23, 24
 _S_Q, _S_KC, _S_VC, _S_KT, _S_VT, _S_CTX, _S_U = 31, 32, 33, 34, 35, 36, 41
+_S_CU = 43
 
 
 def _gen(seed: int, stream: int, device) -> torch.Generator:
@@ -140,6 +142,12 @@ def uniforms(batch: int, nodes: int, seed: int, device="cpu") -> torch.Tensor:
     """float32 [B, n] in [0, 1): u[:, 0] draws the final token, u[:, i] tests node i."""
     dev = _dev(device)
     return torch.rand((batch, nodes), generator=_gen(seed, _S_U, dev), device=dev, dtype=torch.float32)
+
+
+def child_uniforms(batch: int, rows: int, topk: int, seed: int, device="cpu") -> torch.Tensor:
+    """float32 [B, R, k] in [0, 1): the draws of sampled children, one per (row, child)."""
+    dev = _dev(device)
+    return torch.rand((batch, rows, topk), generator=_gen(seed, _S_CU, dev), device=dev, dtype=torch.float32)
 
 
 def ctx_lens(wl: Workload, seed: int) -> torch.Tensor:

@@ -94,6 +94,13 @@ _SIGS = {
     "eagle_build_static_tree_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(StaticTreeCfg)]),
     "eagle_build_static_tree": (ctypes.c_int32, [ctypes.POINTER(StaticTreeCfg)] + [_P] * 9 + [ctypes.c_size_t, _P]),
     "eagle_kv_commit": (ctypes.c_int32, [ctypes.POINTER(AttnCfg), ctypes.c_int32] + [_P] * 9 + [ctypes.c_size_t, _P]),
+    "eagle_build_tree_sampled": (ctypes.c_int32, [ctypes.POINTER(TreeCfg)] + [_P] * 10 + [ctypes.c_size_t, _P]),
+    "eagle_build_static_tree_sampled": (ctypes.c_int32,
+                                        [ctypes.POINTER(StaticTreeCfg)] + [_P] * 10 + [ctypes.c_size_t, _P]),
+    "eagle_build_begin": (ctypes.c_int32, [ctypes.POINTER(TreeCfg), _P, _P, _P, ctypes.c_size_t, _P, _P, _P]),
+    "eagle_build_expand": (ctypes.c_int32,
+                           [ctypes.POINTER(TreeCfg), ctypes.c_int32, _P, _P, _P, ctypes.c_size_t, _P, _P, _P]),
+    "eagle_build_finalize": (ctypes.c_int32, [ctypes.POINTER(TreeCfg), _P, _P, ctypes.c_size_t] + [_P] * 7),
 }
 
 
@@ -210,23 +217,31 @@ def tree_cfg(batch, vocab, depth, topk, keep, tree_temp=1.0) -> TreeCfg:
     return TreeCfg(batch, vocab, depth, topk, keep, float(tree_temp))
 
 
+def _tree_out(B: int, n: int, dev, with_logv: bool) -> dict:
+    out = {k: torch.empty((B, n), dtype=torch.int32, device=dev) for k in ("tokens", "parents", "depths", "node_row")}
+    out["mask"] = torch.empty((B, n), dtype=torch.int64, device=dev)
+    out["node_logv"] = torch.empty((B, n), dtype=torch.float32, device=dev) if with_logv else None
+    return out
+
+
 def build_tree(draft_logits: torch.Tensor, root_token: torch.Tensor, depth: int, topk: int, keep: int,
                tree_temp: float = 1.0, ws: Workspace | None = None, out: dict | None = None,
-               with_logv: bool = True, stream=None) -> dict:
+               with_logv: bool = True, stream=None, child_u: torch.Tensor | None = None) -> dict:
     """eagle_build_tree: draft logits f32 [B,R,V], root tokens i32 [B] -> the flattened tree
     (tokens, parents, depths, node_row i32 [B,n]; mask int64 [B,n] holding the u64 bit masks;
-    node_logv f32 [B,n])."""
+    node_logv f32 [B,n]).  With child_u f32 [B,R,topk]: eagle_build_tree_sampled (each row's
+    children are topk inverse-CDF draws from softmax(x / tree_temp))."""
     lib = load()
     B, R, V = draft_logits.shape
     cfg = tree_cfg(B, V, depth, topk, keep, tree_temp)
     _need(draft_logits, "draft_logits", torch.float32)
     _need(root_token, "root_token", torch.int32, (B,))
+    if child_u is not None:
+        _need(child_u, "child_u", torch.float32, (B, R, topk))
     n = keep + 1
     dev = draft_logits.device
     if out is None:
-        out = {k: torch.empty((B, n), dtype=torch.int32, device=dev) for k in ("tokens", "parents", "depths", "node_row")}
-        out["mask"] = torch.empty((B, n), dtype=torch.int64, device=dev)
-        out["node_logv"] = torch.empty((B, n), dtype=torch.float32, device=dev) if with_logv else None
+        out = _tree_out(B, n, dev, with_logv)
     ws = ws or Workspace(device=dev)
     need = lib.eagle_build_tree_workspace_size(ctypes.byref(cfg))
     if need == 0:
@@ -234,10 +249,80 @@ def build_tree(draft_logits: torch.Tensor, root_token: torch.Tensor, depth: int,
     if R != 1 + (depth - 1) * topk:
         raise ValueError(f"draft_logits must have 1 + (depth-1)*topk = {1 + (depth - 1) * topk} rows, got {R}")
     ws.reserve(need, stream)
-    st = lib.eagle_build_tree(ctypes.byref(cfg), _ptr(draft_logits), _ptr(root_token), _ptr(out["tokens"]),
-                              _ptr(out["parents"]), _ptr(out["depths"]), _ptr(out["node_row"]), _ptr(out["mask"]),
-                              _ptr(out.get("node_logv")), ws.ptr, ctypes.c_size_t(ws.nbytes), _stream(stream))
-    _check(st, "eagle_build_tree")
+    tail = (_ptr(root_token), _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["depths"]), _ptr(out["node_row"]),
+            _ptr(out["mask"]), _ptr(out.get("node_logv")), ws.ptr, ctypes.c_size_t(ws.nbytes), _stream(stream))
+    if child_u is None:
+        _check(lib.eagle_build_tree(ctypes.byref(cfg), _ptr(draft_logits), *tail), "eagle_build_tree")
+    else:
+        _check(lib.eagle_build_tree_sampled(ctypes.byref(cfg), _ptr(draft_logits), _ptr(child_u), *tail),
+               "eagle_build_tree_sampled")
+    return out
+
+
+class BuildState:
+    """The workspace and configuration of one stepwise build (eagle_build_begin / _expand /
+    _finalize); the workspace carries the rows' children and the frontiers between the calls."""
+
+    def __init__(self, batch: int, vocab: int, depth: int, topk: int, keep: int, tree_temp: float = 1.0,
+                 ws: Workspace | None = None, device=None, stream=None):
+        self.cfg = tree_cfg(batch, vocab, depth, topk, keep, tree_temp)
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        need = load().eagle_build_tree_workspace_size(ctypes.byref(self.cfg))
+        if need == 0:
+            _check(EAGLE_ERR_UNSUPPORTED, "eagle_build_tree_workspace_size")
+        self.ws = (ws or Workspace(device=self.device)).reserve(need, stream)
+        self.front_tok = torch.empty((batch, topk), dtype=torch.int32, device=self.device)
+        self.front_par = torch.empty((batch, topk), dtype=torch.int32, device=self.device)
+
+
+def _frontier(state: BuildState, written: bool):
+    return (state.front_tok, state.front_par) if written else None
+
+
+def build_begin(state: BuildState, root_logits: torch.Tensor, child_u: torch.Tensor | None = None, stream=None):
+    """eagle_build_begin: the root's draft logits f32 [B,V] (child_u f32 [B,1,topk] for sampled
+    children) -> the frontier of depth 1 (front_tok, front_par i32 [B,topk]), or None when
+    depth == 1.  The returned tensors belong to ``state`` and are overwritten by the next step."""
+    c = state.cfg
+    _need(root_logits, "root_logits", torch.float32, (c.batch, c.vocab))
+    if child_u is not None:
+        _need(child_u, "child_u", torch.float32, (c.batch, 1, c.topk))
+    st = load().eagle_build_begin(ctypes.byref(c), _ptr(root_logits), _ptr(child_u), state.ws.ptr,
+                                  ctypes.c_size_t(state.ws.nbytes), _ptr(state.front_tok), _ptr(state.front_par),
+                                  _stream(stream))
+    _check(st, "eagle_build_begin")
+    return _frontier(state, c.depth >= 2)
+
+
+def build_expand(state: BuildState, depth: int, frontier_logits: torch.Tensor, child_u: torch.Tensor | None = None,
+                 stream=None):
+    """eagle_build_expand: the draft logits f32 [B,topk,V] of the depth-``depth`` frontier (slot
+    order; child_u f32 [B,topk,topk] for sampled children) -> the frontier of depth + 1, or None
+    when depth + 1 is the last depth."""
+    c = state.cfg
+    _need(frontier_logits, "frontier_logits", torch.float32, (c.batch, c.topk, c.vocab))
+    if child_u is not None:
+        _need(child_u, "child_u", torch.float32, (c.batch, c.topk, c.topk))
+    st = load().eagle_build_expand(ctypes.byref(c), int(depth), _ptr(frontier_logits), _ptr(child_u), state.ws.ptr,
+                                   ctypes.c_size_t(state.ws.nbytes), _ptr(state.front_tok), _ptr(state.front_par),
+                                   _stream(stream))
+    _check(st, "eagle_build_expand")
+    return _frontier(state, depth + 1 <= c.depth - 1)
+
+
+def build_finalize(state: BuildState, root_token: torch.Tensor, out: dict | None = None, with_logv: bool = True,
+                   stream=None) -> dict:
+    """eagle_build_finalize: the rerank, flatten and masks of the stepwise build -> the same dict
+    as build_tree."""
+    c = state.cfg
+    _need(root_token, "root_token", torch.int32, (c.batch,))
+    if out is None:
+        out = _tree_out(c.batch, c.keep + 1, state.device, with_logv)
+    st = load().eagle_build_finalize(ctypes.byref(c), _ptr(root_token), state.ws.ptr, ctypes.c_size_t(state.ws.nbytes),
+                                     _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["depths"]),
+                                     _ptr(out["node_row"]), _ptr(out["mask"]), _ptr(out.get("node_logv")),
+                                     _stream(stream))
+    _check(st, "eagle_build_finalize")
     return out
 
 
@@ -279,10 +364,11 @@ def tree_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor
 
 def build_static_tree(draft_logits: torch.Tensor, root_token: torch.Tensor, template_parents, tree_temp: float = 1.0,
                       ws: Workspace | None = None, out: dict | None = None, with_logv: bool = True,
-                      stream=None) -> dict:
+                      stream=None, child_u: torch.Tensor | None = None) -> dict:
     """eagle_build_static_tree: a static tree (EAGLE-1) or chain from a template of parent
     indices.  draft_logits f32 [B,R,V] (R = template nodes with children, in index order), root
-    tokens i32 [B] -> the same dict as build_tree (n = len(template_parents))."""
+    tokens i32 [B] -> the same dict as build_tree (n = len(template_parents)).  With child_u f32
+    [B,R,kmax] (kmax = the most children of one node): eagle_build_static_tree_sampled."""
     lib = load()
     B, R, V = draft_logits.shape
     cfg = static_tree_cfg(B, V, template_parents, tree_temp)
@@ -292,21 +378,24 @@ def build_static_tree(draft_logits: torch.Tensor, root_token: torch.Tensor, temp
         raise ValueError(f"draft_logits must have one row per template node with children ({internal}), got {R}")
     _need(draft_logits, "draft_logits", torch.float32)
     _need(root_token, "root_token", torch.int32, (B,))
+    if child_u is not None:
+        kmax = max([sum(1 for q in template_parents[1:] if int(q) == p) for p in range(n)] + [1])
+        _need(child_u, "child_u", torch.float32, (B, R, kmax))
     dev = draft_logits.device
     if out is None:
-        out = {k: torch.empty((B, n), dtype=torch.int32, device=dev) for k in ("tokens", "parents", "depths", "node_row")}
-        out["mask"] = torch.empty((B, n), dtype=torch.int64, device=dev)
-        out["node_logv"] = torch.empty((B, n), dtype=torch.float32, device=dev) if with_logv else None
+        out = _tree_out(B, n, dev, with_logv)
     ws = ws or Workspace(device=dev)
     need = lib.eagle_build_static_tree_workspace_size(ctypes.byref(cfg))
     if need == 0:
         _check(EAGLE_ERR_UNSUPPORTED, "eagle_build_static_tree")
     ws.reserve(need, stream)
-    st = lib.eagle_build_static_tree(ctypes.byref(cfg), _ptr(draft_logits), _ptr(root_token), _ptr(out["tokens"]),
-                                     _ptr(out["parents"]), _ptr(out["depths"]), _ptr(out["node_row"]),
-                                     _ptr(out["mask"]), _ptr(out.get("node_logv")), ws.ptr, ctypes.c_size_t(ws.nbytes),
-                                     _stream(stream))
-    _check(st, "eagle_build_static_tree")
+    tail = (_ptr(root_token), _ptr(out["tokens"]), _ptr(out["parents"]), _ptr(out["depths"]), _ptr(out["node_row"]),
+            _ptr(out["mask"]), _ptr(out.get("node_logv")), ws.ptr, ctypes.c_size_t(ws.nbytes), _stream(stream))
+    if child_u is None:
+        _check(lib.eagle_build_static_tree(ctypes.byref(cfg), _ptr(draft_logits), *tail), "eagle_build_static_tree")
+    else:
+        _check(lib.eagle_build_static_tree_sampled(ctypes.byref(cfg), _ptr(draft_logits), _ptr(child_u), *tail),
+               "eagle_build_static_tree_sampled")
     return out
 
 

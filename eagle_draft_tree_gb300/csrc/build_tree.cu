@@ -27,6 +27,11 @@ namespace cg = cooperative_groups;
 
 namespace eagle {
 
+int splits_for_rows(long rows, int vocab);
+eagle_status row_sample_launch(const float *draft, const float *u, int B, int R, int V, int k, float tree_temp,
+                               int32_t *row_tok, double *row_lc, int out_R, int out_r0, int32_t *status,
+                               cudaStream_t stream);
+
 namespace {
 
 constexpr int kRowThreads = 512;
@@ -48,9 +53,9 @@ __device__ __forceinline__ void ms_merge(float &m, float &s, float mo, float so,
 
 struct RowArgs {
     const float *x;     // [B][R][V]
-    int32_t *row_tok;   // [B][R][k]  children tokens
-    double *row_lc;     // [B][R][k]  children log-confidences
-    int V, R, k, chunk;
+    int32_t *row_tok;   // [B][out_R][k]  children tokens (rows out_r0 ..)
+    double *row_lc;     // [B][out_R][k]  children log-confidences (rows out_r0 ..)
+    int V, R, k, chunk, out_R, out_r0;
     float c;            // log2(e) / tree_temp
     double inv_t;       // 1 / tree_temp
 };
@@ -256,7 +261,7 @@ __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
             if (lane == 0) lse = double(M) * a.inv_t + log(S);
             lse = __shfl_sync(0xffffffffu, lse, 0);
             if (lane < a.k) {
-                const size_t o = (size_t(b) * a.R + r) * a.k + lane;
+                const size_t o = (size_t(b) * a.out_R + a.out_r0 + r) * a.k + lane;
                 const uint64_t key = s_lists[cur2][0][lane];
                 a.row_tok[o] = int32_t(topk_key_token(key));
                 a.row_lc[o] = double(topk_key_value(key)) * a.inv_t - lse;
@@ -281,6 +286,15 @@ struct SelectArgs {
     float *node_logv;
     int32_t *status;
     int V, D, k, m, R;
+    // Stepwise builds.  The pool is grown to depth `hi` (rows 0 .. 1 + (hi-1)k - 1 are read);
+    // the frontier of a depth below `read_below` is taken from `slots` (pool index of slot s of
+    // depth f at [b][f][s]), the others are ranked, and stored there when `slots` is set.  When
+    // hi <= D - 1 the frontier of depth hi goes to front_tok / front_par [B][k] (token, parent's
+    // slot at depth hi - 1 or -1) and nothing else is written; `finalize` runs the rerank,
+    // flatten and outputs (hi == D).
+    int32_t *slots;
+    int32_t *front_tok, *front_par;
+    int hi, read_below, finalize;
 };
 
 __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) {
@@ -306,7 +320,8 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = a.k, R = a.R, D = a.D, m = a.m;
 
-    // the rows' children (written by row_topk_kernel): every load in flight before the first store
+    // the rows' children (written by the row kernel): every load in flight before the first store
+    const int nload = (1 + (a.hi - 1) * k) * k;
     {
         constexpr int kPer = kMaxPool / kSelThreads;
         double lcv[kPer];
@@ -314,7 +329,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int i = tid + u * kSelThreads;
-            if (i < R * k) {
+            if (i < nload) {
                 lcv[u] = a.row_lc[size_t(b) * R * k + i];
                 tkv[u] = a.row_tok[size_t(b) * R * k + i];
             }
@@ -322,7 +337,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
 #pragma unroll
         for (int u = 0; u < kPer; ++u) {
             const int i = tid + u * kSelThreads;
-            if (i < R * k) {
+            if (i < nload) {
                 s_lc[i] = lcv[u];
                 s_ctok[i] = tkv[u];
             }
@@ -342,11 +357,24 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
 
     // depths 2..D: the k best nodes of the previous depth are expanded; frontier slot = rank
     int lb = 0, cnt = k, np = k;
-    for (int f = 1; f <= D - 1; ++f) {
+    for (int f = 1; f <= D - 1 && f <= a.hi; ++f) {
+        int32_t *slots_f = a.slots ? a.slots + (size_t(b) * D + f) * k : nullptr;
+        if (f < a.read_below) {
+            // the frontier chosen by an earlier call; an index outside this depth's candidates
+            // (a stale or foreign state) is flagged and replaced by the rank order's slot
+            for (int s = tid; s < k; s += kSelThreads) {
+                int e = slots_f[s];
+                if (e < lb || e >= lb + cnt) {
+                    set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
+                    e = lb + s;
+                }
+                s_slot[s] = e;
+                s_row[e] = 1 + (f - 1) * k + s;
+            }
+        } else
         // rank of each candidate of the previous depth: two adjacent threads per candidate, each
         // counting the keys above it in one half of the candidates (the loop is warp-uniform)
-        const int half = (cnt + 1) >> 1;
-        for (int base = 0; base < cnt; base += kSelThreads / 2) {
+        for (int base = 0, half = (cnt + 1) >> 1; base < cnt; base += kSelThreads / 2) {
             const int ei = base + (tid >> 1);
             const bool act = ei < cnt;
             const int e = lb + ei;
@@ -366,9 +394,18 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
             if (act && !(tid & 1) && rank < k) {
                 s_slot[rank] = e;
                 s_row[e] = 1 + (f - 1) * k + rank;
+                if (slots_f) slots_f[rank] = e;
             }
         }
         __syncthreads();
+        if (f == a.hi) {  // a stepwise call: this depth's frontier is the output
+            for (int s = tid; s < k; s += kSelThreads) {
+                const int e = s_slot[s];
+                a.front_tok[size_t(b) * k + s] = s_ptok[e];
+                a.front_par[size_t(b) * k + s] = f == 1 ? -1 : (e - lb) / k;
+            }
+            break;
+        }
         const int nf = cnt < k ? cnt : k;
         for (int i = tid; i < nf * k; i += kSelThreads) {
             const int sl = i / k, ch = i % k;
@@ -388,6 +425,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         cnt = nf * k;
         np += nf * k;
     }
+    if (!a.finalize) return;
 
     // rerank: the m-th largest composite key (keys are unique).  Radix passes over 8-bit digits
     // from the top: a histogram of the digit among the keys sharing the prefix found so far (equal
@@ -542,8 +580,6 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     }
 }
 
-int kmax_for(int k) { return k <= 4 ? 4 : (k <= 8 ? 8 : 16); }
-
 // ---- static tree (EAGLE-1) and chain: a template of parent indices shared by the batch -------
 // Page: "EAGLE: Speculative Sampling Requires Rethinking Feature Uncertainty", appendix A.1 (a
 // fixed draft tree; greedy: a node's children are the top tokens of the draft distribution at
@@ -612,20 +648,10 @@ __global__ void __launch_bounds__(64) static_tree_kernel(StaticArgs a) {
     if (a.node_logv) a.node_logv[o] = float(logv);
 }
 
-// One wave of CTAs: rows are split over a cluster only while the grid stays within the SM count
-// (each CTA streams its slice with loads of the next batch in flight).
-int splits_for_rows(long rows, int vocab) {
-    long sp = 152 / rows;
-    const long per = long(kRowThreads) * kRowVals;
-    const long useful = (vocab + per - 1) / per;  // no empty CTAs
-    if (sp > useful) sp = useful;
-    if (sp > kMaxSplits) sp = kMaxSplits;
-    return sp < 1 ? 1 : int(sp);
-}
-
 // a1 over R rows of B sequences: each row's k children (token, fp64 log-confidence at tree_temp)
+// into row_tok / row_lc [B][out_R][k] at rows out_r0 .. out_r0 + R - 1.
 eagle_status row_topk_launch(const float *draft, int B, int R, int V, int k, float tree_temp, int32_t *row_tok,
-                             double *row_lc, cudaStream_t stream) {
+                             double *row_lc, int out_R, int out_r0, cudaStream_t stream) {
     const int splits = splits_for_rows(long(B) * R, V);
     int chunk = (V + splits - 1) / splits;
     chunk = (chunk + 3) & ~3;
@@ -637,6 +663,8 @@ eagle_status row_topk_launch(const float *draft, int B, int R, int V, int k, flo
     ra.R = R;
     ra.k = k;
     ra.chunk = chunk;
+    ra.out_R = out_R;
+    ra.out_r0 = out_r0;
     ra.c = kLog2e / tree_temp;
     ra.inv_t = 1.0 / double(tree_temp);
     if (launch_pdl(row_topk_kernel, dim3(splits, R, B), dim3(kRowThreads), 0, stream, unsigned(splits), ra) !=
@@ -646,19 +674,39 @@ eagle_status row_topk_launch(const float *draft, int B, int R, int V, int k, flo
     return EAGLE_OK;
 }
 
-template <int KMAX>
-eagle_status launch_build(const eagle_tree_cfg &c, const float *draft, const int32_t *root, int32_t *tokens,
-                          int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv,
-                          unsigned char *ws, cudaStream_t stream) {
-    const int R = 1 + (c.depth - 1) * c.topk;
-    int32_t *row_tok = reinterpret_cast<int32_t *>(ws + kWsHeader);
-    double *row_lc = reinterpret_cast<double *>(ws + kWsHeader + align_up(size_t(c.batch) * R * c.topk * 4, 256));
-    if (eagle_status e = row_topk_launch(draft, c.batch, R, c.vocab, c.topk, c.tree_temp, row_tok, row_lc, stream))
-        return e;
+// A row's k children: its top k (u == nullptr) or k draws with the uniforms u [B][R][k].
+eagle_status row_children_launch(const float *draft, const float *u, int B, int R, int V, int k, float tree_temp,
+                                 int32_t *row_tok, double *row_lc, int out_R, int out_r0, int32_t *status,
+                                 cudaStream_t stream) {
+    if (u) return row_sample_launch(draft, u, B, R, V, k, tree_temp, row_tok, row_lc, out_R, out_r0, status, stream);
+    return row_topk_launch(draft, B, R, V, k, tree_temp, row_tok, row_lc, out_R, out_r0, stream);
+}
 
+// The build's workspace: status header | row_tok [B][R][k] | row_lc [B][R][k] | slots [B][D][k]
+// (the frontier of every depth, kept between the calls of a stepwise build).
+struct BuildWs {
+    int32_t *status, *row_tok, *slots;
+    double *row_lc;
+};
+BuildWs build_ws(const eagle_tree_cfg &c, void *ws) {
+    unsigned char *w = static_cast<unsigned char *>(ws);
+    const size_t ent = size_t(c.batch) * (1 + (c.depth - 1) * c.topk) * c.topk;
+    BuildWs r;
+    r.status = reinterpret_cast<int32_t *>(w);
+    r.row_tok = reinterpret_cast<int32_t *>(w + kWsHeader);
+    r.row_lc = reinterpret_cast<double *>(w + kWsHeader + align_up(ent * 4, 256));
+    r.slots = reinterpret_cast<int32_t *>(w + kWsHeader + align_up(ent * 4, 256) + align_up(ent * 8, 256));
+    return r;
+}
+
+// The select kernel over the rows' children in the workspace (see SelectArgs for the stages).
+eagle_status select_launch(const eagle_tree_cfg &c, const BuildWs &w, const int32_t *root, int32_t *tokens,
+                           int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv,
+                           int hi, int read_below, bool finalize, bool store_slots, int32_t *front_tok,
+                           int32_t *front_par, cudaStream_t stream) {
     SelectArgs sa;
-    sa.row_tok = row_tok;
-    sa.row_lc = row_lc;
+    sa.row_tok = w.row_tok;
+    sa.row_lc = w.row_lc;
     sa.root_token = root;
     sa.tokens = tokens;
     sa.parents = parents;
@@ -666,12 +714,18 @@ eagle_status launch_build(const eagle_tree_cfg &c, const float *draft, const int
     sa.node_row = node_row;
     sa.mask = mask;
     sa.node_logv = node_logv;
-    sa.status = reinterpret_cast<int32_t *>(ws);
+    sa.status = w.status;
     sa.V = c.vocab;
     sa.D = c.depth;
     sa.k = c.topk;
     sa.m = c.keep;
-    sa.R = R;
+    sa.R = 1 + (c.depth - 1) * c.topk;
+    sa.slots = store_slots || read_below > 1 ? w.slots : nullptr;
+    sa.front_tok = front_tok;
+    sa.front_par = front_par;
+    sa.hi = hi;
+    sa.read_below = read_below;
+    sa.finalize = finalize ? 1 : 0;
     if (launch_pdl(tree_select_kernel, dim3(c.batch), dim3(kSelThreads), 0, stream, 1u, sa) != cudaSuccess)
         return EAGLE_ERR_CUDA;
     note_launch();
@@ -680,14 +734,25 @@ eagle_status launch_build(const eagle_tree_cfg &c, const float *draft, const int
 
 }  // namespace
 
+// One wave of CTAs: rows are split over a cluster only while the grid stays within the SM count
+// (each CTA streams its slice with loads of the next batch in flight).
+int splits_for_rows(long rows, int vocab) {
+    long sp = 152 / rows;
+    const long per = long(kRowThreads) * kRowVals;
+    const long useful = (vocab + per - 1) / per;  // no empty CTAs
+    if (sp > useful) sp = useful;
+    if (sp > kMaxSplits) sp = kMaxSplits;
+    return sp < 1 ? 1 : int(sp);
+}
+
 size_t static_tree_workspace_bytes(const eagle_static_tree_cfg &c, int R, int k) {
     const size_t ent = size_t(c.batch) * (R > 0 ? R : 1) * (k > 0 ? k : 1);
     return kWsHeader + align_up(ent * 4, 256) + align_up(ent * 8, 256);
 }
 
 eagle_status build_static_tree_launch(const eagle_static_tree_cfg &c, int R, int k, const float *draft,
-                                      const int32_t *root, int32_t *tokens, int32_t *parents, int32_t *depths,
-                                      int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
+                                      const float *child_u, const int32_t *root, int32_t *tokens, int32_t *parents,
+                                      int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
                                       cudaStream_t stream) {
     unsigned char *w = static_cast<unsigned char *>(ws);
     const size_t ent = size_t(c.batch) * (R > 0 ? R : 1) * (k > 0 ? k : 1);
@@ -695,8 +760,9 @@ eagle_status build_static_tree_launch(const eagle_static_tree_cfg &c, int R, int
     a.row_tok = reinterpret_cast<int32_t *>(w + kWsHeader);
     a.row_lc = reinterpret_cast<double *>(w + kWsHeader + align_up(ent * 4, 256));
     if (R > 0) {
-        if (eagle_status e = row_topk_launch(draft, c.batch, R, c.vocab, k, c.tree_temp, const_cast<int32_t *>(a.row_tok),
-                                             const_cast<double *>(a.row_lc), stream))
+        if (eagle_status e = row_children_launch(draft, child_u, c.batch, R, c.vocab, k, c.tree_temp,
+                                                 const_cast<int32_t *>(a.row_tok), const_cast<double *>(a.row_lc), R,
+                                                 0, reinterpret_cast<int32_t *>(w), stream))
             return e;
     }
     a.root_token = root;
@@ -718,21 +784,50 @@ eagle_status build_static_tree_launch(const eagle_static_tree_cfg &c, int R, int
 }
 
 size_t build_tree_workspace_bytes(const eagle_tree_cfg &c) {
-    const int R = 1 + (c.depth - 1) * c.topk;
-    const size_t ent = size_t(c.batch) * R * c.topk;
-    return kWsHeader + align_up(ent * 4, 256) + align_up(ent * 8, 256);
+    const size_t ent = size_t(c.batch) * (1 + (c.depth - 1) * c.topk) * c.topk;
+    return kWsHeader + align_up(ent * 4, 256) + align_up(ent * 8, 256) +
+           align_up(size_t(c.batch) * c.depth * c.topk * 4, 256);
 }
 
-eagle_status build_tree_launch(const eagle_tree_cfg &c, const float *draft, const int32_t *root, int32_t *tokens,
-                               int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask,
+// The whole build in one call: every row's children (top k, or draws when child_u is set), then
+// the select kernel over all depths.
+eagle_status build_tree_launch(const eagle_tree_cfg &c, const float *draft, const float *child_u, const int32_t *root,
+                               int32_t *tokens, int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask,
                                float *node_logv, void *ws, cudaStream_t stream) {
-    unsigned char *w = static_cast<unsigned char *>(ws);
-    switch (kmax_for(c.topk)) {
-        case 4: return launch_build<4>(c, draft, root, tokens, parents, depths, node_row, mask, node_logv, w, stream);
-        case 8: return launch_build<8>(c, draft, root, tokens, parents, depths, node_row, mask, node_logv, w, stream);
-        default:
-            return launch_build<16>(c, draft, root, tokens, parents, depths, node_row, mask, node_logv, w, stream);
-    }
+    const BuildWs w = build_ws(c, ws);
+    const int R = 1 + (c.depth - 1) * c.topk;
+    if (eagle_status e = row_children_launch(draft, child_u, c.batch, R, c.vocab, c.topk, c.tree_temp, w.row_tok,
+                                             w.row_lc, R, 0, w.status, stream))
+        return e;
+    return select_launch(c, w, root, tokens, parents, depths, node_row, mask, node_logv, c.depth, 1, true, false,
+                         nullptr, nullptr, stream);
+}
+
+// Stepwise build, stage f (0 = begin: the root's row; f >= 1: the rows of the depth-f frontier).
+// The rows' children go to rows 1 + (f-1)k .. of the workspace (row 0 for the root); then, while
+// a deeper frontier is still to be expanded (f + 1 <= D - 1), the select kernel replays the
+// stored frontiers of depths 1..f, ranks depth f + 1 and writes that frontier.
+eagle_status build_step_launch(const eagle_tree_cfg &c, int f, const float *rows, const float *child_u,
+                               int32_t *front_tok, int32_t *front_par, void *ws, cudaStream_t stream) {
+    const BuildWs w = build_ws(c, ws);
+    const int R = 1 + (c.depth - 1) * c.topk;
+    const int nrows = f == 0 ? 1 : c.topk;
+    const int r0 = f == 0 ? 0 : 1 + (f - 1) * c.topk;
+    if (eagle_status e = row_children_launch(rows, child_u, c.batch, nrows, c.vocab, c.topk, c.tree_temp, w.row_tok,
+                                             w.row_lc, R, r0, w.status, stream))
+        return e;
+    if (f + 1 > c.depth - 1) return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
+    return select_launch(c, w, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, f + 1, f + 1, false,
+                         true, front_tok, front_par, stream);
+}
+
+// Stepwise build, last stage: the select kernel over the stored rows and frontiers.
+eagle_status build_finalize_launch(const eagle_tree_cfg &c, const int32_t *root, int32_t *tokens, int32_t *parents,
+                                   int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
+                                   cudaStream_t stream) {
+    const BuildWs w = build_ws(c, ws);
+    return select_launch(c, w, root, tokens, parents, depths, node_row, mask, node_logv, c.depth, c.depth, true, false,
+                         nullptr, nullptr, stream);
 }
 
 }  // namespace eagle

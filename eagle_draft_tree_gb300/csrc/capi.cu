@@ -9,9 +9,15 @@
 namespace eagle {
 
 size_t build_tree_workspace_bytes(const eagle_tree_cfg &c);
-eagle_status build_tree_launch(const eagle_tree_cfg &c, const float *draft, const int32_t *root, int32_t *tokens,
-                               int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask,
+eagle_status build_tree_launch(const eagle_tree_cfg &c, const float *draft, const float *child_u, const int32_t *root,
+                               int32_t *tokens, int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask,
                                float *node_logv, void *ws, cudaStream_t stream);
+eagle_status build_step_launch(const eagle_tree_cfg &c, int f, const float *rows, const float *child_u,
+                               int32_t *front_tok, int32_t *front_par, void *ws, cudaStream_t stream);
+eagle_status build_finalize_launch(const eagle_tree_cfg &c, const int32_t *root, int32_t *tokens, int32_t *parents,
+                                   int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
+                                   cudaStream_t stream);
+size_t row_sample_max_vocab();
 size_t tree_attention_workspace_bytes(const eagle_attn_cfg &c);
 eagle_status tree_attention_launch(const eagle_attn_cfg &c, const void *q, const void *k_cache, const void *v_cache,
                                    const int32_t *ctx_len, const void *k_tree, const void *v_tree,
@@ -24,8 +30,8 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
 size_t verify_max_vocab();
 size_t static_tree_workspace_bytes(const eagle_static_tree_cfg &c, int R, int k);
 eagle_status build_static_tree_launch(const eagle_static_tree_cfg &c, int R, int k, const float *draft,
-                                      const int32_t *root, int32_t *tokens, int32_t *parents, int32_t *depths,
-                                      int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
+                                      const float *child_u, const int32_t *root, int32_t *tokens, int32_t *parents,
+                                      int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
                                       cudaStream_t stream);
 eagle_status kv_commit_launch(const eagle_attn_cfg &c, int depth, const void *k_tree, const void *v_tree,
                               const int32_t *out_path, const int32_t *out_len, const int32_t *ctx_len,
@@ -143,8 +149,56 @@ eagle_status eagle_build_tree(const eagle_tree_cfg *cfg, const float *draft_logi
     if (!draft_logits || !root_token || !tokens || !parents || !depths || !node_row || !mask || !ws)
         return EAGLE_ERR_INVALID_ARG;
     if (!aligned256(ws) || ws_bytes < build_tree_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
-    return build_tree_launch(*cfg, draft_logits, root_token, tokens, parents, depths, node_row, mask, node_logv, ws,
-                             stream);
+    return build_tree_launch(*cfg, draft_logits, nullptr, root_token, tokens, parents, depths, node_row, mask,
+                             node_logv, ws, stream);
+}
+
+eagle_status eagle_build_tree_sampled(const eagle_tree_cfg *cfg, const float *draft_logits, const float *child_u,
+                                      const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
+                                      int32_t *node_row, uint64_t *mask, float *node_logv, void *ws, size_t ws_bytes,
+                                      cudaStream_t stream) {
+    reset_launches();
+    if (int e = check_tree(cfg)) return e;
+    if (size_t(cfg->vocab) > row_sample_max_vocab()) return EAGLE_ERR_UNSUPPORTED;
+    if (!draft_logits || !child_u || !root_token || !tokens || !parents || !depths || !node_row || !mask || !ws)
+        return EAGLE_ERR_INVALID_ARG;
+    if (!aligned256(ws) || ws_bytes < build_tree_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
+    return build_tree_launch(*cfg, draft_logits, child_u, root_token, tokens, parents, depths, node_row, mask,
+                             node_logv, ws, stream);
+}
+
+eagle_status eagle_build_begin(const eagle_tree_cfg *cfg, const float *root_logits, const float *child_u, void *ws,
+                               size_t ws_bytes, int32_t *frontier_tok, int32_t *frontier_parent,
+                               cudaStream_t stream) {
+    reset_launches();
+    if (int e = check_tree(cfg)) return e;
+    if (child_u && size_t(cfg->vocab) > row_sample_max_vocab()) return EAGLE_ERR_UNSUPPORTED;
+    if (!root_logits || !ws) return EAGLE_ERR_INVALID_ARG;
+    if (cfg->depth >= 2 && (!frontier_tok || !frontier_parent)) return EAGLE_ERR_INVALID_ARG;
+    if (!aligned256(ws) || ws_bytes < build_tree_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
+    return build_step_launch(*cfg, 0, root_logits, child_u, frontier_tok, frontier_parent, ws, stream);
+}
+
+eagle_status eagle_build_expand(const eagle_tree_cfg *cfg, int32_t depth, const float *frontier_logits,
+                                const float *child_u, void *ws, size_t ws_bytes, int32_t *frontier_tok,
+                                int32_t *frontier_parent, cudaStream_t stream) {
+    reset_launches();
+    if (int e = check_tree(cfg)) return e;
+    if (child_u && size_t(cfg->vocab) > row_sample_max_vocab()) return EAGLE_ERR_UNSUPPORTED;
+    if (depth < 1 || depth > cfg->depth - 1 || !frontier_logits || !ws) return EAGLE_ERR_INVALID_ARG;
+    if (depth + 1 <= cfg->depth - 1 && (!frontier_tok || !frontier_parent)) return EAGLE_ERR_INVALID_ARG;
+    if (!aligned256(ws) || ws_bytes < build_tree_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
+    return build_step_launch(*cfg, depth, frontier_logits, child_u, frontier_tok, frontier_parent, ws, stream);
+}
+
+eagle_status eagle_build_finalize(const eagle_tree_cfg *cfg, const int32_t *root_token, void *ws, size_t ws_bytes,
+                                  int32_t *tokens, int32_t *parents, int32_t *depths, int32_t *node_row,
+                                  uint64_t *mask, float *node_logv, cudaStream_t stream) {
+    reset_launches();
+    if (int e = check_tree(cfg)) return e;
+    if (!root_token || !tokens || !parents || !depths || !node_row || !mask || !ws) return EAGLE_ERR_INVALID_ARG;
+    if (!aligned256(ws) || ws_bytes < build_tree_workspace_bytes(*cfg)) return EAGLE_ERR_INVALID_ARG;
+    return build_finalize_launch(*cfg, root_token, tokens, parents, depths, node_row, mask, node_logv, ws, stream);
 }
 
 size_t eagle_tree_attention_workspace_size(const eagle_attn_cfg *cfg) {
@@ -204,8 +258,24 @@ eagle_status eagle_build_static_tree(const eagle_static_tree_cfg *cfg, const flo
     if ((R > 0 && !draft_logits) || !root_token || !tokens || !parents || !depths || !node_row || !mask || !ws)
         return EAGLE_ERR_INVALID_ARG;
     if (!aligned256(ws) || ws_bytes < static_tree_workspace_bytes(*cfg, R, k)) return EAGLE_ERR_INVALID_ARG;
-    return build_static_tree_launch(*cfg, R, k, draft_logits, root_token, tokens, parents, depths, node_row, mask,
-                                    node_logv, ws, stream);
+    return build_static_tree_launch(*cfg, R, k, draft_logits, nullptr, root_token, tokens, parents, depths, node_row,
+                                    mask, node_logv, ws, stream);
+}
+
+eagle_status eagle_build_static_tree_sampled(const eagle_static_tree_cfg *cfg, const float *draft_logits,
+                                             const float *child_u, const int32_t *root_token, int32_t *tokens,
+                                             int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask,
+                                             float *node_logv, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    reset_launches();
+    int R = 0, k = 0;
+    if (int e = check_static(cfg, &R, &k)) return e;
+    if (size_t(cfg->vocab) > row_sample_max_vocab()) return EAGLE_ERR_UNSUPPORTED;
+    if ((R > 0 && (!draft_logits || !child_u)) || !root_token || !tokens || !parents || !depths || !node_row ||
+        !mask || !ws)
+        return EAGLE_ERR_INVALID_ARG;
+    if (!aligned256(ws) || ws_bytes < static_tree_workspace_bytes(*cfg, R, k)) return EAGLE_ERR_INVALID_ARG;
+    return build_static_tree_launch(*cfg, R, k, draft_logits, child_u, root_token, tokens, parents, depths, node_row,
+                                    mask, node_logv, ws, stream);
 }
 
 size_t eagle_kv_commit_workspace_size(const eagle_attn_cfg *cfg) {

@@ -104,6 +104,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// ---- fixed-point weight sums (integers in units of a power of two: sums are exact, so every
+// thread and CTA that forms one gets the same value, whatever the order) ----
+// Warp-wide exact sum of values below 2^54 (the result in every lane): two 32-bit reductions of
+// the low 27 bits and of the rest.
+__device__ __forceinline__ uint64_t warp_sum_fx(uint64_t v) {
+    const uint32_t lo = __reduce_add_sync(0xffffffffu, uint32_t(v) & 0x7ffffffu);
+    const uint32_t hi = __reduce_add_sync(0xffffffffu, uint32_t(v >> 27));
+    return (uint64_t(hi) << 27) + lo;
+}
+// floor(u * total) for u in [0, 1) given as a float, exactly (u = mant 2^-sh).
+__device__ __forceinline__ uint64_t scale_fx(uint64_t total, float u) {
+    if (!(u > 0.f)) return 0;
+    const uint32_t ub = __float_as_uint(u);
+    const int ex = int((ub >> 23) & 0xffu);
+    const uint64_t mant = (ub & 0x7fffffu) | (ex ? 0x800000u : 0u);
+    const int sh = 150 - (ex ? ex : 1);  // >= 24 for u < 1
+    const uint64_t lo = total * mant, hi = __umul64hi(total, mant);
+    if (sh >= 128) return 0;
+    if (sh >= 64) return hi >> (sh - 64);
+    return (hi << (64 - sh)) | (lo >> sh);
+}
+
 // ---- mbarrier + bulk copy (global -> own shared memory), with bounded waits ----
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));

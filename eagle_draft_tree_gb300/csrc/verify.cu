@@ -185,13 +185,6 @@ __device__ __forceinline__ float fx_to_float(uint64_t v) {
     return fmaf(__uint2float_rn(uint32_t(v >> 32)), 9.5367431640625e-07f /* 2^-20 */,
                 __uint2float_rn(uint32_t(v)) * 2.220446049250313e-16f /* 2^-52 */);
 }
-// Warp-wide exact sum of values below 2^53 (the result in every lane): two 32-bit reductions
-// of the low 27 bits and of the rest.
-__device__ __forceinline__ uint64_t warp_sum_fx(uint64_t v) {
-    const uint32_t lo = __reduce_add_sync(0xffffffffu, uint32_t(v) & 0x7ffffffu);
-    const uint32_t hi = __reduce_add_sync(0xffffffffu, uint32_t(v >> 27));
-    return (uint64_t(hi) << 27) + lo;
-}
 __device__ __forceinline__ float4 fx_rec(uint64_t v) {
     return make_float4(__uint_as_float(uint32_t(v)), __uint_as_float(uint32_t(v >> 32)), 0.f, 0.f);
 }
@@ -217,19 +210,6 @@ __device__ __forceinline__ uint64_t weight_fx(const float (&w)[kE]) {
 #pragma unroll
     for (int e = 0; e < kChunks; ++e) t += chunk_weight(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
     return clamp53(t);
-}
-
-// floor(u * total) for u in [0, 1) given as a float, exactly (u = mant 2^-sh).
-__device__ __forceinline__ uint64_t scale_fx(uint64_t total, float u) {
-    if (!(u > 0.f)) return 0;
-    const uint32_t ub = __float_as_uint(u);
-    const int ex = int((ub >> 23) & 0xffu);
-    const uint64_t mant = (ub & 0x7fffffu) | (ex ? 0x800000u : 0u);
-    const int sh = 150 - (ex ? ex : 1);  // >= 24 for u < 1
-    const uint64_t lo = total * mant, hi = __umul64hi(total, mant);
-    if (sh >= 128) return 0;
-    if (sh >= 64) return hi >> (sh - 64);
-    return (hi << (64 - sh)) | (lo >> sh);
 }
 
 // p0/q0 in 2^-52 units, clamped at 2^11 (c_j <= 64 and u S_j < 1, so the clamp never decides a

@@ -14,6 +14,9 @@
  *                         sequence; a token sees only its ancestors).
  *   eagle_build_static_tree  a static draft tree (EAGLE-1) or a chain from a caller's template:
  *                         the same outputs as eagle_build_tree (see the entry point below).
+ *   *_sampled, eagle_build_begin/expand/finalize  the same builds with sampled children (the
+ *                         non-greedy setting) and the dynamic build one depth at a time, so
+ *                         that a draft model can run between the depths (see below).
  *   eagle_tree_attention  tree-masked grouped-query attention of the flattened tree against the
  *                         cached context, for every layer.  Defined by: "LLM speculative decoding
  *                         explained" (hubwiz.com), section 5 (the flattened tree is scored in one
@@ -146,6 +149,65 @@ eagle_status eagle_build_tree(const eagle_tree_cfg *cfg, const float *draft_logi
                               int32_t *tokens, int32_t *parents, int32_t *depths, int32_t *node_row,
                               uint64_t *mask, float *node_logv, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * eagle_build_tree with sampled children: the non-greedy drafting of "EAGLE: Speculative Sampling
+ * Requires Rethinking Feature Uncertainty" (papercache.org), appendix A.1 (a node's k children
+ * are sampled from the draft distribution rather than taken as its top k).
+ *   child_u  f32 [B][R][k]  uniforms in [0, 1) (others are clamped into it; NaN counts as 0).
+ * Row r's children are k independent draws from q_r = softmax(x_r / tree_temp), with
+ * replacement (a token may be drawn twice), draw j by inverse CDF over ascending token id with
+ * child_u[b][r][j]; the children keep draw order, so creation order, frontier slots, the rerank
+ * and every output are then as in eagle_build_tree.  Draft confidences (node_logv) are q at the
+ * drawn tokens.  The draw is decided on exact fixed-point sums of the row's weights against its
+ * maximum (units of 2^-40 of the maximum's weight); the fp64 definition can differ only where a
+ * uniform lies within about 1e-6 of a CDF step.
+ * Losslessness: with tree_temp equal to the verify temperature, verification of a tree whose
+ * every expanded node keeps all k children (keep = topk + (depth-1) topk^2, or a static tree)
+ * commits exactly the target distribution.  A rerank that keeps fewer nodes drops children by
+ * their drawn values, which biases the kept candidates.
+ * Workspace: eagle_build_tree_workspace_size.  Extra checks: vocab <= 2^21 (else
+ * EAGLE_ERR_UNSUPPORTED).  Device-side: a row with no finite logit sets EAGLE_ERR_DEVICE_INPUT
+ * and its children are token 0.
+ */
+eagle_status eagle_build_tree_sampled(const eagle_tree_cfg *cfg, const float *draft_logits, const float *child_u,
+                                      const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
+                                      int32_t *node_row, uint64_t *mask, float *node_logv, void *ws, size_t ws_bytes,
+                                      cudaStream_t stream);
+
+/*
+ * Stepwise build: the same tree as eagle_build_tree (or _sampled), one depth at a time, so that a
+ * draft model can produce each depth's rows from the frontier chosen by the previous step (the
+ * EAGLE-2 notes, "Expanding the Draft Tree": only the k most valuable nodes of a depth are fed to
+ * the draft model for the next depth).  The calls, in this order, on one workspace (size
+ * eagle_build_tree_workspace_size; it carries the state between them):
+ *   eagle_build_begin(root_logits f32 [B][V])              row 0;
+ *   eagle_build_expand(depth = f, frontier_logits [B][k][V])  rows 1 + (f-1)k + s, s < k: the
+ *                                                          draft logits at frontier slot s of
+ *                                                          depth f, for f = 1 .. D-1;
+ *   eagle_build_finalize                                   the rerank, flatten and outputs.
+ * child_u: NULL for top-k children, else the step's uniforms, f32 [B][1][k] for begin and
+ * [B][k][k] for expand (the rows' slices of eagle_build_tree_sampled's child_u).
+ * begin and expand(f) with f + 1 <= D - 1 write the frontier of the next depth (1 for begin,
+ * f + 1 for expand), the nodes the draft model expands next:
+ *   frontier_tok     i32 [B][k]  token of slot s;
+ *   frontier_parent  i32 [B][k]  slot, within the previous depth's frontier, of its parent
+ *                                (-1 at depth 1: the parent is the root).
+ * Otherwise the frontier pointers are not used (they may be NULL).  Fed the rows that
+ * eagle_build_tree would read, the steps produce bit-identical outputs.  Calls out of order read
+ * stale state: the result is unspecified, and frontier slots outside their depth set
+ * EAGLE_ERR_DEVICE_INPUT.
+ */
+eagle_status eagle_build_begin(const eagle_tree_cfg *cfg, const float *root_logits, const float *child_u, void *ws,
+                               size_t ws_bytes, int32_t *frontier_tok, int32_t *frontier_parent,
+                               cudaStream_t stream);
+eagle_status eagle_build_expand(const eagle_tree_cfg *cfg, int32_t depth, const float *frontier_logits,
+                                const float *child_u, void *ws, size_t ws_bytes, int32_t *frontier_tok,
+                                int32_t *frontier_parent, cudaStream_t stream);
+/* Outputs as eagle_build_tree. */
+eagle_status eagle_build_finalize(const eagle_tree_cfg *cfg, const int32_t *root_token, void *ws, size_t ws_bytes,
+                                  int32_t *tokens, int32_t *parents, int32_t *depths, int32_t *node_row,
+                                  uint64_t *mask, float *node_logv, cudaStream_t stream);
+
 /* Workspace bytes needed by eagle_build_static_tree (0 for an invalid or unsupported cfg). */
 size_t eagle_build_static_tree_workspace_size(const eagle_static_tree_cfg *cfg);
 
@@ -171,6 +233,19 @@ eagle_status eagle_build_static_tree(const eagle_static_tree_cfg *cfg, const flo
                                      const int32_t *root_token, int32_t *tokens, int32_t *parents, int32_t *depths,
                                      int32_t *node_row, uint64_t *mask, float *node_logv, void *ws, size_t ws_bytes,
                                      cudaStream_t stream);
+
+/*
+ * eagle_build_static_tree with sampled children (appendix A.1 of the EAGLE-1 page: the
+ * non-greedy setting samples a node's children).  child_u f32 [B][R][kmax], kmax = the most
+ * children of one template node: node p's children, in ascending index, are draws 0, 1, ... of
+ * its row, as eagle_build_tree_sampled draws them.  A static template keeps every drawn child,
+ * so build -> verify at tree_temp = the verify temperature is exactly lossless.
+ * Workspace: eagle_build_static_tree_workspace_size.  Extra checks: vocab <= 2^21.
+ */
+eagle_status eagle_build_static_tree_sampled(const eagle_static_tree_cfg *cfg, const float *draft_logits,
+                                             const float *child_u, const int32_t *root_token, int32_t *tokens,
+                                             int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask,
+                                             float *node_logv, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Workspace bytes needed by eagle_tree_attention. */
 size_t eagle_tree_attention_workspace_size(const eagle_attn_cfg *cfg);

@@ -68,8 +68,9 @@ def _bind(path: str):
     lib.orc_build_static_tree.argtypes = [I, I, I, P, D, P, P, P, P, P, P, P, P]
     lib.orc_build_tree_ex.argtypes = [I, I, I, I, I, D, P, P, P, P, P, P, P, P, P, P, P, P, P, I]
     lib.orc_build_static_tree_ex.argtypes = [I, I, I, P, D, P, P, P, P, P, P, P, P, P, P]
+    lib.orc_row_children.argtypes = [I, I, I, D, P, P, P, P, P]
     for f in (lib.orc_build_tree, lib.orc_tree_attention, lib.orc_tree_attention_rows, lib.orc_tree_verify,
-              lib.orc_kv_commit, lib.orc_build_static_tree, lib.orc_build_tree_ex, lib.orc_build_static_tree_ex):
+              lib.orc_kv_commit, lib.orc_build_static_tree, lib.orc_build_tree_ex, lib.orc_build_static_tree_ex, lib.orc_row_children):
         f.restype = I
     return lib
 
@@ -129,6 +130,9 @@ class Oracle:
 
     def build_static_tree(self, *a, **kw):
         return build_static_tree(*a, _lib=self._lib(), **kw)
+
+    def row_children(self, *a, **kw):
+        return row_children(*a, _lib=self._lib(), **kw)
 
 
 def build_tree(draft_logits, root_token, depth: int, topk: int, keep: int, tree_temp: float = 1.0,
@@ -310,3 +314,20 @@ def build_static_tree(draft_logits, root_token, template_parents, tree_temp: flo
                                                     _ptr(out["node_logv"]), _ptr(out["draw_gap"]))
     _check(st, "build_static_tree")
     return out
+
+
+def row_children(rows, topk: int, tree_temp: float = 1.0, child_u=None, _lib=None):
+    """The children of independent draft rows ([EAGLE-1 notes] A.1: top-k when greedy, k draws
+    from softmax(x / T) when not).  rows float32 [N, V]; child_u None or float32 [N, topk].
+    Returns tok int32 [N, topk], lc float64 [N, topk] (log-confidences) and gap float64 [N, topk]
+    (each draw's distance to the CDF step that decided it; inf for top-k children)."""
+    x = _c(rows, np.float32)
+    N, V = x.shape
+    u = None if child_u is None else _c(child_u, np.float32).reshape(N, topk)
+    tok = np.zeros((N, topk), np.int32)
+    lc = np.zeros((N, topk), np.float64)
+    gap = np.full((N, topk), np.inf, np.float64)
+    st = (_lib or _load()).orc_row_children(N, V, topk, float(tree_temp), _ptr(x), _ptr(u), _ptr(tok), _ptr(lc),
+                                            _ptr(gap))
+    _check(st, "row_children")
+    return dict(tok=tok, lc=lc, gap=gap)

@@ -370,6 +370,36 @@ int orc_build_tree(int B, int V, int D, int k, int m, double tree_temp, const fl
                              node_row, mask, node_logv, margin, NULL, NULL, NULL, nthreads);
 }
 
+/* The children of N independent draft rows, as the builds take them: tok, lc [N][k]; u NULL for
+ * the top k, else [N][k] uniforms (row_sample); gap [N][k] (optional, draws only): each draw's
+ * distance to the CDF step that decided it. */
+int orc_row_children(int N, int V, int k, double T, const float *x, const float *u, int32_t *tok, double *lc,
+                     double *gap)
+{
+    if (N < 0 || V < 1 || k < 1 || k > V || !(T > 0)) return ORC_BAD_ARG;
+    double *qbuf = (double *)calloc((size_t)V, sizeof(double));
+    int *kids = (int *)calloc((size_t)k, sizeof(int));
+    if (!qbuf || !kids) { free(qbuf); free(kids); return ORC_BAD_ARG; }
+    for (int r = 0; r < N; ++r) {
+        const float *row = x + (size_t)r * V;
+        const double lse = row_logsumexp(row, V, T);
+        for (int j = 0; j < k; ++j) {
+            double g = INFINITY;
+            if (u)
+                row_sample(row, V, T, 1, u + (size_t)r * k + j, &kids[j], qbuf, &g);
+            if (gap) gap[(size_t)r * k + j] = g;
+        }
+        if (!u) row_topk(row, V, k, kids);
+        for (int j = 0; j < k; ++j) {
+            tok[(size_t)r * k + j] = kids[j];
+            lc[(size_t)r * k + j] = (double)row[kids[j]] / T - lse;
+        }
+    }
+    free(qbuf);
+    free(kids);
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------------------------ */
 /* 2. Tree attention  ([EAGLE-3 blog] section 5; [EAGLE-2 notes] Tree Attention Mask)           */
 /* ------------------------------------------------------------------------------------------ */

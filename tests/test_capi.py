@@ -144,3 +144,33 @@ def test_static_tree_host_validation(parents, code):
         assert size >= 256 and st == eg.EAGLE_ERR_INVALID_ARG  # valid template, null buffers
     else:
         assert size == 0 and st == code
+
+
+def test_sampled_and_stepwise_host_validation():
+    lib = eg.load()
+    cfg = _tree()
+    fake = ctypes.c_void_p(256 * 1024)  # never dereferenced: a host check fails first
+    P = [fake] * 7
+    # sampled build: the uniforms are required; vocabularies above 2^21 are not supported
+    st = lib.eagle_build_tree_sampled(ctypes.byref(cfg), fake, None, *P, fake, 1 << 30, None)
+    assert st == eg.EAGLE_ERR_INVALID_ARG
+    big = _tree(vocab=(1 << 21) + 4)
+    assert lib.eagle_build_tree_sampled(ctypes.byref(big), *([fake] * 9), fake, 1 << 30, None) == eg.EAGLE_ERR_UNSUPPORTED
+    scfg = eg.static_tree_cfg(2, 1000, [-1, 0, 0, 1], 1.0)
+    st = lib.eagle_build_static_tree_sampled(ctypes.byref(scfg), fake, None, *P, fake, 1 << 30, None)
+    assert st == eg.EAGLE_ERR_INVALID_ARG
+    # stepwise: frontier outputs are required while a deeper frontier remains; depth in 1..D-1
+    assert lib.eagle_build_begin(ctypes.byref(cfg), fake, None, fake, 1 << 30, None, None, None) == \
+        eg.EAGLE_ERR_INVALID_ARG
+    for d in (0, 3):
+        assert lib.eagle_build_expand(ctypes.byref(cfg), d, fake, None, fake, 1 << 30, fake, fake, None) == \
+            eg.EAGLE_ERR_INVALID_ARG
+    assert lib.eagle_build_expand(ctypes.byref(cfg), 1, fake, None, fake, 1 << 30, None, fake, None) == \
+        eg.EAGLE_ERR_INVALID_ARG
+    # too small a workspace (the stepwise state lives in it)
+    assert lib.eagle_build_expand(ctypes.byref(cfg), 2, fake, None, fake, 16, None, None, None) == \
+        eg.EAGLE_ERR_INVALID_ARG
+    assert lib.eagle_build_finalize(ctypes.byref(cfg), fake, fake, 1 << 30, None, *([fake] * 5), None) == \
+        eg.EAGLE_ERR_INVALID_ARG
+    assert lib.eagle_build_finalize(ctypes.byref(_tree(batch=0)), fake, fake, 1 << 30, *([fake] * 6), None) == \
+        eg.EAGLE_ERR_INVALID_ARG

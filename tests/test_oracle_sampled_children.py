@@ -214,3 +214,22 @@ def frontier_consistent(orc, seeds=range(4)) -> bool:
 
 def test_frontier_outputs_match_the_tree():
     assert frontier_consistent(oracle)
+
+
+def test_row_children_are_the_builds_children():
+    """The per-row entry point gives the same children as a depth-1 build that keeps them all
+    (sampled: in draw order; greedy: the top k in rank order)."""
+    rng = np.random.default_rng(13)
+    N, V, k = 12, 300, 5
+    x = rng.normal(0, 2, (N, V)).astype(np.float32)
+    u = rng.random((N, k), dtype=np.float32)
+    for cu, T in ((u, 1.0), (u, 0.6), (None, 1.0)):
+        rc = oracle.row_children(x, k, T, child_u=cu)
+        b = oracle.build_tree(x[:, None], np.zeros(N, np.int32), 1, k, k, T,
+                              child_u=None if cu is None else cu[:, None])
+        if cu is None:  # the build flattens by creation order = rank order
+            assert np.array_equal(rc["tok"], b["tokens"][:, 1:])
+        else:
+            assert np.array_equal(rc["tok"], b["tokens"][:, 1:])
+            assert np.array_equal(rc["gap"].min(1), b["draw_gap"])
+        assert np.allclose(rc["lc"], b["node_logv"][:, 1:], rtol=0, atol=0)

@@ -649,10 +649,12 @@ __global__ void __launch_bounds__(64) static_tree_kernel(StaticArgs a) {
 }
 
 // a1 over R rows of B sequences: each row's k children (token, fp64 log-confidence at tree_temp)
-// into row_tok / row_lc [B][out_R][k] at rows out_r0 .. out_r0 + R - 1.
+// into row_tok / row_lc [B][out_R][k] at rows out_r0 .. out_r0 + R - 1.  A row's slices are
+// planned for `plan_rows` rows in all: the log normaliser's float sums depend on the slicing,
+// so a stepwise build plans its partial calls like the one-call build to get the same bits.
 eagle_status row_topk_launch(const float *draft, int B, int R, int V, int k, float tree_temp, int32_t *row_tok,
-                             double *row_lc, int out_R, int out_r0, cudaStream_t stream) {
-    const int splits = splits_for_rows(long(B) * R, V);
+                             double *row_lc, int out_R, int out_r0, long plan_rows, cudaStream_t stream) {
+    const int splits = splits_for_rows(plan_rows, V);
     int chunk = (V + splits - 1) / splits;
     chunk = (chunk + 3) & ~3;
     RowArgs ra;
@@ -674,12 +676,14 @@ eagle_status row_topk_launch(const float *draft, int B, int R, int V, int k, flo
     return EAGLE_OK;
 }
 
-// A row's k children: its top k (u == nullptr) or k draws with the uniforms u [B][R][k].
+// A row's k children: its top k (u == nullptr) or k draws with the uniforms u [B][R][k].  The
+// draws are exact fixed-point decisions whatever the slicing, so only the top-k kernel takes the
+// one-call plan (B * out_R rows).
 eagle_status row_children_launch(const float *draft, const float *u, int B, int R, int V, int k, float tree_temp,
                                  int32_t *row_tok, double *row_lc, int out_R, int out_r0, int32_t *status,
                                  cudaStream_t stream) {
     if (u) return row_sample_launch(draft, u, B, R, V, k, tree_temp, row_tok, row_lc, out_R, out_r0, status, stream);
-    return row_topk_launch(draft, B, R, V, k, tree_temp, row_tok, row_lc, out_R, out_r0, stream);
+    return row_topk_launch(draft, B, R, V, k, tree_temp, row_tok, row_lc, out_R, out_r0, long(B) * out_R, stream);
 }
 
 // The build's workspace: status header | row_tok [B][R][k] | row_lc [B][R][k] | slots [B][D][k]

@@ -18,7 +18,8 @@
 //   draw j        warp j of each CTA: target = floor(u_j * total) in fixed point; the CTA whose
 //                 slice range holds it walks column -> warp -> lane -> token, re-deriving the one
 //                 chunk's weights from the row with the same arithmetic (hence the same values).
-// The row's log normaliser is M / T + ln(total 2^-40).
+// The row's log normaliser is M / T + ln(total 2^-40).  Chunks start at multiples of 4 tokens and
+// every sum above a chunk is exact, so draws and log-confidences do not depend on the slicing.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>

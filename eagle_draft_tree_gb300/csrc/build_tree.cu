@@ -14,8 +14,9 @@
 //                      cluster's lists and sums through distributed shared memory and writes the
 //                      row's k children (token, fp64 log-confidence).
 //   tree_select_kernel one CTA per sequence: per-depth frontier selection (rank of a 64-bit
-//                      composite key), expansion, the global rerank (8-pass radix select of the
-//                      m-th largest key over the <= 1024-entry pool), flatten, masks.
+//                      composite key), expansion, the global rerank (a key's rank within its
+//                      depth plus binary searches in the other depths' sorted lists), flatten,
+//                      masks.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -39,6 +40,7 @@ constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kRowVals = 16;  // values per thread per batch (4 float4 in registers)
 constexpr int kSelThreads = 256;
 constexpr int kMaxPool = 1024;
+constexpr int kMaxDepth = 64;
 constexpr int kMaxSplits = 8;  // portable cluster size
 
 // Merge (m_a, s_a) and (m_b, s_b) where s = sum 2^((x - m) c).
@@ -300,20 +302,25 @@ struct SelectArgs {
 __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) {
     pdl_wait();
     pdl_launch_next();
-    __shared__ double s_lc[kMaxPool];     // [R*k] child log-confidences (R*k = P <= 1024)
-    __shared__ int s_ctok[kMaxPool];      // [R*k] child tokens
+    // [R*k] child log-confidences (R*k = P <= 1024); after the expansion, the per-depth lists
+    __shared__ union {
+        double lc[kMaxPool];
+        uint64_t sorted[kMaxPool];
+    } s_u;
+    // [R*k] child tokens; after the expansion, the kept flags
+    __shared__ union {
+        int ctok[kMaxPool];
+        int kept[kMaxPool];
+    } s_v;
     __shared__ double s_logv[kMaxPool];   // pool: log V
     __shared__ uint64_t s_key[kMaxPool];  // pool: composite key
     __shared__ int s_par[kMaxPool];       // pool: parent pool index (-1: the root)
     __shared__ int s_row[kMaxPool];       // pool: draft row that expanded it, or -1
-    __shared__ int s_flat[kMaxPool];      // pool: flattened node index, or -1
+    __shared__ int s_flat[kMaxPool];      // pool: rank within its depth, then flattened index or -1
     __shared__ int s_ptok[kMaxPool];      // pool: token
     __shared__ unsigned char s_dep[kMaxPool];
     __shared__ int s_slot[16];
-    __shared__ int s_hist[2][256];  // by pass parity: a pass clears the next pass's buffer
-    __shared__ uint64_t s_prefix;
-    __shared__ uint64_t s_gather[32];
-    __shared__ int s_remaining, s_bcount;
+    __shared__ int s_dlb[kMaxDepth + 2], s_dcnt[kMaxDepth + 2], s_doff[kMaxDepth + 2];  // per depth
     __shared__ int s_wsum[kMaxPool / 32];
 
     const int b = blockIdx.x;
@@ -338,42 +345,28 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         for (int u = 0; u < kPer; ++u) {
             const int i = tid + u * kSelThreads;
             if (i < nload) {
-                s_lc[i] = lcv[u];
-                s_ctok[i] = tkv[u];
+                s_u.lc[i] = lcv[u];
+                s_v.ctok[i] = tkv[u];
             }
         }
     }
     __syncthreads();
     // depth 1: the root's children (row 0)
     for (int i = tid; i < k; i += kSelThreads) {
-        s_logv[i] = s_lc[i];
-        s_key[i] = pool_key(s_lc[i], i);
-        s_ptok[i] = s_ctok[i];
+        s_logv[i] = s_u.lc[i];
+        s_key[i] = pool_key(s_u.lc[i], i);
+        s_ptok[i] = s_v.ctok[i];
         s_par[i] = -1;
         s_row[i] = -1;
         s_dep[i] = 1;
     }
     __syncthreads();
 
-    // depths 2..D: the k best nodes of the previous depth are expanded; frontier slot = rank
-    int lb = 0, cnt = k, np = k;
-    for (int f = 1; f <= D - 1 && f <= a.hi; ++f) {
-        int32_t *slots_f = a.slots ? a.slots + (size_t(b) * D + f) * k : nullptr;
-        if (f < a.read_below) {
-            // the frontier chosen by an earlier call; an index outside this depth's candidates
-            // (a stale or foreign state) is flagged and replaced by the rank order's slot
-            for (int s = tid; s < k; s += kSelThreads) {
-                int e = slots_f[s];
-                if (e < lb || e >= lb + cnt) {
-                    set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
-                    e = lb + s;
-                }
-                s_slot[s] = e;
-                s_row[e] = 1 + (f - 1) * k + s;
-            }
-        } else
-        // rank of each candidate of the previous depth: two adjacent threads per candidate, each
-        // counting the keys above it in one half of the candidates (the loop is warp-uniform)
+    // Rank of each candidate of one depth within the depth (keys are unique): two adjacent
+    // threads per candidate, each counting the keys above it in one half of the depth (the loop
+    // is warp-uniform).  The rank goes to s_flat (free until the flatten); with `frontier`, the k
+    // best are the depth's frontier (slot = rank) and go to s_slot and, if set, slots_f.
+    auto rank_depth = [&](int lb, int cnt, int f, int32_t *slots_f, bool frontier) {
         for (int base = 0, half = (cnt + 1) >> 1; base < cnt; base += kSelThreads / 2) {
             const int ei = base + (tid >> 1);
             const bool act = ei < cnt;
@@ -391,11 +384,41 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
             for (; o < o1; ++o) r0 += s_key[o] > v;
             const int part = (r0 + r1) + (r2 + r3);
             const int rank = part + __shfl_xor_sync(0xffffffffu, part, 1);
-            if (act && !(tid & 1) && rank < k) {
-                s_slot[rank] = e;
-                s_row[e] = 1 + (f - 1) * k + rank;
-                if (slots_f) slots_f[rank] = e;
+            if (act && !(tid & 1)) {
+                s_flat[e] = rank;
+                if (frontier && rank < k) {
+                    s_slot[rank] = e;
+                    s_row[e] = 1 + (f - 1) * k + rank;
+                    if (slots_f) slots_f[rank] = e;
+                }
             }
+        }
+    };
+
+    // depths 2..D: the k best nodes of the previous depth are expanded; frontier slot = rank
+    int lb = 0, cnt = k, np = k;
+    uint64_t ranked = 0;  // depths whose candidates were ranked here (the same in every thread)
+    for (int f = 1; f <= D - 1 && f <= a.hi; ++f) {
+        if (tid == 0) {
+            s_dlb[f] = lb;
+            s_dcnt[f] = cnt;
+        }
+        int32_t *slots_f = a.slots ? a.slots + (size_t(b) * D + f) * k : nullptr;
+        if (f < a.read_below) {
+            // the frontier chosen by an earlier call; an index outside this depth's candidates
+            // (a stale or foreign state) is flagged and replaced by the rank order's slot
+            for (int s = tid; s < k; s += kSelThreads) {
+                int e = slots_f[s];
+                if (e < lb || e >= lb + cnt) {
+                    set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
+                    e = lb + s;
+                }
+                s_slot[s] = e;
+                s_row[e] = 1 + (f - 1) * k + s;
+            }
+        } else {
+            rank_depth(lb, cnt, f, slots_f, true);
+            ranked |= 1ull << f;
         }
         __syncthreads();
         if (f == a.hi) {  // a stepwise call: this depth's frontier is the output
@@ -412,10 +435,10 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
             const int par = s_slot[sl];
             const int rr = 1 + (f - 1) * k + sl;
             const int e = np + i;
-            const double lv = s_logv[par] + s_lc[rr * k + ch];
+            const double lv = s_logv[par] + s_u.lc[rr * k + ch];
             s_logv[e] = lv;
             s_key[e] = pool_key(lv, e);
-            s_ptok[e] = s_ctok[rr * k + ch];
+            s_ptok[e] = s_v.ctok[rr * k + ch];
             s_par[e] = par;
             s_row[e] = -1;
             s_dep[e] = (unsigned char)(f + 1);
@@ -427,93 +450,60 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     }
     if (!a.finalize) return;
 
-    // rerank: the m-th largest composite key (keys are unique).  Radix passes over 8-bit digits
-    // from the top: a histogram of the digit among the keys sharing the prefix found so far (equal
-    // digits of a warp counted once per warp, via __match_any_sync: most keys share their top
-    // bits, and per-key atomics on one bucket serialise); the bucket holding the m-th largest
-    // extends the prefix.  Once that bucket holds at most 32 keys, one warp gathers them, sorts
-    // them and reads the answer off.
+    // rerank: keep the m largest keys of the pool (keys are unique).  A key's rank in the pool is
+    // its rank within its depth plus, for every other depth, the number of that depth's keys
+    // above it.  Only a depth's m best keys can be kept or decide a count below m, so each
+    // depth contributes a descending list of its first min(cnt, m) keys, and the counts are
+    // binary searches in those lists.
+    if (tid == 0) {  // the last depth
+        s_dlb[D] = lb;
+        s_dcnt[D] = cnt;
+    }
+    __syncthreads();
+    for (int d = 1; d <= D; ++d)  // depths not ranked above (the last; frontiers read from slots)
+        if (d == 64 || !((ranked >> d) & 1ull)) rank_depth(s_dlb[d], s_dcnt[d], d, nullptr, false);
     if (tid == 0) {
-        s_prefix = 0;
-        s_remaining = m;
-        s_bcount = 0x7fffffff;
+        int off = 0;
+        for (int d = 1; d <= D; ++d) {
+            s_doff[d] = off;
+            off += min(s_dcnt[d], m);
+        }
+        s_doff[D + 1] = off;
     }
-    s_hist[0][tid] = 0;  // kSelThreads == 256 buckets
-    __syncthreads();
-    uint64_t hmask = 0;
-    for (int shift = 56, cur = 0; shift >= 0; shift -= 8, cur ^= 1) {
-        s_hist[cur ^ 1][tid] = 0;  // the previous pass's buffer, read before its closing barrier
-        const uint64_t prefix = s_prefix;
-        for (int e0 = 0; e0 < np; e0 += kSelThreads) {  // whole warps take part in the match
-            const int e = e0 + tid;
-            const uint64_t key = e < np ? s_key[e] : 0ull;
-            const bool in = e < np && (key & hmask) == prefix;
-            const unsigned dig = in ? unsigned((key >> shift) & 255) : 256u + unsigned(lane);
-            const unsigned grp = __match_any_sync(0xffffffffu, dig);
-            if (in && lane == __ffs(grp) - 1) atomicAdd(&s_hist[cur][dig], __popc(grp));
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // buckets from the top: lane l owns buckets 255-8l .. 248-8l
-            int cntl = 0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) cntl += s_hist[cur][255 - 8 * lane - q];
-            int incl = cntl;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += o;
-            }
-            const int need = s_remaining;
-            const int excl = incl - cntl;
-            if (excl < need && need <= incl) {
-                int acc = excl;
-                for (int q = 0; q < 8; ++q) {
-                    const int bucket = 255 - 8 * lane - q;
-                    const int h = s_hist[cur][bucket];
-                    if (acc + h >= need) {
-                        s_prefix = prefix | (uint64_t(bucket) << shift);
-                        s_remaining = need - acc;
-                        s_bcount = h;
-                        break;
-                    }
-                    acc += h;
-                }
-            }
-        }
-        hmask |= uint64_t(255) << shift;
-        __syncthreads();
-        if (s_bcount <= 32) break;  // CTA-uniform
-    }
-    if (warp == 0) {
-        // the <= 32 keys of the chosen bucket, in creation order, then sorted descending
-        const uint64_t prefix = s_prefix;
-        uint64_t mine = 0;
-        int filled = 0;
-        for (int e0 = 0; e0 < np; e0 += 32) {
-            const int e = e0 + lane;
-            const bool in = e < np && (s_key[e] & hmask) == prefix;
-            const unsigned bal = __ballot_sync(0xffffffffu, in);
-            const int pos = filled + __popc(bal & ((1u << lane) - 1u));
-            const uint64_t key = in ? s_key[e] : 0ull;
-            // lane `pos` receives it: gather through shared memory
-            if (in && pos < 32) s_gather[pos] = key;
-            filled += __popc(bal);
-        }
-        __syncwarp();
-        mine = lane < min(filled, 32) ? s_gather[lane] : 0ull;
-        const uint64_t srt = warp_sort_desc(mine);
-        const uint64_t kth = __shfl_sync(0xffffffffu, srt, s_remaining - 1);
-        if (lane == 0) s_prefix = kth;
+    __syncthreads();  // ranks and offsets; the rows' children are no longer read
+    for (int e = tid; e < np; e += kSelThreads) {
+        const int r = s_flat[e];
+        if (r < m) s_u.sorted[s_doff[s_dep[e]] + r] = s_key[e];
     }
     __syncthreads();
-    const uint64_t thr = s_prefix;  // the m-th largest key itself
+    for (int e = tid; e < np; e += kSelThreads) {
+        const int d = s_dep[e];
+        const uint64_t v = s_key[e];
+        int g = s_flat[e];
+        // two depths' searches at a time, so that their shared-memory loads overlap
+        for (int d2 = 1; d2 <= D && g < m; d2 += 2) {
+            const int d3 = d2 + 1;
+            const int la = d2 == d ? 0 : min(s_dcnt[d2], m);
+            const int lb2 = (d3 > D || d3 == d) ? 0 : min(s_dcnt[d3], m);
+            const uint64_t *A = s_u.sorted + s_doff[d2];
+            const uint64_t *Bl = s_u.sorted + s_doff[d3 <= D ? d3 : D + 1];
+            int pa = 0, pb = 0;  // keys above v in each list (lists are descending, m <= 63)
+#pragma unroll
+            for (int step = 32; step > 0; step >>= 1) {
+                if (pa + step <= la && A[pa + step - 1] > v) pa += step;
+                if (pb + step <= lb2 && Bl[pb + step - 1] > v) pb += step;
+            }
+            g += pa + pb;
+        }
+        s_v.kept[e] = g < m;
+    }
+    __syncthreads();
 
     // flatten: flat index = 1 + number of kept entries created earlier (ballots over creation order)
     const int nchunks = (np + 31) / 32;
     for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
         const int e = ch * 32 + lane;
-        const bool kept = e < np && s_key[e] >= thr;
+        const bool kept = e < np && s_v.kept[e];
         const unsigned bal = __ballot_sync(0xffffffffu, kept);
         if (lane == 0) s_wsum[ch] = __popc(bal);
     }
@@ -531,7 +521,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     __syncthreads();
     for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
         const int e = ch * 32 + lane;
-        const bool kept = e < np && s_key[e] >= thr;
+        const bool kept = e < np && s_v.kept[e];
         const unsigned bal = __ballot_sync(0xffffffffu, kept);
         if (e < np) s_flat[e] = kept ? 1 + s_wsum[ch] + __popc(bal & ((1u << lane) - 1u)) : -1;
     }

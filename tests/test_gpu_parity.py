@@ -27,7 +27,7 @@ BUILD_SHAPES = [
     # (B, V, D, k, m)
     (1, 1000, 3, 4, 10), (3, 1000, 3, 4, 10), (2, 32000, 6, 10, 50), (2, 128256, 8, 10, 60),
     (4, 16, 2, 3, 12), (2, 500, 1, 5, 5), (2, 300, 5, 1, 5), (2, 4096, 4, 16, 63), (5, 777, 3, 7, 30),
-    (2, 2048, 2, 2, 1),
+    (2, 2048, 2, 2, 1), (2, 300, 64, 1, 63), (1, 2000, 11, 10, 63),
 ]
 
 

@@ -112,6 +112,8 @@ SHAPES = [  # B, V, D, k, m, T: whole trees (small vocabularies: almost every dr
     (4, 1003, 4, 3, 20, 0.7),     # V not a multiple of 4: scalar loads
     (6, 5000, 2, 16, 63, 1.0),    # k = 16: one warp per draw, all 16 warps
     (16, 300, 6, 10, 60, 1.0),
+    (2, 300, 64, 1, 63, 1.0),     # the deepest tree: a chain of 64 depths
+    (1, 2000, 11, 10, 63, 1.0),   # a pool of 1010 candidates
 ]
 
 

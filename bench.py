@@ -48,6 +48,15 @@ def _peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def _side_roofline(nbytes: float, us: float, what: str) -> dict:
+    """HBM roofline of a separately timed call: its algorithmic bytes over its event time."""
+    pk = _peaks()
+    achieved = nbytes / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "algorithmic_bytes": nbytes, "timed": what,
+            "peak_source": f"{pk['source']} hbm_gbs (MEASURED_PEAKS.json)"}
+
+
 def _workload_desc(wl) -> str:
     ctx = f"ctx={wl.ctx}" if wl.ctx_min == wl.ctx else f"ctx=U[{wl.ctx_min},{wl.ctx}]"
     return (f"{wl.name}: B={wl.batch} V={wl.vocab} D={wl.depth} k={wl.topk} m={wl.keep} L={wl.layers} "
@@ -389,6 +398,7 @@ def run_kv_commit(eg, lib, wl, rd: Round, outs, ws, stream, dev, calls: int = 20
     rows = int(outs["out_len"].sum().item())
     moved = 2 * 2 * L * rows * Hkv * d * kc.element_size()  # K and V, read and written
     return {"us": us, "rows_per_sequence": rows / B, "bytes_moved": moved, "gbs": moved / (us * 1e-6) / 1e9,
+            "roofline": _side_roofline(moved, us, "kv_commit_kernel"),
             "note": "not in the round's metric; latency-bound (a few KB per layer and sequence)"}
 
 
@@ -428,6 +438,10 @@ def run_draft_attention(eg, lib, wl, ws, stream, dev, calls: int = 200) -> dict:
         e1.record(stream)
         torch.cuda.synchronize(dev)
         res[f"n{n}_us"] = e0.elapsed_time(e1) / calls * 1e3
+        es = 2  # bf16
+        nbytes = (2 * ctx * wl.heads_kv * wl.head_dim * es + 2 * n * wl.heads_q * wl.head_dim * es
+                  + 2 * n * wl.heads_kv * wl.head_dim * es + n * 8)  # K/V context, q and out, tree K/V, masks
+        res["roofline"] = _side_roofline(nbytes, res[f"n{n}_us"], f"tree attention at n={n} (split + merge)")
     if ws.status(stream) != 0:
         raise RuntimeError("device status not OK after the draft-shape attention")
     res["shape"] = f"L=1 B=1 Hq={wl.heads_q} Hkv={wl.heads_kv} d={wl.head_dim} ctx={ctx}"
@@ -466,6 +480,9 @@ def run_static_tree(eg, lib, wl, ws, stream, dev, calls: int = 200) -> dict:
         e1.record(stream)
         torch.cuda.synchronize(dev)
         res[f"{name}_n{n}_us"] = e0.elapsed_time(e1) / calls * 1e3
+        if name == "chain":
+            res["roofline"] = _side_roofline(B * R * V * 4, res[f"{name}_n{n}_us"],
+                                             f"chain of {wl.depth}: row top-k + static tree kernel")
     if ws.status(stream) != 0:
         raise RuntimeError("device status not OK after the static builds")
     res["note"] = f"not in the round's metric; B={B} V={V}, draft rows L2-warm across calls"
@@ -524,6 +541,7 @@ def run_sampled_build(eg, lib, wl, ws, stream, dev, calls: int = 100) -> dict:
         res[name] = e0.elapsed_time(e1) / calls * 1e3
     if ws.status(stream) != 0:
         raise RuntimeError("device status not OK after the sampled builds")
+    res["roofline"] = _side_roofline(B * R * V * 4, res["sampled_us"], "row_sample_kernel + tree_select_kernel")
     res["note"] = (f"not in the round's metric; B={B} V={V} D={D} k={k} m={m}; the stepwise build is "
                    f"{2 * D} launches with no draft model between them; draft rows L2-warm across calls")
     return res
@@ -556,6 +574,62 @@ def _traffic(attn_bytes: float):
 
 
 # ----------------------------------------------------------------------------------- CPU oracle
+
+def side_cpu_baselines(wl, seed: int) -> dict:
+    """The fp64 oracle on the separately timed calls' shapes (one call each, on the host cores),
+    beside their GPU timings: the KV commit, tree attention at the draft shape (the largest n),
+    the static chain and the sampled-children build."""
+    import numpy as np
+
+    import oracle
+
+    nthreads = os.cpu_count() or 1
+    out = {}
+    oracle.build()  # compiled outside the timings
+
+    def timed(fn):  # the second of two calls (the first touches fresh pages and caches)
+        fn()
+        t0 = time.perf_counter()
+        fn()
+        return (time.perf_counter() - t0) * 1e6
+
+    def entry(us, sample):
+        return {"us": us, "unit": "us per call", "cores": nthreads, "kind": "oracle", "sample": sample}
+
+    # KV commit: L layers, one sequence, the round's tree, three committed rows
+    L, n, Hkv, d, D = wl.layers, wl.nodes, wl.heads_kv, wl.head_dim, wl.depth
+    S = wl.ctx + D + 8
+    g = np.random.default_rng(seed)
+    kt = g.integers(0, 1 << 16, (L, 1, n, Hkv, d), dtype=np.uint16)
+    vt = g.integers(0, 1 << 16, (L, 1, n, Hkv, d), dtype=np.uint16)
+    kc = np.zeros((L, 1, S, Hkv, d), np.uint16)
+    path = np.full((1, D), -1, np.int32)
+    path[0, :2] = [1, 2]
+    us = timed(lambda: oracle.kv_commit(kt, vt, path, np.array([3], np.int32), np.array([wl.ctx], np.int32), kc, kc))
+    out["kv_commit"] = entry(us, f"L={L} B=1 n={n} rows=3, bf16 bytes copied")
+    # tree attention at the draft shape, the largest tree a draft step sees
+    nd = max(x for x in (1 + wl.topk, 1 + 3 * wl.topk, 1 + 6 * wl.topk) if x <= 64)
+    one = wl.with_(layers=1, batch=1, keep=nd - 1)
+    inp = datagen.attention_inputs(one, seed)
+    mask = np.array([[[(1 << (i + 1)) - 1] for i in range(nd)]], np.uint64)
+    arrs = [datagen.to_numpy(inp[k]) for k in ("q", "k_cache", "v_cache")]
+    ctx = np.array([wl.ctx], np.int32)
+    kt2, vt2 = datagen.to_numpy(inp["k_tree"]), datagen.to_numpy(inp["v_tree"])
+    us = timed(lambda: oracle.tree_attention(*arrs, ctx, kt2, vt2, mask, nthreads=nthreads))
+    out["draft_attention"] = entry(us, f"L=1 B=1 n={nd} Hq={wl.heads_q} Hkv={wl.heads_kv} d={wl.head_dim} "
+                                       f"ctx={wl.ctx}, fp64 literal softmax")
+    # static chain of the workload's depth
+    x = datagen.draft_logits(1, D, wl.vocab, seed).numpy()
+    us = timed(lambda: oracle.build_static_tree(x, np.zeros(1, np.int32), [-1] + list(range(D))))
+    out["static_tree"] = entry(us, f"chain of {D}, B=1 V={wl.vocab}")
+    # sampled-children build at the workload's shape (one sequence)
+    R = 1 + (D - 1) * wl.topk
+    x = datagen.draft_logits(1, R, wl.vocab, seed).numpy()
+    cu = datagen.child_uniforms(1, R, wl.topk, seed).numpy()
+    us = timed(lambda: oracle.build_tree(x, np.zeros(1, np.int32), D, wl.topk, wl.keep, child_u=cu))
+    out["sampled_build"] = entry(us, f"B=1 V={wl.vocab} D={D} k={wl.topk} m={wl.keep}, one sequence")
+    return out
+
 
 class OracleRound:
     """The fp64 oracle on one round of a workload, split into timeable items: the build of every
@@ -699,6 +773,9 @@ def main():
         wl = datagen.WORKLOADS[args.workload]
         if world == 1 and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(wl, args.seed)
+            for key, val in side_cpu_baselines(wl, args.seed).items():
+                if isinstance(res.get(key), dict):
+                    res[key]["cpu_baseline"] = val
         else:
             res["cpu_baseline"] = None
         print(json.dumps(res), flush=True)

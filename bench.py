@@ -57,6 +57,20 @@ def _side_roofline(nbytes: float, us: float, what: str) -> dict:
             "peak_source": f"{pk['source']} hbm_gbs (MEASURED_PEAKS.json)"}
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: a job of N replicas is done when its last replica is."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(steps_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job rounds/s: every rank's rounds over the slowest rank's time (weak scaling)."""
+    return world * steps_per_rank / (ms_max * 1e-3)
+
+
 def _workload_desc(wl) -> str:
     ctx = f"ctx={wl.ctx}" if wl.ctx_min == wl.ctx else f"ctx=U[{wl.ctx_min},{wl.ctx}]"
     return (f"{wl.name}: B={wl.batch} V={wl.vocab} D={wl.depth} k={wl.topk} m={wl.keep} L={wl.layers} "
@@ -233,10 +247,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
     ms = e0.elapsed_time(e1)
     attn_ms = statistics.mean(attn_ev[i][0].elapsed_time(attn_ev[i][1]) for i in sampled)
     gpu_launches = launches[0]
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     if ws.status(stream) != 0:
         raise RuntimeError("device status not OK after the timed steps")
 
@@ -258,7 +269,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
     peaks = _peaks()
     attn_bytes = bytes_["attention"]
     achieved = attn_bytes / (attn_ms * 1e-3) / 1e9
-    value = world * K / (ms * 1e-3)
+    value = job_rate(K, world, ms)
     metric_bytes = bytes_["metric"]
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -355,12 +366,8 @@ def run_e2e(eg, lib, wl, rd: Round, outs, ws, stream, dev, steps, world) -> dict
         one()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": world * steps / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    return {"value": job_rate(steps, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "pipeline": "inputs copied on a second stream in the order the calls need them; two device "
                         "input sets alternate between rounds"}

@@ -6,17 +6,21 @@
 // every candidate, shallower first on equal V, so the kept set is still a connected tree) and
 // "Tree Attention Mask" (flattened sequence, ancestors-only visibility).
 //
-// Two kernels:
+// Kernels:
 //   row_topk_kernel    one HBM pass over every draft row.  A row is cut into `splits` slices
 //                      handled by the CTAs of one thread-block cluster; each CTA keeps an online
-//                      log-sum-exp of x/T and a top-KMAX list (per-warp sorted lists that only
-//                      see values above a block-shared threshold), then rank 0 merges the
-//                      cluster's lists and sums through distributed shared memory and writes the
-//                      row's k children (token, fp64 log-confidence).
+//                      log-sum-exp of x/T and a top-16 list (per-warp sorted lists that only see
+//                      values above a block-shared threshold), then rank 0 merges the cluster's
+//                      lists and sums through distributed shared memory and writes the row's k
+//                      children (token, fp64 log-confidence).  With sampled children the rows go
+//                      to row_sample_kernel (sample_children.cu) instead, same outputs.
 //   tree_select_kernel one CTA per sequence: per-depth frontier selection (rank of a 64-bit
 //                      composite key), expansion, the global rerank (a key's rank within its
 //                      depth plus binary searches in the other depths' sorted lists), flatten,
-//                      masks.
+//                      masks.  The stepwise build runs it per depth (frontier only) and once more
+//                      to finalize, replaying the stored frontiers.
+//   static_tree_kernel the static (EAGLE-1) tree or chain of a caller's template over the rows'
+//                      children (see the section below).
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>

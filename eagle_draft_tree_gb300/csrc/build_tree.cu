@@ -17,8 +17,8 @@
 //   tree_select_kernel one CTA per sequence: per-depth frontier selection (rank of a 64-bit
 //                      composite key), expansion, the global rerank (a key's rank within its
 //                      depth plus binary searches in the other depths' sorted lists), flatten,
-//                      masks.  The stepwise build runs it per depth (frontier only) and once more
-//                      to finalize, replaying the stored frontiers.
+//                      masks.  A stepwise build runs it once, to finalize, replaying the frontiers
+//                      tree_step_kernel chose one depth at a time.
 //   static_tree_kernel the static (EAGLE-1) tree or chain of a caller's template over the rows'
 //                      children (see the section below).
 #include <cooperative_groups.h>
@@ -292,15 +292,10 @@ struct SelectArgs {
     float *node_logv;
     int32_t *status;
     int V, D, k, m, R;
-    // Stepwise builds.  The pool is grown to depth `hi` (rows 0 .. 1 + (hi-1)k - 1 are read);
-    // the frontier of a depth below `read_below` is taken from `slots` (pool index of slot s of
-    // depth f at [b][f][s]), the others are ranked, and stored there when `slots` is set.  When
-    // hi <= D - 1 the frontier of depth hi goes to front_tok / front_par [B][k] (token, parent's
-    // slot at depth hi - 1 or -1) and nothing else is written; `finalize` runs the rerank,
-    // flatten and outputs (hi == D).
-    int32_t *slots;
-    int32_t *front_tok, *front_par;
-    int hi, read_below, finalize;
+    // The finalize stage of a stepwise build: the frontier of every depth comes from `slots`
+    // (pool index of slot s of depth f at [b][f][s], as the step kernel stored it) instead of
+    // being ranked again.  nullptr in the one-call build.
+    const int32_t *slots;
 };
 
 __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) {
@@ -332,7 +327,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     const int k = a.k, R = a.R, D = a.D, m = a.m;
 
     // the rows' children (written by the row kernel): every load in flight before the first store
-    const int nload = (1 + (a.hi - 1) * k) * k;
+    const int nload = R * k;
     {
         constexpr int kPer = kMaxPool / kSelThreads;
         double lcv[kPer];
@@ -369,8 +364,8 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     // Rank of each candidate of one depth within the depth (keys are unique): two adjacent
     // threads per candidate, each counting the keys above it in one half of the depth (the loop
     // is warp-uniform).  The rank goes to s_flat (free until the flatten); with `frontier`, the k
-    // best are the depth's frontier (slot = rank) and go to s_slot and, if set, slots_f.
-    auto rank_depth = [&](int lb, int cnt, int f, int32_t *slots_f, bool frontier) {
+    // best are the depth's frontier (slot = rank) and go to s_slot.
+    auto rank_depth = [&](int lb, int cnt, int f, bool frontier) {
         for (int base = 0, half = (cnt + 1) >> 1; base < cnt; base += kSelThreads / 2) {
             const int ei = base + (tid >> 1);
             const bool act = ei < cnt;
@@ -393,7 +388,6 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
                 if (frontier && rank < k) {
                     s_slot[rank] = e;
                     s_row[e] = 1 + (f - 1) * k + rank;
-                    if (slots_f) slots_f[rank] = e;
                 }
             }
         }
@@ -402,13 +396,13 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     // depths 2..D: the k best nodes of the previous depth are expanded; frontier slot = rank
     int lb = 0, cnt = k, np = k;
     uint64_t ranked = 0;  // depths whose candidates were ranked here (the same in every thread)
-    for (int f = 1; f <= D - 1 && f <= a.hi; ++f) {
+    for (int f = 1; f <= D - 1; ++f) {
         if (tid == 0) {
             s_dlb[f] = lb;
             s_dcnt[f] = cnt;
         }
-        int32_t *slots_f = a.slots ? a.slots + (size_t(b) * D + f) * k : nullptr;
-        if (f < a.read_below) {
+        if (a.slots) {
+            const int32_t *slots_f = a.slots + (size_t(b) * D + f) * k;
             // the frontier chosen by an earlier call; an index outside this depth's candidates
             // (a stale or foreign state) is flagged and replaced by the rank order's slot
             for (int s = tid; s < k; s += kSelThreads) {
@@ -421,18 +415,10 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
                 s_row[e] = 1 + (f - 1) * k + s;
             }
         } else {
-            rank_depth(lb, cnt, f, slots_f, true);
+            rank_depth(lb, cnt, f, true);
             ranked |= 1ull << f;
         }
         __syncthreads();
-        if (f == a.hi) {  // a stepwise call: this depth's frontier is the output
-            for (int s = tid; s < k; s += kSelThreads) {
-                const int e = s_slot[s];
-                a.front_tok[size_t(b) * k + s] = s_ptok[e];
-                a.front_par[size_t(b) * k + s] = f == 1 ? -1 : (e - lb) / k;
-            }
-            break;
-        }
         const int nf = cnt < k ? cnt : k;
         for (int i = tid; i < nf * k; i += kSelThreads) {
             const int sl = i / k, ch = i % k;
@@ -452,7 +438,6 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         cnt = nf * k;
         np += nf * k;
     }
-    if (!a.finalize) return;
 
     // rerank: keep the m largest keys of the pool (keys are unique).  A key's rank in the pool is
     // its rank within its depth plus, for every other depth, the number of that depth's keys
@@ -465,7 +450,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     }
     __syncthreads();
     for (int d = 1; d <= D; ++d)  // depths not ranked above (the last; frontiers read from slots)
-        if (d == 64 || !((ranked >> d) & 1ull)) rank_depth(s_dlb[d], s_dcnt[d], d, nullptr, false);
+        if (d == 64 || !((ranked >> d) & 1ull)) rank_depth(s_dlb[d], s_dcnt[d], d, false);
     if (tid == 0) {
         int off = 0;
         for (int d = 1; d <= D; ++d) {
@@ -571,6 +556,73 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         node_row[i] = s_row[e];
         mask[i] = bits;
         if (a.node_logv) a.node_logv[size_t(b) * n + i] = float(s_logv[e]);
+    }
+}
+
+// ---- stepwise build: one depth's frontier --------------------------------------------------
+// The candidates of depth hi are the root's children (hi = 1: row 0) or the children of the
+// depth hi - 1 frontier that the previous step stored (its pool indices and log V in the
+// workspace; slot s read row 1 + (hi - 2)k + s).  Their keys are the select kernel's: log V =
+// the parent's log V + the child's log-confidence, creation index = the depth's pool offset
+// (0 at depth 1, k + (d - 2)k^2 at depth d >= 2) + slot * k + child.  The k best are ranked by
+// counting, stored (pool index, log V) for the next step and for the finalize replay, and
+// returned (token, parent slot).
+constexpr int kStepThreads = 256;
+constexpr int kStepMax = 256;  // k^2 candidates, k <= 16
+
+struct StepArgs {
+    const int32_t *row_tok;  // [B][R][k]
+    const double *row_lc;    // [B][R][k]
+    int32_t *slots;          // [B][D][k] pool index of each frontier slot
+    double *flogv;           // [B][D][k] log V of each frontier slot
+    int32_t *front_tok, *front_par;  // [B][k]
+    int D, k, R, hi;
+};
+
+__global__ void __launch_bounds__(kStepThreads) tree_step_kernel(StepArgs a) {
+    pdl_wait();
+    pdl_launch_next();
+    __shared__ uint64_t s_key[kStepMax];
+    __shared__ double s_lv[kStepMax];
+    __shared__ int s_tok[kStepMax];
+    const int b = blockIdx.x, tid = threadIdx.x, k = a.k, hi = a.hi, D = a.D;
+    const int cnt = hi == 1 ? k : k * k;
+    const int lb = hi == 1 ? 0 : k + (hi - 2) * k * k;
+    const int r0 = hi == 1 ? 0 : 1 + (hi - 2) * k;
+    for (int i = tid; i < cnt; i += kStepThreads) {
+        const int sl = hi == 1 ? 0 : i / k, ch = hi == 1 ? i : i % k;
+        const size_t o = (size_t(b) * a.R + r0 + sl) * k + ch;
+        const double lc = a.row_lc[o];
+        const double lv = hi == 1 ? lc : a.flogv[(size_t(b) * D + hi - 1) * k + sl] + lc;
+        s_lv[i] = lv;
+        s_key[i] = pool_key(lv, lb + i);
+        s_tok[i] = a.row_tok[o];
+    }
+    __syncthreads();
+    // rank by counting: two adjacent threads per candidate, each over one half
+    for (int base = 0, half = (cnt + 1) >> 1; base < cnt; base += kStepThreads / 2) {
+        const int i = base + (tid >> 1);
+        const bool act = i < cnt;
+        const uint64_t v = act ? s_key[i] : ~0ull;
+        const int o0 = (tid & 1) * half, o1 = min(o0 + half, cnt);
+        int r0c = 0, r1c = 0, r2c = 0, r3c = 0;
+        int o = o0;
+        for (; o + 4 <= o1; o += 4) {
+            r0c += s_key[o] > v;
+            r1c += s_key[o + 1] > v;
+            r2c += s_key[o + 2] > v;
+            r3c += s_key[o + 3] > v;
+        }
+        for (; o < o1; ++o) r0c += s_key[o] > v;
+        const int part = (r0c + r1c) + (r2c + r3c);
+        const int rank = part + __shfl_xor_sync(0xffffffffu, part, 1);
+        if (act && !(tid & 1) && rank < k) {
+            const size_t so = (size_t(b) * D + hi) * k + rank;
+            a.slots[so] = lb + i;
+            a.flogv[so] = s_lv[i];
+            a.front_tok[size_t(b) * k + rank] = s_tok[i];
+            a.front_par[size_t(b) * k + rank] = hi == 1 ? -1 : i / k;
+        }
     }
 }
 
@@ -684,7 +736,7 @@ eagle_status row_children_launch(const float *draft, const float *u, int B, int 
 // (the frontier of every depth, kept between the calls of a stepwise build).
 struct BuildWs {
     int32_t *status, *row_tok, *slots;
-    double *row_lc;
+    double *row_lc, *flogv;
 };
 BuildWs build_ws(const eagle_tree_cfg &c, void *ws) {
     unsigned char *w = static_cast<unsigned char *>(ws);
@@ -693,15 +745,17 @@ BuildWs build_ws(const eagle_tree_cfg &c, void *ws) {
     r.status = reinterpret_cast<int32_t *>(w);
     r.row_tok = reinterpret_cast<int32_t *>(w + kWsHeader);
     r.row_lc = reinterpret_cast<double *>(w + kWsHeader + align_up(ent * 4, 256));
+    const size_t sl = size_t(c.batch) * c.depth * c.topk;
     r.slots = reinterpret_cast<int32_t *>(w + kWsHeader + align_up(ent * 4, 256) + align_up(ent * 8, 256));
+    r.flogv = reinterpret_cast<double *>(reinterpret_cast<unsigned char *>(r.slots) + align_up(sl * 4, 256));
     return r;
 }
 
-// The select kernel over the rows' children in the workspace (see SelectArgs for the stages).
+// The select kernel over the rows' children in the workspace; with `replay`, the frontiers the
+// step kernel stored.
 eagle_status select_launch(const eagle_tree_cfg &c, const BuildWs &w, const int32_t *root, int32_t *tokens,
                            int32_t *parents, int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv,
-                           int hi, int read_below, bool finalize, bool store_slots, int32_t *front_tok,
-                           int32_t *front_par, cudaStream_t stream) {
+                           bool replay, cudaStream_t stream) {
     SelectArgs sa;
     sa.row_tok = w.row_tok;
     sa.row_lc = w.row_lc;
@@ -718,12 +772,7 @@ eagle_status select_launch(const eagle_tree_cfg &c, const BuildWs &w, const int3
     sa.k = c.topk;
     sa.m = c.keep;
     sa.R = 1 + (c.depth - 1) * c.topk;
-    sa.slots = store_slots || read_below > 1 ? w.slots : nullptr;
-    sa.front_tok = front_tok;
-    sa.front_par = front_par;
-    sa.hi = hi;
-    sa.read_below = read_below;
-    sa.finalize = finalize ? 1 : 0;
+    sa.slots = replay ? w.slots : nullptr;
     if (launch_pdl(tree_select_kernel, dim3(c.batch), dim3(kSelThreads), 0, stream, 1u, sa) != cudaSuccess)
         return EAGLE_ERR_CUDA;
     note_launch();
@@ -783,8 +832,9 @@ eagle_status build_static_tree_launch(const eagle_static_tree_cfg &c, int R, int
 
 size_t build_tree_workspace_bytes(const eagle_tree_cfg &c) {
     const size_t ent = size_t(c.batch) * (1 + (c.depth - 1) * c.topk) * c.topk;
-    return kWsHeader + align_up(ent * 4, 256) + align_up(ent * 8, 256) +
-           align_up(size_t(c.batch) * c.depth * c.topk * 4, 256);
+    const size_t sl = size_t(c.batch) * c.depth * c.topk;
+    return kWsHeader + align_up(ent * 4, 256) + align_up(ent * 8, 256) + align_up(sl * 4, 256) +
+           align_up(sl * 8, 256);
 }
 
 // The whole build in one call: every row's children (top k, or draws when child_u is set), then
@@ -797,14 +847,13 @@ eagle_status build_tree_launch(const eagle_tree_cfg &c, const float *draft, cons
     if (eagle_status e = row_children_launch(draft, child_u, c.batch, R, c.vocab, c.topk, c.tree_temp, w.row_tok,
                                              w.row_lc, R, 0, w.status, stream))
         return e;
-    return select_launch(c, w, root, tokens, parents, depths, node_row, mask, node_logv, c.depth, 1, true, false,
-                         nullptr, nullptr, stream);
+    return select_launch(c, w, root, tokens, parents, depths, node_row, mask, node_logv, false, stream);
 }
 
 // Stepwise build, stage f (0 = begin: the root's row; f >= 1: the rows of the depth-f frontier).
 // The rows' children go to rows 1 + (f-1)k .. of the workspace (row 0 for the root); then, while
-// a deeper frontier is still to be expanded (f + 1 <= D - 1), the select kernel replays the
-// stored frontiers of depths 1..f, ranks depth f + 1 and writes that frontier.
+// a deeper frontier is still to be expanded (f + 1 <= D - 1), the step kernel ranks depth f + 1
+// from the stored depth-f frontier and writes the new frontier.
 eagle_status build_step_launch(const eagle_tree_cfg &c, int f, const float *rows, const float *child_u,
                                int32_t *front_tok, int32_t *front_par, void *ws, cudaStream_t stream) {
     const BuildWs w = build_ws(c, ws);
@@ -815,8 +864,21 @@ eagle_status build_step_launch(const eagle_tree_cfg &c, int f, const float *rows
                                              w.row_lc, R, r0, w.status, stream))
         return e;
     if (f + 1 > c.depth - 1) return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
-    return select_launch(c, w, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, f + 1, f + 1, false,
-                         true, front_tok, front_par, stream);
+    StepArgs sa;
+    sa.row_tok = w.row_tok;
+    sa.row_lc = w.row_lc;
+    sa.slots = w.slots;
+    sa.flogv = w.flogv;
+    sa.front_tok = front_tok;
+    sa.front_par = front_par;
+    sa.D = c.depth;
+    sa.k = c.topk;
+    sa.R = R;
+    sa.hi = f + 1;
+    if (launch_pdl(tree_step_kernel, dim3(c.batch), dim3(kStepThreads), 0, stream, 1u, sa) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
+    note_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
 
 // Stepwise build, last stage: the select kernel over the stored rows and frontiers.
@@ -824,8 +886,7 @@ eagle_status build_finalize_launch(const eagle_tree_cfg &c, const int32_t *root,
                                    int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
                                    cudaStream_t stream) {
     const BuildWs w = build_ws(c, ws);
-    return select_launch(c, w, root, tokens, parents, depths, node_row, mask, node_logv, c.depth, c.depth, true, false,
-                         nullptr, nullptr, stream);
+    return select_launch(c, w, root, tokens, parents, depths, node_row, mask, node_logv, true, stream);
 }
 
 }  // namespace eagle

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
             double lse = 0.0;
-            if (lane == 0) lse = double(M) * a.inv_t + log(S);
+            if (lane == 0) lse = double(M) * a.inv_t + ln_pos(S);  // S >= 1: the maximum's own term
             lse = __shfl_sync(0xffffffffu, lse, 0);
             if (lane < a.k) {
                 const size_t o = (size_t(b) * a.out_R + a.out_r0 + r) * a.k + lane;

@@ -126,6 +126,19 @@ __device__ __forceinline__ uint64_t scale_fx(uint64_t total, float u) {
     return (hi << (64 - sh)) | (lo >> sh);
 }
 
+// ln x for a positive finite double without the double-precision log (on GB300 the FP64 pipe is
+// narrow and a double log costs microseconds of latency): x = f 2^e with f in [1, 2) taken from
+// the bits, ln x = e ln 2 + ln f, with ln f in single precision plus the first-order correction
+// for f's rounding to float (absolute error about 6e-8).  For arguments that are themselves sums
+// of single-precision terms.
+__device__ __forceinline__ double ln_pos(double x) {
+    const unsigned long long bits = static_cast<unsigned long long>(__double_as_longlong(x));
+    const int e = int((bits >> 52) & 0x7ffull) - 1023;
+    const double f = __longlong_as_double(static_cast<long long>((bits & 0xfffffffffffffull) | 0x3ff0000000000000ull));
+    const float hi = float(f);
+    return double(e) * 0.69314718055994530942 + double(logf(hi)) + (f - double(hi)) * double(1.f / hi);
+}
+
 // ---- mbarrier + bulk copy (global -> own shared memory), with bounded waits ----
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(bar));

@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kSmpThreads) row_sample_kernel(SampleArgs a) {
                                       : (w[3] > 0.f && a3 > rr) ? 3
                                                                 : lastp;
                         const int tok = min(lo + 4 * q + i, hi - 1);  // in range even on a fallback
-                        const double lse = double(M) * a.inv_t + (log(double(total)) - kLn2_40);
+                        const double lse = double(M) * a.inv_t + (ln_pos(double(total)) - kLn2_40);
                         a.row_tok[o] = tok;
                         a.row_lc[o] = double(__ldg(row + tok)) * a.inv_t - lse;
                     }

@@ -211,6 +211,25 @@ def test_stepwise_equals_one_call_and_reports_the_frontiers(B, V, D, k, m, sampl
         assert np.array_equal(ft[ok], o["front_tok"][ok, f]) and np.array_equal(fp[ok], o["front_par"][ok, f])
 
 
+@pytest.mark.parametrize("sampled", [False, True])
+def test_stepwise_at_the_serving_batch(sampled):
+    """The serving workload's shape (B = 64, V = 128256, D = 8, k = 10, m = 60): the stepwise build
+    equals the one-call build bit for bit; trees are valid; equal to the oracle away from the
+    excuse bands."""
+    B, V, D, k, m = 64, 128256, 8, 10, 60
+    draft, cu, root = _inputs(B, V, D, k, 64)
+    cu = cu if sampled else None
+    whole = eg.build_tree(draft, root, D, k, m, 1.0, child_u=cu)
+    steps, fronts, st = _stepwise(draft, cu, root, D, k, m, 1.0)
+    assert st.ws.status() == eg.EAGLE_OK
+    for key in ("tokens", "parents", "depths", "node_row", "mask", "node_logv"):
+        assert torch.equal(whole[key], steps[key]), key
+    _valid_tree(steps, B, V)
+    o = oracle.build_tree(np_(draft), np_(root), D, k, m, 1.0, child_u=None if cu is None else np_(cu))
+    excused = _compare(steps, o, bounded=not sampled)
+    assert excused < B  # some trees compare exactly
+
+
 def test_finalize_on_a_fresh_state_is_flagged():
     B, V, D, k, m = 2, 500, 3, 3, 9
     root = datagen.root_tokens(B, V, 1, DEV)

@@ -10,7 +10,9 @@ k children are sampled from the draft distribution).
   target distribution (chi-square), for a static tree and for a dynamic tree whose draft rows
   are chosen by the depth-1 frontier the build reports (the interleaving a real draft model
   does); with top-k children the same test fails (the test has power);
-- the frontier outputs agree with the tree (tokens of the expanded nodes, parent slots).
+- the frontier outputs agree with the tree (tokens of the expanded nodes, parent slots);
+- children drawn at the verify temperature stay lossless at T = 0.7, and drawing them at another
+  temperature fails the same test.
 """
 import json
 import os
@@ -233,3 +235,35 @@ def test_row_children_are_the_builds_children():
             assert np.array_equal(rc["tok"], b["tokens"][:, 1:])
             assert np.array_equal(rc["gap"].min(1), b["draw_gap"])
         assert np.allclose(rc["lc"], b["node_logv"][:, 1:], rtol=0, atol=0)
+
+
+def _temperature_trial_pvalue(tree_temp, verify_temp, trials=200_000, seed=33):
+    """Static root tree (k = 3) built at tree_temp, verified at verify_temp: the first committed
+    token against the target distribution at verify_temp."""
+    V, k = 16, 3
+    rng = np.random.default_rng(seed)
+    p, q = _dists(rng, V)
+    p2 = rng.dirichlet(np.ones(V), size=V)
+    B = trials
+    dft = np.broadcast_to(_logits(q), (B, 1, V)).copy()
+    t = oracle.build_static_tree(dft, np.zeros(B, np.int32), [-1, 0, 0, 0], tree_temp,
+                                 child_u=rng.random((B, 1, k), dtype=np.float32))
+    tgt = np.empty((B, k + 1, V), np.float32)
+    tgt[:, 0] = _logits(p)
+    tgt[:, 1:] = _logits(p2)[t["tokens"][:, 1:]]
+    o = oracle.tree_verify(tgt, dft, t["tokens"], t["parents"], t["node_row"],
+                           rng.random((B, k + 1), dtype=np.float32), verify_temp, 2)
+    pe = softmax(_logits(p).astype(np.float64) / verify_temp)
+    obs = np.bincount(o["out_tokens"][:, 0], minlength=V)
+    return chisquare(obs, pe * obs.sum()).pvalue
+
+
+def test_sampled_children_at_the_verify_temperature_are_lossless():
+    """Children drawn at the temperature the verification uses for q: the committed token follows
+    the target at that temperature ([hubwiz] section 2: both distributions are tempered)."""
+    assert _temperature_trial_pvalue(0.7, 0.7) > 1e-3
+
+
+def test_children_drawn_at_another_temperature_are_not():
+    """The control: children drawn from q at T = 2 but tested as if drawn at T = 0.7."""
+    assert _temperature_trial_pvalue(2.0, 0.7) < 1e-6

@@ -469,20 +469,23 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         const int d = s_dep[e];
         const uint64_t v = s_key[e];
         int g = s_flat[e];
-        // two depths' searches at a time, so that their shared-memory loads overlap
-        for (int d2 = 1; d2 <= D && g < m; d2 += 2) {
-            const int d3 = d2 + 1;
-            const int la = d2 == d ? 0 : min(s_dcnt[d2], m);
-            const int lb2 = (d3 > D || d3 == d) ? 0 : min(s_dcnt[d3], m);
-            const uint64_t *A = s_u.sorted + s_doff[d2];
-            const uint64_t *Bl = s_u.sorted + s_doff[d3 <= D ? d3 : D + 1];
-            int pa = 0, pb = 0;  // keys above v in each list (lists are descending, m <= 63)
+        // four depths' searches at a time, so that their shared-memory loads overlap (a depth past
+        // D, or the key's own depth, contributes an empty list)
+        for (int d2 = 1; d2 <= D && g < m; d2 += 4) {
+            int len[4], pos[4] = {0, 0, 0, 0};
+            const uint64_t *lst[4];
 #pragma unroll
-            for (int step = 32; step > 0; step >>= 1) {
-                if (pa + step <= la && A[pa + step - 1] > v) pa += step;
-                if (pb + step <= lb2 && Bl[pb + step - 1] > v) pb += step;
+            for (int u = 0; u < 4; ++u) {
+                const int dd = d2 + u;
+                len[u] = (dd > D || dd == d) ? 0 : min(s_dcnt[dd], m);
+                lst[u] = s_u.sorted + s_doff[dd <= D ? dd : D + 1];
             }
-            g += pa + pb;
+#pragma unroll
+            for (int step = 32; step > 0; step >>= 1)  // lists are descending, m <= 63
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (pos[u] + step <= len[u] && lst[u][pos[u] + step - 1] > v) pos[u] += step;
+            g += (pos[0] + pos[1]) + (pos[2] + pos[3]);
         }
         s_v.kept[e] = g < m;
     }

@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(kSmpThreads) row_sample_kernel(SampleArgs a) {
         if (s < rank) excl += t;
         total += t;
     }
-    // the peers may leave once every CTA has read the totals; the draws touch local memory only
+    // the peers may leave once every CTA has read the totals: the draws read only this CTA's own
+    // shared memory and global memory
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     const uint64_t mine = s_tot;
 

@@ -71,3 +71,17 @@ def test_reference_arm_runs_on_rank_zero_only():
     line = json.loads(r0.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_side_call_cpu_baselines_cover_every_side_call():
+    """The benchmark's oracle timings beside its separately timed calls (tiny workload, CPU)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import datagen
+
+    res = bench.side_cpu_baselines(datagen.WORKLOADS["tiny_f32"], 1)
+    assert set(res) == {"kv_commit", "draft_attention", "static_tree", "sampled_build"}
+    for v in res.values():
+        assert v["kind"] == "oracle" and v["us"] > 0 and v["cores"] >= 1 and v["sample"]
+    rl = bench._side_roofline(1e6, 10.0, "x")
+    assert rl["bound"] == "hbm" and abs(rl["achieved"] - 100.0) < 1e-9 and rl["frac"] == rl["achieved"] / rl["peak"]

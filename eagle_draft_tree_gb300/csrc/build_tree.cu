@@ -10,14 +10,15 @@
 //   row_topk_kernel    one HBM pass over every draft row.  A row is cut into `splits` slices
 //                      handled by the CTAs of one thread-block cluster; each CTA keeps an online
 //                      log-sum-exp of x/T and a top-16 list (per-warp sorted lists that only see
-//                      values above a block-shared threshold), then rank 0 merges the cluster's
-//                      lists and sums through distributed shared memory and writes the row's k
-//                      children (token, fp64 log-confidence).  With sampled children the rows go
+//                      values above a block-shared threshold), pushes both into rank 0's shared
+//                      memory, and rank 0 merges them after one cluster barrier and writes the
+//                      row's k children (token, fp64 log-confidence).  With sampled children the rows go
 //                      to row_sample_kernel (sample_children.cu) instead, same outputs.
 //   tree_select_kernel one CTA per sequence: per-depth frontier selection (rank of a 64-bit
-//                      composite key), expansion, the global rerank (a key's rank within its
-//                      depth plus binary searches in the other depths' sorted lists), flatten,
-//                      masks.  A stepwise build runs it once, to finalize, replaying the frontiers
+//                      composite key within its depth by counting, a group of threads per
+//                      candidate), the frontier's expansion, the global rerank (a key's rank
+//                      within its depth plus binary searches in the other depths' sorted lists),
+//                      flatten, masks.  A stepwise build runs it once, to finalize, replaying the frontiers
 //                      tree_step_kernel chose one depth at a time.
 //   static_tree_kernel the static (EAGLE-1) tree or chain of a caller's template over the rows'
 //                      children (see the section below).
@@ -42,9 +43,9 @@ namespace {
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kRowVals = 16;  // values per thread per batch (4 float4 in registers)
-constexpr int kSelThreads = 256;
+constexpr int kSelThreads = 512;
 constexpr int kMaxPool = 1024;
-constexpr int kMaxDepth = 64;
+constexpr int kMaxSelDepth = 65;  // depths 1 .. 64
 constexpr int kMaxSplits = 8;  // portable cluster size
 
 // Merge (m_a, s_a) and (m_b, s_b) where s = sum 2^((x - m) c).
@@ -110,8 +111,8 @@ __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
     __shared__ uint64_t s_lists[2][kRowWarps][16];
     __shared__ unsigned long long s_bound;  // CTA-wide lower bound of the slice's 16th key
     __shared__ float2 s_ms[kRowWarps];
-    __shared__ uint64_t s_blk[16];  // this CTA's list, read by the cluster's rank 0
-    __shared__ float2 s_blkms;
+    __shared__ uint64_t s_recv[kMaxSplits][16];  // rank 0: every slice's list, pushed by its CTA
+    __shared__ float2 s_recvms[kMaxSplits];      // rank 0: every slice's (max, scaled sum)
 
     cg::cluster_group cluster = cg::this_cluster();
     const int split = int(cluster.block_rank());
@@ -234,7 +235,9 @@ __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
     if (lane < 16) s_lists[0][warp][lane] = top.key;
     __syncthreads();
     const int cur = tree_merge16(s_lists, kRowWarps);
-    if (tid < 16) s_blk[tid] = s_lists[cur][0][tid];
+    // this CTA's list and (max, sum) go to rank 0's receive slots (rank 0's own by local stores);
+    // the cluster barrier (release / acquire) then makes them visible there.  Nothing of a
+    // slice's own shared memory is read by another CTA, so the slices leave after the barrier.
     if (warp == 0) {
         float mm = lane < kRowWarps ? s_ms[lane].x : -INFINITY;
         float ss = lane < kRowWarps ? s_ms[lane].y : 0.f;
@@ -244,37 +247,32 @@ __global__ void __launch_bounds__(kRowThreads) row_topk_kernel(RowArgs a) {
             float so = __shfl_xor_sync(0xffffffffu, ss, off);
             ms_merge(mm, ss, mo, so, c);
         }
-        if (lane == 0) s_blkms = make_float2(mm, ss);
+        if (lane < 16) cluster.map_shared_rank(&s_recv[split][0], 0)[lane] = s_lists[cur][0][lane];
+        if (lane == 0) *cluster.map_shared_rank(&s_recvms[split], 0) = make_float2(mm, ss);
     }
     cluster.sync();
+    if (split != 0 || warp != 0) return;
 
-    // cluster rank 0: merge the slices' lists and sums, write the row's children
-    if (split == 0) {
-        for (int t = tid; t < splits * 16; t += kRowThreads)
-            s_lists[0][t / 16][t % 16] = cluster.map_shared_rank(&s_blk[0], t / 16)[t % 16];
-        __syncthreads();
-        const int cur2 = tree_merge16(s_lists, splits);
-        if (warp == 0) {
-            float2 ms = make_float2(-INFINITY, 0.f);
-            if (lane < splits) ms = *cluster.map_shared_rank(&s_blkms, lane);
-            float M = ms.x;
+    // cluster rank 0, one warp: merge the slices' lists (lanes 0..15 carry the running top 16,
+    // lanes 16..31 the next slice's list reversed: a bitonic sequence for the merge network) and
+    // sums, write the row's children
+    uint64_t run = lane < 16 ? s_recv[0][lane] : 0ull;
+    for (int j = 1; j < splits; ++j) run = warp_bitonic_merge32(lane < 16 ? run : s_recv[j][31 - lane]);
+    const float2 ms = lane < splits ? s_recvms[lane] : make_float2(-INFINITY, 0.f);
+    float M = ms.x;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            double S = ms.x == -INFINITY ? 0.0 : double(ms.y) * double(exp2f((ms.x - M) * c));
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    double S = ms.x == -INFINITY ? 0.0 : double(ms.y) * double(exp2f((ms.x - M) * c));
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
-            double lse = 0.0;
-            if (lane == 0) lse = double(M) * a.inv_t + ln_pos(S);  // S >= 1: the maximum's own term
-            lse = __shfl_sync(0xffffffffu, lse, 0);
-            if (lane < a.k) {
-                const size_t o = (size_t(b) * a.out_R + a.out_r0 + r) * a.k + lane;
-                const uint64_t key = s_lists[cur2][0][lane];
-                a.row_tok[o] = int32_t(topk_key_token(key));
-                a.row_lc[o] = double(topk_key_value(key)) * a.inv_t - lse;
-            }
-        }
+    for (int off = 16; off > 0; off >>= 1) S += __shfl_xor_sync(0xffffffffu, S, off);
+    double lse = 0.0;
+    if (lane == 0) lse = double(M) * a.inv_t + ln_pos(S);  // S >= 1: the maximum's own term
+    lse = __shfl_sync(0xffffffffu, lse, 0);
+    if (lane < a.k) {
+        const size_t o = (size_t(b) * a.out_R + a.out_r0 + r) * a.k + lane;
+        a.row_tok[o] = int32_t(topk_key_token(run));
+        a.row_lc[o] = double(topk_key_value(run)) * a.inv_t - lse;
     }
-    cluster.sync();  // peers' shared memory stays alive until rank 0 has read it
 }
 
 // Composite selection key: larger = better.  High 54 bits: orderable log V (the low 10 bits of
@@ -298,33 +296,96 @@ struct SelectArgs {
     const int32_t *slots;
 };
 
+// Pool layout: depth 1 holds the root's k children (entries 0 .. k - 1, in child-rank order);
+// depth f >= 2 holds the k^2 children of the depth f - 1 frontier from k + (f - 2)k^2 on, slot by
+// slot (slot s's k children at s k .. s k + k - 1 of the depth).  The pool index is the creation
+// index.
+__device__ __forceinline__ int depth_base(int f, int k) { return f == 1 ? 0 : k + (f - 2) * k * k; }
+__device__ __forceinline__ int depth_count(int f, int k) { return f == 1 ? k : k * k; }
+__device__ __forceinline__ int depth_of(int e, int k) { return e < k ? 1 : 2 + (e - k) / (k * k); }
+// Start of depth f's list of its min(count, m) best keys (descending) in the rerank's table.
+__device__ __forceinline__ int list_base(int f, int k, int m) {
+    return f == 1 ? 0 : min(k, m) + (f - 2) * min(k * k, m);
+}
+
+struct SelSmem {
+    union {
+        double lc[kMaxPool];        // [R*k] the rows' child log-confidences (R*k = P <= 1024)
+        uint64_t sorted[kMaxPool];  // after the depth loop: each depth's best keys, descending
+    } u;
+    union {
+        int ctok[kMaxPool];  // [R*k] the rows' child tokens
+        int kept[kMaxPool];  // after the depth loop: kept flags
+    } v;
+    double logv[kMaxPool];   // pool: log V
+    uint64_t key[kMaxPool];  // pool: composite key
+    int par[kMaxPool];       // pool: parent pool index (-1: the root)
+    int row[kMaxPool];       // pool: draft row that expanded it, or -1
+    int flat[kMaxPool];      // pool: rank within its depth, then flattened index or -1
+    int ptok[kMaxPool];      // pool: token
+    int lent[kMaxPool];      // the rerank table: pool index of each sorted-list entry
+    int fslot[kMaxSelDepth][16];  // frontier of each depth: pool index of slot s
+    int wsum[kMaxPool / 32];
+};
+
+// Ranks of a depth's candidates within the depth (cnt <= 256 unique keys; rank = the number of
+// keys above).  Each thread holds four consecutive candidates in registers and compares them with
+// a strided slice of the keys, so every key read from shared memory serves four comparisons (the
+// rank is bound by the bytes shared memory delivers, not by the comparisons).  The NS threads of
+// a group cover the keys between them and sum their counts by shuffles, two counts packed in one
+// word (each < 2^16).  Warps past the last group skip the count.  `done(i, rank)` runs in one
+// thread per candidate.
+template <int NS, typename F>
+__device__ __forceinline__ void rank_blocked(const uint64_t *keys, int cnt, F &&done) {
+    const int tid = threadIdx.x;
+    const int groups = (cnt + 3) >> 2;
+    if ((tid & ~31) >= groups * NS) return;  // warp-uniform
+    const int g = tid / NS, sl = tid % NS;
+    const int c0 = 4 * g;
+    const uint64_t v0 = c0 < cnt ? keys[c0] : ~0ull, v1 = c0 + 1 < cnt ? keys[c0 + 1] : ~0ull;
+    const uint64_t v2 = c0 + 2 < cnt ? keys[c0 + 2] : ~0ull, v3 = c0 + 3 < cnt ? keys[c0 + 3] : ~0ull;
+    uint32_t n01 = 0, n23 = 0;  // counts of candidates 0, 1 (low, high half) and 2, 3
+    for (int o = sl; o < cnt; o += NS) {
+        const uint64_t kv = keys[o];
+        n01 += (kv > v0 ? 1u : 0u) + (kv > v1 ? 0x10000u : 0u);
+        n23 += (kv > v2 ? 1u : 0u) + (kv > v3 ? 0x10000u : 0u);
+    }
+#pragma unroll
+    for (int x = 1; x < NS; x <<= 1) {
+        n01 += __shfl_xor_sync(0xffffffffu, n01, x);
+        n23 += __shfl_xor_sync(0xffffffffu, n23, x);
+    }
+    if (sl == 0 && g < groups) {
+        if (c0 < cnt) done(c0, int(n01 & 0xffffu));
+        if (c0 + 1 < cnt) done(c0 + 1, int(n01 >> 16));
+        if (c0 + 2 < cnt) done(c0 + 2, int(n23 & 0xffffu));
+        if (c0 + 3 < cnt) done(c0 + 3, int(n23 >> 16));
+    }
+}
+template <typename F>
+__device__ __forceinline__ void rank_depth(const uint64_t *keys, int cnt, F &&done) {
+    const int groups = (cnt + 3) >> 2;
+    if (groups * 32 <= kSelThreads) rank_blocked<32>(keys, cnt, done);
+    else if (groups * 16 <= kSelThreads) rank_blocked<16>(keys, cnt, done);
+    else rank_blocked<8>(keys, cnt, done);
+}
+
+// One CTA per sequence.  Depth by depth: every candidate's rank within its depth (counting, a
+// group of threads per candidate), then the expansion of the k best (the frontier), each phase
+// closed by a block barrier.  The rerank keeps the m largest keys of the pool: a key's rank in the
+// pool is its rank within its depth plus, for every other depth, the number of that depth's keys
+// above it, found by binary search in that depth's sorted list of its m best keys; only the
+// entries of those lists can be kept.  Then the flatten (creation order) and the outputs.
 __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) {
     pdl_wait();
     pdl_launch_next();
-    // [R*k] child log-confidences (R*k = P <= 1024); after the expansion, the per-depth lists
-    __shared__ union {
-        double lc[kMaxPool];
-        uint64_t sorted[kMaxPool];
-    } s_u;
-    // [R*k] child tokens; after the expansion, the kept flags
-    __shared__ union {
-        int ctok[kMaxPool];
-        int kept[kMaxPool];
-    } s_v;
-    __shared__ double s_logv[kMaxPool];   // pool: log V
-    __shared__ uint64_t s_key[kMaxPool];  // pool: composite key
-    __shared__ int s_par[kMaxPool];       // pool: parent pool index (-1: the root)
-    __shared__ int s_row[kMaxPool];       // pool: draft row that expanded it, or -1
-    __shared__ int s_flat[kMaxPool];      // pool: rank within its depth, then flattened index or -1
-    __shared__ int s_ptok[kMaxPool];      // pool: token
-    __shared__ unsigned char s_dep[kMaxPool];
-    __shared__ int s_slot[16];
-    __shared__ int s_dlb[kMaxDepth + 2], s_dcnt[kMaxDepth + 2], s_doff[kMaxDepth + 2];  // per depth
-    __shared__ int s_wsum[kMaxPool / 32];
+    extern __shared__ __align__(16) unsigned char sel_smem_raw[];
+    SelSmem &S = *reinterpret_cast<SelSmem *>(sel_smem_raw);
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int k = a.k, R = a.R, D = a.D, m = a.m;
+    const int np = k + (D - 1) * k * k;  // pool size
 
     // the rows' children (written by the row kernel): every load in flight before the first store
     const int nload = R * k;
@@ -344,150 +405,106 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         for (int u = 0; u < kPer; ++u) {
             const int i = tid + u * kSelThreads;
             if (i < nload) {
-                s_u.lc[i] = lcv[u];
-                s_v.ctok[i] = tkv[u];
+                S.u.lc[i] = lcv[u];
+                S.v.ctok[i] = tkv[u];
             }
+            if (i < np) S.row[i] = -1;
         }
     }
     __syncthreads();
     // depth 1: the root's children (row 0)
     for (int i = tid; i < k; i += kSelThreads) {
-        s_logv[i] = s_u.lc[i];
-        s_key[i] = pool_key(s_u.lc[i], i);
-        s_ptok[i] = s_v.ctok[i];
-        s_par[i] = -1;
-        s_row[i] = -1;
-        s_dep[i] = 1;
+        S.logv[i] = S.u.lc[i];
+        S.key[i] = pool_key(S.u.lc[i], i);
+        S.ptok[i] = S.v.ctok[i];
+        S.par[i] = -1;
     }
     __syncthreads();
 
-    // Rank of each candidate of one depth within the depth (keys are unique): two adjacent
-    // threads per candidate, each counting the keys above it in one half of the depth (the loop
-    // is warp-uniform).  The rank goes to s_flat (free until the flatten); with `frontier`, the k
-    // best are the depth's frontier (slot = rank) and go to s_slot.
-    auto rank_depth = [&](int lb, int cnt, int f, bool frontier) {
-        for (int base = 0, half = (cnt + 1) >> 1; base < cnt; base += kSelThreads / 2) {
-            const int ei = base + (tid >> 1);
-            const bool act = ei < cnt;
-            const int e = lb + ei;
-            const uint64_t v = act ? s_key[e] : ~0ull;
-            const int o0 = lb + (tid & 1) * half, o1 = min(o0 + half, lb + cnt);
-            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;  // four independent chains of shared loads
-            int o = o0;
-            for (; o + 4 <= o1; o += 4) {
-                r0 += s_key[o] > v;
-                r1 += s_key[o + 1] > v;
-                r2 += s_key[o + 2] > v;
-                r3 += s_key[o + 3] > v;
+    for (int f = 1; f <= D; ++f) {
+        const int lb = depth_base(f, k), cnt = depth_count(f, k);
+        // rank within the depth; a candidate of rank r < k is frontier slot r
+        rank_depth(S.key + lb, cnt, [&](int i, int rank) {
+            const int e = lb + i;
+            S.flat[e] = rank;
+            if (f < D && !a.slots && rank < k) {
+                S.fslot[f][rank] = e;
+                S.row[e] = 1 + (f - 1) * k + rank;
             }
-            for (; o < o1; ++o) r0 += s_key[o] > v;
-            const int part = (r0 + r1) + (r2 + r3);
-            const int rank = part + __shfl_xor_sync(0xffffffffu, part, 1);
-            if (act && !(tid & 1)) {
-                s_flat[e] = rank;
-                if (frontier && rank < k) {
-                    s_slot[rank] = e;
-                    s_row[e] = 1 + (f - 1) * k + rank;
-                }
-            }
-        }
-    };
-
-    // depths 2..D: the k best nodes of the previous depth are expanded; frontier slot = rank
-    int lb = 0, cnt = k, np = k;
-    uint64_t ranked = 0;  // depths whose candidates were ranked here (the same in every thread)
-    for (int f = 1; f <= D - 1; ++f) {
-        if (tid == 0) {
-            s_dlb[f] = lb;
-            s_dcnt[f] = cnt;
-        }
-        if (a.slots) {
-            const int32_t *slots_f = a.slots + (size_t(b) * D + f) * k;
-            // the frontier chosen by an earlier call; an index outside this depth's candidates
-            // (a stale or foreign state) is flagged and replaced by the rank order's slot
-            for (int s = tid; s < k; s += kSelThreads) {
-                int e = slots_f[s];
+        });
+        __syncthreads();
+        if (f == D) break;
+        // expansion: child c of frontier slot s (expanded with draft row 1 + (f - 1)k + s) becomes
+        // entry s k + c of depth f + 1
+        const int nb = lb + cnt;
+        const int32_t *slots_f = a.slots ? a.slots + (size_t(b) * D + f) * k : nullptr;
+        for (int t = tid; t < k * k; t += kSelThreads) {
+            const int s = t / k, c = t - s * k;
+            const int rr = 1 + (f - 1) * k + s;
+            int e;
+            if (slots_f) {
+                // the frontier chosen by an earlier call (stepwise build); an index outside this
+                // depth's candidates (a stale or foreign state) is flagged and replaced by the
+                // slot's own position
+                e = slots_f[s];
                 if (e < lb || e >= lb + cnt) {
-                    set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
+                    if (c == 0) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
                     e = lb + s;
                 }
-                s_slot[s] = e;
-                s_row[e] = 1 + (f - 1) * k + s;
+                if (c == 0) S.row[e] = rr;
+            } else {
+                e = S.fslot[f][s];
             }
-        } else {
-            rank_depth(lb, cnt, f, true);
-            ranked |= 1ull << f;
+            const int ne = nb + t;
+            const double lv = S.logv[e] + S.u.lc[rr * k + c];
+            S.logv[ne] = lv;
+            S.key[ne] = pool_key(lv, ne);
+            S.ptok[ne] = S.v.ctok[rr * k + c];
+            S.par[ne] = e;
         }
         __syncthreads();
-        const int nf = cnt < k ? cnt : k;
-        for (int i = tid; i < nf * k; i += kSelThreads) {
-            const int sl = i / k, ch = i % k;
-            const int par = s_slot[sl];
-            const int rr = 1 + (f - 1) * k + sl;
-            const int e = np + i;
-            const double lv = s_logv[par] + s_u.lc[rr * k + ch];
-            s_logv[e] = lv;
-            s_key[e] = pool_key(lv, e);
-            s_ptok[e] = s_v.ctok[rr * k + ch];
-            s_par[e] = par;
-            s_row[e] = -1;
-            s_dep[e] = (unsigned char)(f + 1);
-        }
-        __syncthreads();
-        lb = np;
-        cnt = nf * k;
-        np += nf * k;
     }
 
-    // rerank: keep the m largest keys of the pool (keys are unique).  A key's rank in the pool is
-    // its rank within its depth plus, for every other depth, the number of that depth's keys
-    // above it.  Only a depth's m best keys can be kept or decide a count below m, so each
-    // depth contributes a descending list of its first min(cnt, m) keys, and the counts are
-    // binary searches in those lists.
-    if (tid == 0) {  // the last depth
-        s_dlb[D] = lb;
-        s_dcnt[D] = cnt;
-    }
-    __syncthreads();
-    for (int d = 1; d <= D; ++d)  // depths not ranked above (the last; frontiers read from slots)
-        if (d == 64 || !((ranked >> d) & 1ull)) rank_depth(s_dlb[d], s_dcnt[d], d, false);
-    if (tid == 0) {
-        int off = 0;
-        for (int d = 1; d <= D; ++d) {
-            s_doff[d] = off;
-            off += min(s_dcnt[d], m);
+    // rerank table: each depth's min(count, m) best keys in descending order with their pool
+    // indices; every entry of the table gets its rank in the pool, and those below m are kept
+    const int k1 = min(k, m), kk = min(k * k, m);
+    const int nlist = k1 + (D - 1) * kk;
+    for (int e = tid; e < np; e += kSelThreads) {
+        const int r = S.flat[e];
+        if (r < m) {
+            const int idx = list_base(depth_of(e, k), k, m) + r;
+            S.u.sorted[idx] = S.key[e];
+            S.lent[idx] = e;
         }
-        s_doff[D + 1] = off;
-    }
-    __syncthreads();  // ranks and offsets; the rows' children are no longer read
-    for (int e = tid; e < np; e += kSelThreads) {
-        const int r = s_flat[e];
-        if (r < m) s_u.sorted[s_doff[s_dep[e]] + r] = s_key[e];
+        S.v.kept[e] = 0;
     }
     __syncthreads();
-    for (int e = tid; e < np; e += kSelThreads) {
-        const int d = s_dep[e];
-        const uint64_t v = s_key[e];
-        int g = s_flat[e];
-        // four depths' searches at a time, so that their shared-memory loads overlap (a depth past
-        // D, or the key's own depth, contributes an empty list)
+    for (int t = tid; t < nlist; t += kSelThreads) {
+        const int d = t < k1 ? 1 : 2 + (t - k1) / kk;
+        const uint64_t v = S.u.sorted[t];
+        int g = t - list_base(d, k, m);
+        // four depths' searches at a time, with unconditional loads from clamped indices so that
+        // their shared-memory loads overlap (a depth past D, or the key's own depth, contributes
+        // an empty list)
         for (int d2 = 1; d2 <= D && g < m; d2 += 4) {
             int len[4], pos[4] = {0, 0, 0, 0};
             const uint64_t *lst[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int dd = d2 + u;
-                len[u] = (dd > D || dd == d) ? 0 : min(s_dcnt[dd], m);
-                lst[u] = s_u.sorted + s_doff[dd <= D ? dd : D + 1];
+                len[u] = (dd > D || dd == d) ? 0 : (dd == 1 ? k1 : kk);
+                lst[u] = S.u.sorted + (dd <= D ? list_base(dd, k, m) : 0);
             }
 #pragma unroll
             for (int step = 32; step > 0; step >>= 1)  // lists are descending, m <= 63
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (pos[u] + step <= len[u] && lst[u][pos[u] + step - 1] > v) pos[u] += step;
+                for (int u = 0; u < 4; ++u) {
+                    const uint64_t kv = lst[u][max(min(pos[u] + step, len[u]) - 1, 0)];
+                    pos[u] += (pos[u] + step <= len[u] && kv > v) ? step : 0;
+                }
             g += (pos[0] + pos[1]) + (pos[2] + pos[3]);
         }
-        s_v.kept[e] = g < m;
+        if (g < m) S.v.kept[S.lent[t]] = 1;
     }
     __syncthreads();
 
@@ -495,27 +512,27 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     const int nchunks = (np + 31) / 32;
     for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
         const int e = ch * 32 + lane;
-        const bool kept = e < np && s_v.kept[e];
+        const bool kept = e < np && S.v.kept[e];
         const unsigned bal = __ballot_sync(0xffffffffu, kept);
-        if (lane == 0) s_wsum[ch] = __popc(bal);
+        if (lane == 0) S.wsum[ch] = __popc(bal);
     }
     __syncthreads();
     if (warp == 0) {
-        int v = lane < nchunks ? s_wsum[lane] : 0;
+        int v = lane < nchunks ? S.wsum[lane] : 0;
         int incl = v;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             int o = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off) incl += o;
         }
-        if (lane < nchunks) s_wsum[lane] = incl - v;
+        if (lane < nchunks) S.wsum[lane] = incl - v;
     }
     __syncthreads();
     for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
         const int e = ch * 32 + lane;
-        const bool kept = e < np && s_v.kept[e];
+        const bool kept = e < np && S.v.kept[e];
         const unsigned bal = __ballot_sync(0xffffffffu, kept);
-        if (e < np) s_flat[e] = kept ? 1 + s_wsum[ch] + __popc(bal & ((1u << lane) - 1u)) : -1;
+        if (e < np) S.flat[e] = kept ? 1 + S.wsum[ch] + __popc(bal & ((1u << lane) - 1u)) : -1;
     }
     __syncthreads();
 
@@ -537,28 +554,28 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         if (a.node_logv) a.node_logv[size_t(b) * n] = 0.f;
     }
     for (int e = tid; e < np; e += kSelThreads) {
-        const int i = s_flat[e];
+        const int i = S.flat[e];
         if (i < 0) continue;
-        const int pe = s_par[e];
+        const int pe = S.par[e];
         int pi = 0;
         if (pe >= 0) {
-            pi = s_flat[pe];
+            pi = S.flat[pe];
             if (pi < 0) {  // cannot happen for a consistent pool: the kept set is ancestor-closed
                 set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
                 pi = 0;
             }
         }
         uint64_t bits = 1ull | (1ull << i);
-        for (int anc = pe; anc >= 0; anc = s_par[anc]) {
-            const int fi = s_flat[anc];
+        for (int anc = pe; anc >= 0; anc = S.par[anc]) {
+            const int fi = S.flat[anc];
             if (fi > 0) bits |= 1ull << fi;
         }
-        tokens[i] = s_ptok[e];
+        tokens[i] = S.ptok[e];
         parents[i] = pi;
-        depths[i] = s_dep[e];
-        node_row[i] = s_row[e];
+        depths[i] = depth_of(e, k);
+        node_row[i] = S.row[e];
         mask[i] = bits;
-        if (a.node_logv) a.node_logv[size_t(b) * n + i] = float(s_logv[e]);
+        if (a.node_logv) a.node_logv[size_t(b) * n + i] = float(S.logv[e]);
     }
 }
 
@@ -776,7 +793,14 @@ eagle_status select_launch(const eagle_tree_cfg &c, const BuildWs &w, const int3
     sa.m = c.keep;
     sa.R = 1 + (c.depth - 1) * c.topk;
     sa.slots = replay ? w.slots : nullptr;
-    if (launch_pdl(tree_select_kernel, dim3(c.batch), dim3(kSelThreads), 0, stream, 1u, sa) != cudaSuccess)
+    static std::atomic<uint64_t> ready{0};
+    if (once_per_device(ready, [] {
+            return cudaFuncSetAttribute(tree_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        int(sizeof(SelSmem)));
+        }) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
+    if (launch_pdl(tree_select_kernel, dim3(c.batch), dim3(kSelThreads), sizeof(SelSmem), stream, 1u, sa) !=
+        cudaSuccess)
         return EAGLE_ERR_CUDA;
     note_launch();
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
@@ -787,7 +811,7 @@ eagle_status select_launch(const eagle_tree_cfg &c, const BuildWs &w, const int3
 // One wave of CTAs: rows are split over a cluster only while the grid stays within the SM count
 // (each CTA streams its slice with loads of the next batch in flight).
 int splits_for_rows(long rows, int vocab) {
-    long sp = 152 / rows;
+    long sp = device_sm_count() / rows;
     const long per = long(kRowThreads) * kRowVals;
     const long useful = (vocab + per - 1) / per;  // no empty CTAs
     if (sp > useful) sp = useful;

@@ -41,6 +41,27 @@ static thread_local int32_t t_launches = 0;
 void note_launch() { ++t_launches; }
 void reset_launches() { t_launches = 0; }
 
+int device_sm_count() {
+    constexpr int kDefault = 152;
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();  // a host without a device: clear the error, use the default
+        return kDefault;
+    }
+    if (dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return kDefault;
+    }
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 namespace {
 
 bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }

@@ -4,13 +4,15 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "eagle.h"
 
 namespace eagle {
 
-// The first 256 bytes of every workspace hold the device status word.
+// The first 256 bytes of every workspace hold the device status word (offset 0) and, for the
+// verify, its per-call failure tag (offset 16).
 constexpr size_t kWsHeader = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -91,9 +93,11 @@ __device__ __forceinline__ uint64_t warp_bitonic_merge32(uint64_t v) {
     return v;
 }
 
-// Orderable 64-bit image of a double (integer order = numeric order; -0 folded onto +0).
+// Orderable 64-bit image of a double (integer order = numeric order; -0 folded onto +0 by an
+// integer test, which keeps the narrow FP64 pipe out of it).
 __device__ __forceinline__ uint64_t double_order_key(double d) {
-    const uint64_t u = static_cast<uint64_t>(__double_as_longlong(d + 0.0));
+    uint64_t u = static_cast<uint64_t>(__double_as_longlong(d));
+    if (u == 0x8000000000000000ull) u = 0;
     return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
 }
 
@@ -254,6 +258,25 @@ constexpr double kLn2 = 0.69314718055994530942;
 namespace eagle {
 void note_launch();
 void reset_launches();
+
+// Streaming multiprocessors of the current device, queried once per device (152 on GB300, and
+// 152 when no device can be queried, as in host-only use of the workspace-size functions).
+int device_sm_count();
+
+// Function attributes (dynamic shared memory size, cluster shape) belong to a device: `set` runs
+// once for each device this process launches on, recorded in the caller's bit set `ready`
+// (devices 64 and up run `set` on every call).
+template <typename F>
+cudaError_t once_per_device(std::atomic<uint64_t> &ready, F &&set) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+    if (bit && (ready.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = set();
+    if (e == cudaSuccess && bit) ready.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // Launch `kernel` with programmatic stream serialisation (and a cluster shape when cluster_x > 1).
 template <typename... KArgs, typename... Args>

@@ -369,13 +369,12 @@ __global__ void __launch_bounds__(128) tree_attn_f32_kernel(AttnArgs a) {
 template <int HD>
 eagle_status launch_bf16(const AttnArgs &a, cudaStream_t stream) {
     constexpr size_t smem = size_t(2) * 2 * kTileKeys * HD * 2;  // 2 stages x (K + V)
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(tree_attn_bf16_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-            cudaSuccess)
-            return EAGLE_ERR_CUDA;
-        attr = true;
-    }
+    static std::atomic<uint64_t> ready{0};
+    if (once_per_device(ready, [&] {
+            return cudaFuncSetAttribute(tree_attn_bf16_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        int(smem));
+        }) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
     const long grid = long(a.L) * a.B * a.Hkv * a.mgroups;
     tree_attn_bf16_kernel<HD><<<unsigned(grid), 32 * kWarps, smem, stream>>>(a);
     note_launch();
@@ -394,16 +393,17 @@ eagle_status launch_f32(const AttnArgs &a, cudaStream_t stream) {
 }  // namespace
 
 // Context split of the tensor-core kernel: when the (layer, sequence, KV head, row group) units
-// fill less than half of the GPU's 152 SMs (a draft model's single layer, one sequence), each
-// unit's context tiles are shared among several CTAs whose partial results a merge kernel
-// combines exactly; the workspace then holds the partials.
+// fill less than half of the GPU's SMs (a draft model's single layer, one sequence), each unit's
+// context tiles are shared among several CTAs whose partial results a merge kernel combines
+// exactly; the workspace then holds the partials.
 int attn_tc_splits(const eagle_attn_cfg &c) {
     if (c.dtype != EAGLE_DTYPE_BF16 || c.head_dim != 128 || c.heads_kv < 1 || c.heads_q % c.heads_kv) return 1;
     const long rows = long(c.heads_q / c.heads_kv) * c.nodes;
     const long units = long(c.layers) * c.batch * c.heads_kv * ((rows + 255) / 256);
-    if (units * 2 > 152) return 1;
+    const long sms = device_sm_count();
+    if (units * 2 > sms) return 1;
     const long nctx = (long(c.max_seq) + 127) / 128;
-    long s = 152 / units;
+    long s = sms / units;
     if (s > nctx / 2) s = nctx / 2;  // at least two tiles a split: the partials and the merge stay small
     if (s > 32) s = 32;
     return s < 2 ? 1 : int(s);

@@ -738,16 +738,17 @@ eagle_status tree_attention_tc_launch(const AttnTcParams &p, const void *q, cons
         !make_kv_map(&vm, v_cache, p.Hkv, LB * p.S_max, kNkv, 2) || !make_kv_map(&ktm, k_tree, p.Hkv, LB * p.n, kNkv, 2) ||
         !make_kv_map(&vtm, v_tree, p.Hkv, LB * p.n, kNkv, 2))
         return EAGLE_ERR_UNSUPPORTED;  // the caller falls back to the mma.sync kernel
-    static bool attr = false;
+    static std::atomic<uint64_t> ready{0};
     const size_t smem = kSmemBytes + 1024;
-    if (!attr) {
-        if (cudaFuncSetAttribute(tree_attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-                cudaSuccess ||
-            cudaFuncSetAttribute(tree_attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-                cudaSuccess)
-            return EAGLE_ERR_CUDA;
-        attr = true;
-    }
+    if (once_per_device(ready, [&] {
+            cudaError_t e =
+                cudaFuncSetAttribute(tree_attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(tree_attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+            return e;
+        }) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
     const long grid = long(p.L) * p.B * p.Hkv * p.mgroups * p.splits;
     const cudaError_t e = p.splits > 1 ? launch_pdl(tree_attn_tc_kernel<true>, dim3(unsigned(grid)), dim3(kThreads), smem,
                                                     stream, 1u, qm, km, vm, ktm, vtm, p)

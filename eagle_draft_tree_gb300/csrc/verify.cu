@@ -87,6 +87,11 @@ struct VerifyArgs {
     float *out_ratio;       // optional
     int32_t *out_tokens, *out_len, *out_path;
     int32_t *status;
+    // Per-call failure tag (a word of the workspace header): a prep CTA whose wait ran out stores
+    // this call's `gen` there, and the walk then commits nothing (out_len = 0) for any sequence.
+    // Tags are unique per call in a process, so a tag left by an earlier call never matches.
+    int32_t *fail_tag;
+    int32_t gen;
     int B, n, V, R, D, slice;
     float inv_t;    // 1/T (T > 0)
     double inv_td;  // 1/T in double
@@ -495,6 +500,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         if (!got && lane == 0) {
             s_fail = 1;
             set_status(a.status, EAGLE_ERR_TIMEOUT);
+            atomicExch(a.fail_tag, a.gen);
         }
     };
     if (bulkA) {
@@ -518,6 +524,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         if (lane == 0) {
             s_fail = 1;
             set_status(a.status, EAGLE_ERR_TIMEOUT);
+            atomicExch(a.fail_tag, a.gen);
         }
     };
     auto post = [&](float4 v) {  // lane 0's v: this warp's partial
@@ -840,6 +847,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
             }
         }
     }
+    // a bonus draw that could not be made: nothing of this sequence is committed
+    if (a.bonus_mode && tid == 0 && *reinterpret_cast<volatile int *>(&s_fail)) a.out_len[b] = 0;
     cluster_wait();  // no peer leaves while records it sent may still be landing here, or vice versa
 }
 
@@ -882,7 +891,9 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
     // uniform.  A chain that stopped at its first accepted child was tested by the prep (the
     // verdict is in sj); with every ratio wanted, each child's is computed here, one thread per
     // node, in double precision from its parent's row statistics.
-    const bool ok = !s_bad;
+    // a prep CTA of this call whose wait ran out left its statistics unwritten: commit nothing
+    const bool call_failed = *reinterpret_cast<volatile const int32_t *>(a.fail_tag) == a.gen;
+    const bool ok = !s_bad && !call_failed;
     bool acc = false;
     if (tid < n) {
         float r = NAN;
@@ -913,7 +924,7 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
     for (int j = 0; j < D; ++j) op[j] = -1;
     a.bonus[b] = -1;
     if (!ok) {
-        set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
+        set_status(a.status, call_failed ? EAGLE_ERR_TIMEOUT : EAGLE_ERR_DEVICE_INPUT);
         a.out_len[b] = 0;
         return;
     }
@@ -951,19 +962,15 @@ size_t tree_verify_workspace_bytes(const eagle_verify_cfg &c) {
 namespace {
 template <int CL>
 cudaError_t launch_prep(const VerifyArgs &a, int clusters, int batch, cudaStream_t stream) {
-    // function attributes are per device: set them once for each device this process launches on
     static std::atomic<uint64_t> ready{0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (!bit || !(ready.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(verify_prep_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = once_per_device(ready, [] {
+        cudaError_t r = cudaFuncSetAttribute(verify_prep_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              int(kPrepSmem));
-        if (e == cudaSuccess && CL > 8)
-            e = cudaFuncSetAttribute(verify_prep_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (e != cudaSuccess) return e;
-        ready.fetch_or(bit);
-    }
+        if (r == cudaSuccess && CL > 8)
+            r = cudaFuncSetAttribute(verify_prep_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     return launch_pdl(verify_prep_kernel<CL>, dim3(CL, clusters, batch), dim3(kPrepThreads), kPrepSmem, stream,
                       unsigned(CL), a);
 }
@@ -982,7 +989,12 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
     a.parents = parents;
     a.node_row = node_row;
     a.uniforms = uniforms;
+    static std::atomic<uint32_t> call_gen{0};
+    uint32_t gen = call_gen.fetch_add(1, std::memory_order_relaxed) + 1;
+    if (gen == 0u) gen = call_gen.fetch_add(1, std::memory_order_relaxed) + 1;  // 0: a fresh workspace's tag
     a.status = reinterpret_cast<int32_t *>(w);
+    a.fail_tag = reinterpret_cast<int32_t *>(w + 16);
+    a.gen = int32_t(gen);
     a.stat = reinterpret_cast<NodeStat *>(w + kWsHeader);
     a.final_tok = reinterpret_cast<int32_t *>(w + kWsHeader + align_up(size_t(c.batch) * n * sizeof(NodeStat), 256));
     a.bonus = reinterpret_cast<int32_t *>(reinterpret_cast<unsigned char *>(a.final_tok) +

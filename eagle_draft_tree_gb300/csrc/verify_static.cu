@@ -13,8 +13,10 @@ constexpr size_t kVerifyScratchBytes = size_t(256) << 10;  // 256 KB: e.g. 113 s
 constexpr int kMaxDevices = 64;
 
 // The scratch itself: file-scope device storage, zero-filled when the module is loaded.  Only its
-// first word (the device status word) is ever read before this call writes it, and that word
-// starts at zero; every other byte is written by a kernel of the call before another reads it.
+// header (the device status word and the per-call failure tag) is ever read before this call
+// writes it, and both start at zero; every other byte is written by a kernel of the call before
+// another reads it.  A call whose waits ran out is recognised by its own failure tag, so what an
+// earlier call left never reaches the outputs.
 static __device__ __align__(256) unsigned char g_verify_scratch[kVerifyScratchBytes];
 
 // Per-device address of the scratch, looked up by the first call on each device.
@@ -36,6 +38,10 @@ extern "C" eagle_status eagle_tree_verify_static(const eagle_verify_cfg *cfg, co
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return EAGLE_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return EAGLE_ERR_UNSUPPORTED;
+    // the scratch address below is the current device's: the stream must belong to that device
+    int sdev = -1;
+    if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return EAGLE_ERR_INVALID_ARG;
+    if (sdev != dev) return EAGLE_ERR_INVALID_ARG;
     void *scratch = g_scratch_addr[dev].load(std::memory_order_acquire);
     if (!scratch) {
         if (cudaGetSymbolAddress(&scratch, g_verify_scratch) != cudaSuccess || !scratch) return EAGLE_ERR_CUDA;

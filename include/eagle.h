@@ -325,7 +325,8 @@ size_t eagle_tree_verify_workspace_size(const eagle_verify_cfg *cfg);
  *                            rejected; NaN for the root and at T == 0.
  * Device-side check: a malformed tree (parent not before child, token outside [0, V), missing
  * draft row under a node with children) sets EAGLE_ERR_DEVICE_INPUT and that sequence's
- * out_len to 0.
+ * out_len to 0.  A device wait that runs out (EAGLE_ERR_TIMEOUT) sets out_len to 0 for every
+ * sequence of the call.
  */
 eagle_status eagle_tree_verify(const eagle_verify_cfg *cfg, const float *target_logits, const float *draft_logits,
                                const int32_t *tokens, const int32_t *parents, const int32_t *node_row,
@@ -343,10 +344,14 @@ eagle_status eagle_tree_verify(const eagle_verify_cfg *cfg, const float *target_
  * scratch.  The pages describe no such entry point; it is an interface convenience only.
  *   - Allocates nothing.  The first call on each device looks up the scratch's address
  *     (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *     `stream` must belong to the current device (EAGLE_ERR_INVALID_ARG otherwise): the scratch
+ *     used is the current device's.
  *   - The scratch starts zeroed (static storage) and needs no initialisation; no state carries
  *     from one call to the next except the device status word, which this entry point never
- *     reads: device-side errors show only through out_len (0 for a malformed tree).  Callers
- *     that need the status word use eagle_tree_verify with their own workspace.
+ *     reads: device-side errors show only through out_len, which is 0 for a malformed tree and
+ *     for every sequence of a call in which a device wait ran out (each call tags its own
+ *     failures, so an earlier call's scratch contents never reach the outputs).  Callers that
+ *     need the status word use eagle_tree_verify with their own workspace.
  *   - There is one scratch per device: two calls that may overlap on the device (different
  *     streams, or different host threads) race on it and must be serialised by the caller.
  */

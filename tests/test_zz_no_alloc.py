@@ -68,3 +68,22 @@ def test_static_verify_after_a_different_round():
     torch.cuda.synchronize()
     for k in ("out_tokens", "out_len", "out_path"):
         assert torch.equal(first[k], again[k]), k
+
+
+@pytest.mark.gpu
+def test_static_verify_reports_a_malformed_tree_through_out_len():
+    """This entry point never reads the device status word, so a device-side error has to show in
+    its outputs: a sequence whose tree names a parent after its child commits nothing
+    (out_len = 0), while the other sequences of the call commit what eagle_tree_verify commits."""
+    wl = datagen.WORKLOADS["serving_b64"].with_(batch=4)
+    draft, tree, target, u = _inputs(wl, seed=7)
+    ref = eg.tree_verify(target, draft, tree, u, temperature=0.7, depth=wl.depth, topk=wl.topk)
+    bad = {k: v.clone() for k, v in tree.items()}
+    bad["parents"][2, 5] = 9  # node 5's parent after it: not a tree in creation order
+    for _ in range(2):
+        got = eg.tree_verify_static(target, draft, bad, u, temperature=0.7, depth=wl.depth, topk=wl.topk)
+        torch.cuda.synchronize()
+        assert int(got["out_len"][2]) == 0
+        for b in (0, 1, 3):
+            assert int(got["out_len"][b]) == int(ref["out_len"][b])
+            assert torch.equal(got["out_tokens"][b], ref["out_tokens"][b])

@@ -19,23 +19,28 @@
 // the tree reduces to comparisons of uniforms with precomputed ratios.
 //
 //   verify_prep_kernel  one cluster of CL CTAs (8, or 16 for vocabularies above 131072) per node
-//                       with children (sampling; greedy: per pair of nodes).  Each thread holds 32
-//                       consecutive tokens of a row in registers: the node's target and draft rows.
-//                       Log-sum-exp, the S_j passes and the inverse-CDF scan are register loops;
-//                       each CTA reduces a pass to one record and pushes it to every peer
-//                       (st.async completing on the receiver's mbarrier), so a pass costs one
-//                       point-to-point exchange, not a cluster-wide barrier, and the final draw
-//                       reuses the records of the last exchange.  Per-node statistics (row
-//                       maxima, log normalisers, each child's c_j and S_j) and every such node's
-//                       final draw go to the workspace.
-//   verify_walk_kernel  one CTA per sequence: validates the tree, computes every child's accept
-//                       ratio in double precision (one thread per node), and walks the tree.  A
-//                       walk that ends at a leaf (every draft on its path accepted) leaves the
-//                       bonus token's slot to the next launch.
-//   the same prep kernel, bonus mode: one cluster per sequence draws the bonus token from the
-//                       target distribution of the leaf the walk ended at, if it did.  A leaf's
-//                       draw is needed by at most one walk, so it is made only for that leaf
-//                       instead of for every leaf up front.
+//                       with children (sampling; greedy: per pair of nodes).  Each CTA bulk-copies
+//                       its slices of the node's target and draft rows into shared memory; thread
+//                       t takes 8 chunks of 4 tokens, chunk e at token 4 (t + 512 e) of the slice,
+//                       into registers.  Log-sum-exp, the S_j passes and the inverse-CDF scan are
+//                       register loops; each CTA reduces a pass to one record and pushes it to
+//                       every peer (st.async completing on the receiver's mbarrier), so a pass
+//                       costs one point-to-point exchange, not a cluster-wide barrier.  A chain
+//                       stops at its first accepted child.  When that child is a leaf the walk may
+//                       end there, so the cluster also draws the leaf's bonus token from the
+//                       leaf's target row (the first child's row slice is prefetched with the
+//                       node's own rows, as it is the one usually accepted); the root without
+//                       children draws its own final token.  Per-node statistics (row maxima, log
+//                       normalisers, each child's c_j and S_j with the prep's verdict) and the
+//                       draws go to the workspace.
+//   verify_walk_kernel  one CTA per sequence: validates the tree and walks it over the prep's
+//                       verdicts, committing the draft tokens of the accepted path and the final
+//                       or bonus token the prep drew where the walk stops.  With every child's
+//                       ratio wanted (out_ratio) the chains run to the end, the walk makes every
+//                       test itself in double precision (one thread per node), and a walk that
+//                       ends at a leaf leaves the bonus token's slot to a third launch: the prep
+//                       kernel in bonus mode, one cluster per sequence, draws it from that leaf's
+//                       target distribution.
 #include <atomic>
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
@@ -55,7 +60,8 @@ constexpr int kWarpsPrep = kPrepThreads / 32;
 constexpr int kE = 32;                       // tokens per thread and row, in kChunks chunks of 4
 constexpr int kChunks = kE / 4;
 constexpr int kSliceMax = kPrepThreads * kE;  // one CTA's slice of a row (16384 tokens)
-constexpr size_t kPrepSmem = 2 * size_t(kSliceMax) * sizeof(float);  // both rows' slices, 128 KB
+// the node's two rows' slices and a prefetched slice of its first child's row, 192 KB
+constexpr size_t kPrepSmem = 3 * size_t(kSliceMax) * sizeof(float);
 constexpr int kMaxNodes = 64;
 constexpr double kFxInv = 1.0 / 4503599627370496.0;  // fixed-point unit of weight sums: 2^-52
 
@@ -377,15 +383,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     __shared__ float4 s_recv[2][CL];                 // the cluster's records of an exchange, by parity
     __shared__ __align__(8) uint64_t s_rbar[2];
     __shared__ __align__(8) uint64_t s_pbar;     // every warp's partial of the current pass posted
-    __shared__ __align__(8) uint64_t s_lbar[2];  // a row slice landed
+    __shared__ __align__(8) uint64_t s_lbar[3];  // a row slice landed
     __shared__ int s_kid[kMaxNodes];             // children of the node (sampling), ascending
     __shared__ uint64_t s_rrfx[kMaxNodes];       // each child's p0/q0 at its token, 2^-52 units
     __shared__ float s_uk[kMaxNodes];            // each child's uniform
     __shared__ int s_dec[2];                     // the accept test of the current child, by parity
     __shared__ __align__(8) uint64_t s_decbar;   // s_dec written
     __shared__ int s_nk, s_fail, s_second;
-    __shared__ int s_own[2];
-    __shared__ uint64_t s_local[2];
+    __shared__ uint64_t s_leaves;  // the tree's leaves (nodes without children), one bit each
+    __shared__ int s_acc;          // the child at which the chain stopped (accepted)
+    __shared__ int s_pre;          // the child whose target row slice was prefetched, or -1
+    __shared__ int s_own[1];
+    __shared__ uint64_t s_local[1];
     __shared__ DrawSmem s_draw;
 
     cg::cluster_group cluster = cg::this_cluster();
@@ -414,6 +423,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         mbar_init(&s_pbar, kWarpsPrep);
         mbar_init(&s_lbar[0], 1);
         mbar_init(&s_lbar[1], 1);
+        mbar_init(&s_lbar[2], 1);
         mbar_init(&s_decbar, 1);
         fence_barrier_init();
     }
@@ -423,7 +433,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
             s_nk = 0;
             s_second = -1;
             s_fail = 0;
-            s_own[0] = s_own[1] = -1;
+            s_own[0] = -1;
         }
     } else if (warp == 0) {
         // every node's "has children" bit, and the children of node y, from the <= 64 parents
@@ -444,11 +454,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         if (lane == 0) {
             s_nk = __popc(b0) + __popc(b1);
             int second = -1;  // greedy: the paired node (-2: this cluster has no work)
-            if (!a.greedy && ((leaves >> y) & 1ull)) second = -2;
+            // a leaf's cluster has no work, except the root's when the root has no children and
+            // the prep makes the leaves' draws (its final token is drawn from its target row)
+            if (!a.greedy && ((leaves >> y) & 1ull) && !(y == 0 && !a.full_chain)) second = -2;
+            s_leaves = leaves;
             if (a.greedy) second = 2 * y + 1 < n ? 2 * y + 1 : -1;
             s_second = second;
             s_fail = 0;
-            s_own[0] = s_own[1] = -1;
+            s_own[0] = -1;
         }
     }
     __syncthreads();
@@ -478,7 +491,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         return r && ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(r) & 15) == 0) && cnt > 0;
     };
     const bool bulkA = bulk_ok(rowA), bulkB = bulk_ok(rowB);
+    // The first child is the one most often accepted; when it is a leaf the walk may end there
+    // and need its bonus draw, so its target row's slice follows the node's own two rows in
+    // (used only if that child is accepted; the CTA waits for it before leaving either way).
     if (tid == 0) {
+        const int pre = (!a.greedy && !a.bonus_mode && !a.full_chain && has_q && ((s_leaves >> s_kid[0]) & 1ull))
+                            ? s_kid[0] : -1;
+        const float *rowP = pre >= 0 ? a.target + (size_t(b) * n + pre) * V + lo : nullptr;
+        const bool bulkP = bulk_ok(rowP);
+        s_pre = bulkP ? pre : -1;
         if (bulkA) {
             mbar_expect_tx(&s_lbar[0], uint32_t(cnt) * 4u);
             bulk_g2s(s_rows, rowA, uint32_t(cnt) * 4u, &s_lbar[0]);
@@ -486,6 +507,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         if (bulkB) {
             mbar_expect_tx(&s_lbar[1], uint32_t(cnt) * 4u);
             bulk_g2s(s_rows + kSliceMax, rowB, uint32_t(cnt) * 4u, &s_lbar[1]);
+        }
+        if (bulkP) {
+            mbar_expect_tx(&s_lbar[2], uint32_t(cnt) * 4u);
+            bulk_g2s(s_rows + 2 * kSliceMax, rowP, uint32_t(cnt) * 4u, &s_lbar[2]);
         }
     }
     // every final draw uses the sequence's first uniform (the root's, which no accept test uses)
@@ -621,6 +646,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         return;
     }
 
+    // sampling from here on: the second held row is the node's draft row (no paired node)
     const float c = a.c;
     // ---- row statistics of both held rows.  Values become 2^((x - m) c) against the thread's max
     // m, so the probabilities later cost one multiply each (no second exponential).
@@ -639,18 +665,18 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         const float4 g = ms_fold2(mine, c);
         const float l2A = g.y > 0.f ? log2f(g.y) : 0.f;
         const float l2B = g.w > 0.f ? log2f(g.w) : 0.f;
-        // side work off warp 0 (which gathers the next pass): the leaves' draw owners from the
-        // per-rank probability totals, and the node's row statistics
-        if ((warp == 1 && !has_q) || (warp == 2 && nodeB >= 0)) {
-            const int k = warp - 1;
-            const float m = k ? mine.z : mine.x, sm = k ? mine.w : mine.y, M = k ? g.z : g.x, l2 = k ? l2B : l2A;
-            const float tr = m == -INFINITY ? 0.f : sm * fast_exp2((m - M) * c - l2);
+        // side work off warp 0 (which gathers the next pass): a node without a draft row (the
+        // bonus launch's leaf, or the root without children) draws from its target
+        // distribution: the draw's owner from the per-rank probability totals; and the node's row
+        // statistics
+        if (warp == 1 && !has_q) {
+            const float tr = mine.x == -INFINITY ? 0.f : mine.y * fast_exp2((mine.x - g.x) * c - l2A);
             int own;
             uint64_t loc;
             decide_owner_warp<CL>(lane < CL ? to_fx(tr) : 0ull, uA, own, loc);
             if (lane == 0) {
-                s_own[k] = own;
-                s_local[k] = loc;
+                s_own[0] = own;
+                s_local[0] = loc;
             }
         }
         gst = g;
@@ -706,7 +732,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     uint64_t cj = 0, Sj = 1ull << 52;
     float cnf = 1.f;  // c_1 = c_0 + S_0
     bool decided = !has_q;
-    bool accepted = false;  // a child was accepted and the chain stopped there
+    bool accepted = false;  // a child was accepted and the chain stopped there (s_acc)
     for (int j = 0; j < J && has_q; ++j) {
         // the last pass forms exact chunk weights (they may become the final draw's); earlier
         // passes need only the sum: one float sum per thread
@@ -760,6 +786,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
             if (!mbar_warp_wait_bounded(&s_decbar, j & 1)) fail();
             if (*reinterpret_cast<volatile int *>(&s_dec[j & 1])) {
                 accepted = true;
+                if (tid == 0) s_acc = s_kid[j];
                 break;
             }
         }
@@ -805,34 +832,67 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
             }
         }
     }
+    // ---- an accepted child that is a leaf: the walk may end there, with a bonus token drawn from
+    // the leaf's own target distribution (inverse CDF with the sequence's first uniform).  It is
+    // drawn here, while the other nodes' chains still run, instead of in a launch after the walk
+    // (unless every ratio is wanted: the walk then makes the tests and the bonus launch the draw).
+    // The decision is the same in every CTA of the cluster, so the exchanges stay paired.
+    if (accepted) __syncthreads();  // s_acc is visible; every thread has read its row A chunks
+    const int spec = (accepted && !a.full_chain && ((s_leaves >> s_acc) & 1ull)) ? s_acc : -1;
+    if (spec >= 0) {
+        const float *rowL = a.target + (size_t(b) * n + spec) * V + lo;
+        const bool pref = spec == s_pre;              // prefetched into the third slice buffer
+        const bool copy = !pref && bulk_ok(rowL);     // else copied now into the first one
+        if (copy && tid == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic reads before the copy
+            mbar_expect_tx(&s_lbar[0], uint32_t(cnt) * 4u);
+            bulk_g2s(s_rows, rowL, uint32_t(cnt) * 4u, &s_lbar[0]);
+        }
+        if (pref || copy) {
+            // the first buffer's barrier is in its phase 1 after the row A copy, else 0
+            const bool got = mbar_warp_wait_bounded(&s_lbar[pref ? 2 : 0], pref ? 0u : (bulkA ? 1u : 0u));
+            if (!got && lane == 0) {
+                s_fail = 1;
+                set_status(a.status, EAGLE_ERR_TIMEOUT);
+                atomicExch(a.fail_tag, a.gen);
+            }
+            read_chunks(xp, s_rows + (pref ? 2 * kSliceMax : 0), cnt);
+        } else {
+            load_chunks(xp, rowL, cnt);
+        }
+        float mL;
+        const float sL = exp_run(xp, mL, c);
+        const float4 neutral = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+        post(ms_fold2(make_float4(mL, sL, -INFINITY, 0.f), c));
+        if (warp == 0 && wait_posts()) send(ms_fold2(lane < kWarpsPrep ? s_wp[lane] : neutral, c));
+        const int slot = xch & 1;
+        const bool ok = wait_recv();
+        const float4 mine = ok && lane < CL ? s_recv[slot][lane] : neutral;  // lane r < CL: rank r's record
+        const float4 gl = ms_fold2(mine, c);
+        const float l2 = gl.y > 0.f ? log2f(gl.y) : 0.f;
+        if (warp == 1) {  // the draw's owner from the per-rank probability totals
+            const float tr = mine.x == -INFINITY ? 0.f : mine.y * fast_exp2((mine.x - gl.x) * c - l2);
+            int own;
+            uint64_t loc;
+            decide_owner_warp<CL>(lane < CL ? to_fx(tr) : 0ull, uA, own, loc);
+            if (lane == 0) {
+                s_own[0] = own;
+                s_local[0] = loc;
+            }
+        }
+        const float fL = mL == -INFINITY ? 0.f : fast_exp2(fmaf(mL - gl.x, c, -l2));
+#pragma unroll
+        for (int j = 0; j < kE; ++j) xp[j] *= fL;
+    }
     // every record this CTA sends has been sent: the closing cluster barrier can start
     cluster_arrive();
     __syncthreads();  // the draw decisions are visible
 
-    // ---- final draws: node A over xp (probabilities or residual), leaf B over xq.  Leaf B's weights
-    // wait in this thread's own chunks of the second slice buffer (its copy was consumed), so one
-    // draw instance serves both and only one row is live in registers.
-    if (nodeB >= 0) {
-        float *dst = s_rows + kSliceMax;
-#pragma unroll
-        for (int e = 0; e < kChunks; ++e)
-            *reinterpret_cast<float4 *>(dst + chunk_tok(e)) = make_float4(xq[4 * e], xq[4 * e + 1], xq[4 * e + 2], xq[4 * e + 3]);
-    }
-    for (int k = 0; k < (accepted ? 0 : nodeB >= 0 ? 2 : 1); ++k) {
-        const int owner = s_own[k];
-        const int node = k ? nodeB : nodeA;
-        if (k == 1) {
-            __syncthreads();  // every thread is done with the first draw's shared state
-            const float *src = s_rows + kSliceMax;
-#pragma unroll
-            for (int e = 0; e < kChunks; ++e) {
-                const float4 v = *reinterpret_cast<const float4 *>(src + chunk_tok(e));
-                xp[4 * e] = v.x;
-                xp[4 * e + 1] = v.y;
-                xp[4 * e + 2] = v.z;
-                xp[4 * e + 3] = v.w;
-            }
-        }
+    // ---- the final draw, over xp: node A's probabilities or residual (every child rejected), or
+    // the accepted leaf's probabilities
+    if (!accepted || spec >= 0) {
+        const int owner = s_own[0];
+        const int node = spec >= 0 ? spec : nodeA;
         int32_t *slot = a.bonus_mode ? a.out_tokens + size_t(b) * (a.D + 1) + (breq >> 8) : nullptr;
         if (owner < 0) {
             if (rank == 0 && tid == 0 && !s_fail) {  // no positive mass
@@ -840,7 +900,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
                 if (slot) *slot = 0;
             }
         } else if (rank == owner) {
-            const int found = draw_in_slice(xp, s_local[k], s_draw);
+            const int found = draw_in_slice(xp, s_local[0], s_draw);
             if (found >= 0 && !s_fail) {
                 a.final_tok[size_t(b) * n + node] = lo + found;
                 if (slot) *slot = lo + found;
@@ -849,6 +909,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     }
     // a bonus draw that could not be made: nothing of this sequence is committed
     if (a.bonus_mode && tid == 0 && *reinterpret_cast<volatile int *>(&s_fail)) a.out_len[b] = 0;
+    // an unused prefetch has landed before the shared memory is released (bounded)
+    if (s_pre >= 0 && spec != s_pre) mbar_warp_wait_bounded(&s_lbar[2], 0);
     cluster_wait();  // no peer leaves while records it sent may still be landing here, or vice versa
 }
 
@@ -933,9 +995,10 @@ __global__ void __launch_bounds__(64) verify_walk_kernel(VerifyArgs a) {
         const int next = s_next[node];
         if (next >= n || len >= D) {
             if (next < n) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);  // tree deeper than D
-            if (!a.greedy && !s_kids[node]) {
-                // a leaf: its draw from the target distribution is made by the bonus launch,
-                // which also writes the token into this slot
+            if (!a.greedy && !s_kids[node] && a.full_chain) {
+                // a leaf with every ratio wanted: its draw from the target distribution is made by
+                // the bonus launch, which also writes the token into this slot (otherwise the prep
+                // drew it: the leaf's parent accepted it, or it is the root without children)
                 a.bonus[b] = node | (len << 8);
                 ++len;
             } else {
@@ -1025,7 +1088,7 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
     note_launch();
     if (launch_pdl(verify_walk_kernel, dim3(c.batch), dim3(64), 0, stream, 1u, a) != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();
-    if (!a.greedy) {  // the bonus token of a walk that ended at a leaf
+    if (!a.greedy && a.full_chain) {  // the bonus token of a walk that ended at a leaf
         a.bonus_mode = 1;
         e = cl == 8 ? launch_prep<8>(a, 1, c.batch, stream) : launch_prep<16>(a, 1, c.batch, stream);
         if (e != cudaSuccess) return EAGLE_ERR_CUDA;

@@ -39,13 +39,20 @@ METRIC = "tree-verify rounds/s (build+attn+sample) at 8B shape; tree-attn HBM GB
 UNIT = "rounds/s"
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
+
+
 def _peaks() -> dict:
+    """Roofline denominators: the measured copy bandwidth and bf16 GEMM rates of this machine's
+    GB300s (burst: a kernel timed alone; sustained: seconds of back-to-back work), else the
+    fallback figures."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", 1700.0)), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
 def _side_roofline(nbytes: float, us: float, what: str) -> dict:
@@ -264,6 +271,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
     draft_attn = run_draft_attention(eg, lib, wl, ws, stream, dev)
     static = run_static_tree(eg, lib, wl, ws, stream, dev)
     sampled_build = run_sampled_build(eg, lib, wl, ws, stream, dev)
+    attn_workloads = run_attention_workloads(eg, lib, ws, stream, dev, args.attn_launches)
 
     bytes_ = datagen.bytes_of(wl, ctx_total=float(sets[0].attn["ctx_len"].sum().item()))
     peaks = _peaks()
@@ -284,12 +292,16 @@ def run_ours(args, rank, world, dev) -> dict | None:
                      "algorithmic_bytes": attn_bytes, "avg_launch_ms": attn_ms,
                      "launch_samples": f"CUDA events around the attention launch of every {ATTN_EVERY}th timed "
                                        f"step ({len(sampled)} launches)",
+                     "frac_nominal": achieved / NOMINAL_HBM_GBS, "nominal_peak": NOMINAL_HBM_GBS,
+                     "loop_check": _loop_check(attn_workloads, wl.name),
                      "peak_source": f"{peaks['source']} hbm_gbs (MEASURED_PEAKS.json)"},
         "end_to_end_hbm": {"metric_bytes": metric_bytes, "exact_bytes": bytes_["exact"],
                            "gbs": metric_bytes / (ms / K * 1e-3) / 1e9,
-                           "frac": metric_bytes / (ms / K * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+                           "frac": metric_bytes / (ms / K * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                           "frac_nominal": metric_bytes / (ms / K * 1e-3) / 1e9 / NOMINAL_HBM_GBS},
         "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks, "mean_committed": mean_len,
         "kv_commit": commit, "draft_attention": draft_attn, "static_tree": static, "sampled_build": sampled_build,
+        "attention_workloads": attn_workloads,
     }
     return res
 
@@ -496,6 +508,107 @@ def run_static_tree(eg, lib, wl, ws, stream, dev, calls: int = 200) -> dict:
     return res
 
 
+def _loop_check(sweep: dict, name: str):
+    """The same kernel's time from the attention-only loop of the sweep (many launches), beside the
+    in-round samples of the headline roofline."""
+    r = sweep.get(name)
+    if not r:
+        return None
+    return {"us_per_launch": r["us_per_launch"], "launches": r["launches"], "frac": r["roofline"]["frac"]}
+
+
+def run_attention_workloads(eg, lib, ws, stream, dev, launches: int = 100) -> dict:
+    """Tree attention alone on every bf16 workload's shape (the round's dominant kernel), each
+    timed with CUDA events over `launches` back-to-back launches of the whole-model call (all
+    layers, the batch, the workload's tree from eagle_build_tree), HBM-cold: the KV cache of a
+    launch is far larger than the L2, and the 8B shape alternates two input sets.  Reported per
+    workload: the time per launch, the HBM roofline (algorithmic bytes: KV cache, tree K/V, Q and
+    O) against the measured copy peak and the nominal HBM rate, and the tensor roofline (QK^T and
+    PV flops) against the measured bf16 rates.  At the 8B shape the same attention also runs as
+    one launch per layer (a target model interleaves its layers with other work), 32 launches."""
+    pk = _peaks()
+    out = {}
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    for name in ("llama31_8b", "vicuna_13b", "llama2_70b_b4", "serving_b64"):
+        wl = datagen.WORKLOADS[name]
+        B, n, L = wl.batch, wl.nodes, wl.layers
+        nsets = 2 if name == "llama31_8b" else 1
+        sets = []
+        for s in range(nsets):
+            seed = 40 + s
+            inp = datagen.attention_inputs(wl, seed, dev)
+            draft = datagen.draft_logits(B, wl.rows, wl.vocab, seed, dev)
+            tree = eg.build_tree(draft, datagen.root_tokens(B, wl.vocab, seed, dev), depth=wl.depth, topk=wl.topk,
+                                 keep=wl.keep, ws=ws)
+            del draft
+            inp["mask"] = tree["mask"]
+            inp["out"] = torch.empty_like(inp["q"])
+            sets.append(inp)
+        cfg = eg.AttnCfg(B, L, n, wl.heads_q, wl.heads_kv, wl.head_dim, wl.max_seq, eg.EAGLE_DTYPE_BF16, 0.0)
+        ws.reserve(lib.eagle_tree_attention_workspace_size(ctypes.byref(cfg)))
+        wsp, wsn = ws.ptr, ctypes.c_size_t(ws.nbytes)
+        args = [(ctypes.byref(cfg), P(a["q"]), P(a["k_cache"]), P(a["v_cache"]), P(a["ctx_len"]), P(a["k_tree"]),
+                 P(a["v_tree"]), P(a["mask"]), P(a["out"]), wsp, wsn, sptr) for a in sets]
+        for i in range(3):
+            if lib.eagle_tree_attention(*args[i % nsets]) != 0:
+                raise RuntimeError(f"eagle_tree_attention failed ({name})")
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(launches):
+            lib.eagle_tree_attention(*args[i % nsets])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = e0.elapsed_time(e1) / launches * 1e3
+        ctx_total = float(sets[0]["ctx_len"].sum().item())
+        nbytes = datagen.bytes_of(wl, ctx_total=ctx_total)["attention"]
+        flops = datagen.attention_flops(wl, ctx_total=ctx_total)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        tfs = flops / (us * 1e-6) / 1e12
+        res = {"us_per_launch": us, "launches": launches, "algorithmic_bytes": nbytes, "flops": flops,
+               "flop_per_byte": flops / nbytes,
+               "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                            "frac": gbs / pk["hbm_gbs"], "frac_nominal": gbs / NOMINAL_HBM_GBS,
+                            "nominal_peak": NOMINAL_HBM_GBS,
+                            "peak_source": f"{pk['source']} hbm_gbs (MEASURED_PEAKS.json)"},
+               "tensor": {"achieved": tfs, "unit": "TFLOP/s", "frac_sustained": tfs / pk["bf16_tflops_sustained"],
+                          "frac_burst": tfs / pk["bf16_tflops"], "peak_sustained": pk["bf16_tflops_sustained"],
+                          "peak_burst": pk["bf16_tflops"]},
+               "shape": _workload_desc(wl), "l2": f"{nsets} input set(s), KV cache {datagen.bytes_of(wl, ctx_total)['kv'] / 1e6:.0f} MB"}
+        if name == "llama31_8b":
+            # one launch per layer: the layer's slices of q, the caches, the tree K/V and the output
+            a = sets[0]
+            cfg1 = eg.AttnCfg(B, 1, n, wl.heads_q, wl.heads_kv, wl.head_dim, wl.max_seq, eg.EAGLE_DTYPE_BF16, 0.0)
+            ws.reserve(lib.eagle_tree_attention_workspace_size(ctypes.byref(cfg1)))  # the context split's partials
+            wsp, wsn = ws.ptr, ctypes.c_size_t(ws.nbytes)
+            largs = [(ctypes.byref(cfg1), P(a["q"][l]), P(a["k_cache"][l]), P(a["v_cache"][l]), P(a["ctx_len"]),
+                      P(a["k_tree"][l]), P(a["v_tree"][l]), P(a["mask"]), P(a["out"][l]), wsp, wsn, sptr)
+                     for l in range(L)]
+            reps = max(4, launches // L)
+            for la in largs:
+                lib.eagle_tree_attention(*la)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for _ in range(reps):
+                for la in largs:
+                    lib.eagle_tree_attention(*la)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            us_l = e0.elapsed_time(e1) / reps * 1e3
+            gbs_l = nbytes / (us_l * 1e-6) / 1e9
+            res["per_layer_launches"] = {"us_all_layers": us_l, "us_per_layer": us_l / L, "rounds": reps,
+                                         "achieved_gbs": gbs_l, "frac": gbs_l / pk["hbm_gbs"],
+                                         "note": f"{L} launches of one layer each; a layer's KV is read again only "
+                                                 f"after the other {L - 1} layers', so every launch is HBM-cold"}
+        if ws.status(stream) != 0:
+            raise RuntimeError(f"device status not OK after the attention sweep ({name})")
+        out[name] = res
+        del sets, args
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_sampled_build(eg, lib, wl, ws, stream, dev, calls: int = 100) -> dict:
     """The dynamic build with sampled children (eagle_build_tree_sampled) and as a stepwise build
     (eagle_build_begin, D - 1 eagle_build_expand, eagle_build_finalize), beside the greedy
@@ -692,20 +805,32 @@ class OracleRound:
                 "attn_units_timed": len(self.times["attn"]), "round_s": round(self.round_seconds(), 3)}
 
 
-def cpu_baseline(wl, seed, budget_s: float = 20.0) -> dict:
-    nthreads = os.cpu_count() or 1
+def _oracle_rate(wl, seed, nthreads: int, budget_s: float) -> tuple:
+    """The oracle's rounds/s on `nthreads` host threads over a bounded sample of one round (its build,
+    its verify and as many attention units as the budget allows, extrapolated in units)."""
     orc = OracleRound(wl, seed, nthreads)
     t0 = time.perf_counter()
     i = 0
     while i < 3 or (time.perf_counter() - t0 < budget_s and i < orc.units + 2):
         orc.item(i)
         i += 1
-    return {"value": 1.0 / orc.round_seconds(), "unit": UNIT, "cores": nthreads, "kind": "oracle",
+    return 1.0 / orc.round_seconds(), orc
+
+
+def cpu_baseline(wl, seed, budget_s: float = 20.0, single_budget_s: float = 12.0) -> dict:
+    nthreads = os.cpu_count() or 1
+    value, orc = _oracle_rate(wl, seed, nthreads, budget_s)
+    v1, orc1 = _oracle_rate(wl, seed, 1, single_budget_s)
+    return {"value": value, "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": (f"one round's build and verify of every sequence plus {len(orc.times['attn'])} of "
                        f"{orc.units} attention units (layer x KV head; all nodes and query heads of the group; "
                        f"full context), attention extrapolated linearly in units; fp64 C oracle, OpenMP on "
                        f"{nthreads} threads"),
-            "seconds": orc.summary()}
+            "seconds": orc.summary(),
+            "single_core": {"value": v1, "unit": UNIT, "cores": 1, "kind": "oracle",
+                            "sample": (f"the same round on one thread: build, verify and {len(orc1.times['attn'])} "
+                                       f"of {orc1.units} attention units, extrapolated in units"),
+                            "seconds": orc1.summary()}}
 
 
 def run_reference(args, rank, world) -> dict | None:
@@ -755,6 +880,8 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attn-launches", type=int, default=100,
+                    help="launches per workload in the attention-only sweep")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

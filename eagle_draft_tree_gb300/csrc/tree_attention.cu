@@ -14,7 +14,8 @@
 // ldmatrix is conflict-free); QK^T and PV use bf16 mma.sync m16n8k16 with fp32 accumulation;
 // online softmax in base 2 on the SFU.  The row groups of a unit are adjacent in the grid, so the
 // unit's K/V bytes come from HBM once and from L2 for the other groups.
-// fp32 kernel: plain FFMA (one warp per query row), for the fp32 workload and its 1e-4 bar.
+// fp32 kernel: plain FFMA flash attention (16 query rows per CTA, 32-key tiles in shared memory),
+// for the fp32 workload and its 1e-4 bar.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -120,6 +121,8 @@ __device__ __forceinline__ void load_tile(uint32_t sk, uint32_t sv, const __nv_b
 
 template <int HD>
 __global__ void __launch_bounds__(32 * kWarps) tree_attn_bf16_kernel(AttnArgs a) {
+    pdl_wait();
+    pdl_launch_next();
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr int KC = HD / 16;  // k16 chunks of the head dim
     constexpr int DT = HD / 8;   // n8 tiles of the head dim
@@ -309,61 +312,134 @@ __global__ void __launch_bounds__(32 * kWarps) tree_attn_bf16_kernel(AttnArgs a)
     }
 }
 
-// fp32: one warp per query row, lanes split the head dim.
+// fp32: a CTA per (unit, block of kF32Rows query rows), 256 threads.  The unit's keys (its
+// context, then the n tree keys) stream through shared memory in tiles of kF32Keys; thread t owns
+// query row t / 16 of the block: two of the tile's scores (keys t % 16 and t % 16 + 16, full dot
+// products from shared memory) and HD / 16 output columns (t % 16 + 16 c).  The 16 threads of a
+// row are one half-warp, so the row's online softmax (running max, rescale, running sum) meets by
+// shuffles and its probabilities pass through shared memory under a warp barrier only.  Keys that
+// a row does not see score -inf; the rows of absent keys are zero in shared memory, so whatever a
+// cache position past the context holds never reaches an output.
+constexpr int kF32Rows = 16;
+constexpr int kF32Keys = 32;
+constexpr int kF32Threads = 256;
+
 template <int HD>
-__global__ void __launch_bounds__(128) tree_attn_f32_kernel(AttnArgs a) {
-    constexpr int PER = HD / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const int unit = blockIdx.x;
+__global__ void __launch_bounds__(kF32Threads) tree_attn_f32_kernel(AttnArgs a) {
+    pdl_wait();
+    pdl_launch_next();
+    constexpr int NO = HD / 16;  // output columns per thread
+    __shared__ float sQ[kF32Rows][HD + 1];  // padded: the two half-warps' rows sit in different banks
+    __shared__ float sK[kF32Keys][HD + 1];  // padded: the 16 keys a half-warp reads sit in distinct banks
+    __shared__ float sV[kF32Keys][HD];
+    __shared__ float sP[kF32Rows][kF32Keys + 1];
+    const int tid = threadIdx.x;
+    const int rblocks = (a.rows + kF32Rows - 1) / kF32Rows;
+    const int unit = blockIdx.x / rblocks, rb = blockIdx.x % rblocks;
     const int g = unit % a.Hkv;
     const int b = (unit / a.Hkv) % a.B;
     const int l = unit / (a.Hkv * a.B);
     const int ctx = a.ctx_len[b];
     if (ctx < 0 || ctx > a.S_max) {
-        if (threadIdx.x == 0 && g == 0) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
-        return;
+        if (tid == 0 && g == 0 && rb == 0) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
+        return;  // uniform for the CTA
     }
     const float *Q = static_cast<const float *>(a.q);
     const float *kc = static_cast<const float *>(a.k_cache) + ((size_t(l) * a.B + b) * a.S_max * a.Hkv + g) * HD;
     const float *vc = static_cast<const float *>(a.v_cache) + ((size_t(l) * a.B + b) * a.S_max * a.Hkv + g) * HD;
     const float *kt = static_cast<const float *>(a.k_tree) + ((size_t(l) * a.B + b) * a.n * a.Hkv + g) * HD;
     const float *vt = static_cast<const float *>(a.v_tree) + ((size_t(l) * a.B + b) * a.n * a.Hkv + g) * HD;
-    const size_t stride = size_t(a.Hkv) * HD;
-    float *O = static_cast<float *>(a.out);
+    const size_t stride = size_t(a.Hkv) * HD;  // between consecutive keys of one KV head
 
-    for (int r = warp; r < a.rows; r += nwarps) {
-        const int node = r / a.G, h = g * a.G + r % a.G;
-        const size_t qo = (((size_t(l) * a.B + b) * a.n + node) * a.Hq + h) * HD;
-        float qv[PER], acc[PER];
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-            qv[e] = Q[qo + lane + 32 * e];
-            acc[e] = 0.f;
+    // the block's query rows, pre-scaled (row r: node r / G, query head g G + r % G)
+    const int r0 = rb * kF32Rows;
+    for (int i = tid; i < kF32Rows * (HD / 4); i += kF32Threads) {
+        const int rr = i / (HD / 4), c4 = i % (HD / 4), r = r0 + rr;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < a.rows) {
+            const size_t qo = (((size_t(l) * a.B + b) * a.n + r / a.G) * a.Hq + g * a.G + r % a.G) * HD;
+            v = reinterpret_cast<const float4 *>(Q + qo)[c4];
+            v.x *= a.scale;
+            v.y *= a.scale;
+            v.z *= a.scale;
+            v.w *= a.scale;
         }
-        const uint64_t msk = a.mask[size_t(b) * a.n + node];
-        float mrun = -INFINITY, lrun = 0.f;
-        auto visit = [&](const float *kp, const float *vp) {
-            float dot = 0.f;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) dot = fmaf(qv[e], kp[lane + 32 * e], dot);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-            const float x = dot * a.scale;
-            const float mn = fmaxf(mrun, x);
-            const float alpha = expf(mrun - mn);
-            const float p = expf(x - mn);
-            lrun = lrun * alpha + p;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] = fmaf(p, vp[lane + 32 * e], acc[e] * alpha);
-            mrun = mn;
-        };
-        for (int j = 0; j < ctx; ++j) visit(kc + size_t(j) * stride, vc + size_t(j) * stride);
-        for (int j = 0; j < a.n; ++j)
-            if ((msk >> j) & 1ull) visit(kt + size_t(j) * stride, vt + size_t(j) * stride);
-        const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) O[qo + lane + 32 * e] = acc[e] * inv;
+        sQ[rr][4 * c4] = v.x;
+        sQ[rr][4 * c4 + 1] = v.y;
+        sQ[rr][4 * c4 + 2] = v.z;
+        sQ[rr][4 * c4 + 3] = v.w;
     }
+    const int orow = tid >> 4, sub = tid & 15;
+    const int r = r0 + orow;
+    const bool rvalid = r < a.rows;
+    const uint64_t tmask = rvalid ? a.mask[size_t(b) * a.n + r / a.G] : 0ull;
+    float o[NO];
+#pragma unroll
+    for (int c = 0; c < NO; ++c) o[c] = 0.f;
+    float m = -INFINITY, lsum = 0.f;
+    const int nk = ctx + a.n;  // the context's keys, then the tree's
+    for (int j0 = 0; j0 < nk; j0 += kF32Keys) {
+        __syncthreads();  // the previous tile is consumed (and, the first time, sQ is written)
+        for (int i = tid; i < kF32Keys * (HD / 4); i += kF32Threads) {
+            const int jj = i / (HD / 4), c4 = i % (HD / 4), j = j0 + jj;
+            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+            if (j < ctx) {
+                kv = reinterpret_cast<const float4 *>(kc + size_t(j) * stride)[c4];
+                vv = reinterpret_cast<const float4 *>(vc + size_t(j) * stride)[c4];
+            } else if (j < nk) {
+                kv = reinterpret_cast<const float4 *>(kt + size_t(j - ctx) * stride)[c4];
+                vv = reinterpret_cast<const float4 *>(vt + size_t(j - ctx) * stride)[c4];
+            }
+            sK[jj][4 * c4] = kv.x;
+            sK[jj][4 * c4 + 1] = kv.y;
+            sK[jj][4 * c4 + 2] = kv.z;
+            sK[jj][4 * c4 + 3] = kv.w;
+            *reinterpret_cast<float4 *>(&sV[jj][4 * c4]) = vv;
+        }
+        __syncthreads();
+        // two scores of this thread's row: keys sub and sub + 16 of the tile
+        float s2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int jj = sub + 16 * h, j = j0 + jj;
+            const bool vis = rvalid && (j < ctx || (j < nk && ((tmask >> (j - ctx)) & 1ull)));
+            float acc = 0.f;
+#pragma unroll 16
+            for (int d = 0; d < HD; ++d) acc = fmaf(sQ[orow][d], sK[jj][d], acc);
+            s2[h] = vis ? acc : -INFINITY;
+        }
+        // online softmax over the row's half-warp
+        float tmx = fmaxf(s2[0], s2[1]);
+#pragma unroll
+        for (int x = 8; x > 0; x >>= 1) tmx = fmaxf(tmx, __shfl_xor_sync(0xffffffffu, tmx, x));
+        const float mn = fmaxf(m, tmx);
+        const float alpha = mn == -INFINITY ? 1.f : expf(m - mn);  // m = -inf: nothing to rescale
+        const float p0 = s2[0] == -INFINITY ? 0.f : expf(s2[0] - mn);
+        const float p1 = s2[1] == -INFINITY ? 0.f : expf(s2[1] - mn);
+        float ps = p0 + p1;
+#pragma unroll
+        for (int x = 8; x > 0; x >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, x);
+        lsum = lsum * alpha + ps;
+        m = mn;
+        sP[orow][sub] = p0;
+        sP[orow][sub + 16] = p1;
+        __syncwarp();  // the row's probabilities are written by its own half-warp
+#pragma unroll
+        for (int c = 0; c < NO; ++c) o[c] *= alpha;
+#pragma unroll 8
+        for (int jj = 0; jj < kF32Keys; ++jj) {
+            const float p = sP[orow][jj];
+#pragma unroll
+            for (int c = 0; c < NO; ++c) o[c] = fmaf(p, sV[jj][sub + 16 * c], o[c]);
+        }
+        __syncwarp();  // sP is rewritten by the next tile
+    }
+    if (!rvalid) return;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    float *O = static_cast<float *>(a.out) +
+               (((size_t(l) * a.B + b) * a.n + r / a.G) * a.Hq + g * a.G + r % a.G) * HD;
+#pragma unroll
+    for (int c = 0; c < NO; ++c) O[sub + 16 * c] = o[c] * inv;
 }
 
 template <int HD>
@@ -376,15 +452,18 @@ eagle_status launch_bf16(const AttnArgs &a, cudaStream_t stream) {
         }) != cudaSuccess)
         return EAGLE_ERR_CUDA;
     const long grid = long(a.L) * a.B * a.Hkv * a.mgroups;
-    tree_attn_bf16_kernel<HD><<<unsigned(grid), 32 * kWarps, smem, stream>>>(a);
+    if (launch_pdl(tree_attn_bf16_kernel<HD>, dim3(unsigned(grid)), dim3(32 * kWarps), smem, stream, 1u, a) !=
+        cudaSuccess)
+        return EAGLE_ERR_CUDA;
     note_launch();
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
 
 template <int HD>
 eagle_status launch_f32(const AttnArgs &a, cudaStream_t stream) {
-    const long grid = long(a.L) * a.B * a.Hkv;
-    tree_attn_f32_kernel<HD><<<unsigned(grid), 128, 0, stream>>>(a);
+    const long grid = long(a.L) * a.B * a.Hkv * ((a.rows + kF32Rows - 1) / kF32Rows);
+    if (launch_pdl(tree_attn_f32_kernel<HD>, dim3(unsigned(grid)), dim3(kF32Threads), 0, stream, 1u, a) != cudaSuccess)
+        return EAGLE_ERR_CUDA;
     note_launch();
     return cudaPeekAtLastError() == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }

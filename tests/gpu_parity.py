@@ -114,3 +114,31 @@ def oracle_attention_rows(inp: dict, mask_np, rows, G, scale):
                                        kt, vt, m1, scale=scale)
         outs.append(r[0])
     return np.stack(outs)
+
+
+def oracle_attention_unit(inp: dict, mask_np, l: int, b: int, g: int, G: int, scale):
+    """fp64 oracle for one whole (layer, sequence, KV head) unit: every node and every query head of
+    the group, float64 [n, G, d], from that unit's own slice of the inputs."""
+    ctx = int(inp["ctx_len"][b])
+    q1 = np_(inp["q"][l, b, :, g * G:(g + 1) * G][None, None].contiguous())
+    kc = np_(inp["k_cache"][l, b, :ctx, g][None, None, :, None, :].contiguous())
+    vc = np_(inp["v_cache"][l, b, :ctx, g][None, None, :, None, :].contiguous())
+    kt = np_(inp["k_tree"][l, b, :, g][None, None, :, None, :].contiguous())
+    vt = np_(inp["v_tree"][l, b, :, g][None, None, :, None, :].contiguous())
+    m1 = np.ascontiguousarray(mask_np[b][None])
+    r = oracle.tree_attention(q1, kc, vc, np.array([ctx], np.int32), kt, vt, m1, scale=scale)
+    return r[0, 0]
+
+
+def whole_units(wl, ctx_len) -> list:
+    """(layer, sequence, KV head) units checked whole at full size: the first and the last layer
+    and KV head, on the first and last sequence, or on the shortest- and longest-context sequence
+    when the contexts are ragged."""
+    L, B, Hkv = wl.layers, wl.batch, wl.heads_kv
+    ctx = [int(c) for c in ctx_len]
+    if len(set(ctx)) > 1:
+        seqs = [int(np.argmin(ctx)), int(np.argmax(ctx))]
+    else:
+        seqs = [0, B - 1]
+    units = {(0, seqs[0], 0), (L - 1, seqs[1], Hkv - 1), (0, seqs[1], Hkv - 1), (L - 1, seqs[0], 0)}
+    return sorted(units)

@@ -1,6 +1,7 @@
 """The five workloads at full size, through the C ABI in the benchmark's launch configuration:
 every tree index and committed token against the oracle, attention on sampled rows (each row's
-oracle value computed from its own slice of the inputs)."""
+oracle value computed from its own slice of the inputs) and on whole (layer, sequence, KV head)
+units: every node and query head of the unit against its own fp64 evaluation."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +10,7 @@ import datagen
 import eagle_draft_tree_gb300 as eg
 import oracle
 from tests.gpu_parity import (ATTN_TOL, attention_sample_rows, compare_build, compare_verify, gpu_build, np_,
-                              oracle_attention_rows, oracle_tree_tensors)
+                              oracle_attention_rows, oracle_attention_unit, oracle_tree_tensors, whole_units)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -67,3 +68,10 @@ def test_workload_round(name):
     err = np.abs(got - ref).max()
     assert err <= ATTN_TOL[wl.kv_dtype], err
     assert torch.isfinite(out).all()
+    # whole units, element by element
+    G = wl.group
+    for (l, b, g) in whole_units(wl, inp["ctx_len"]):
+        ref_u = oracle_attention_unit(inp, o_tree["mask"], l, b, g, G, datagen.scale_of(wl))
+        got_u = out[l, b, :, g * G:(g + 1) * G].double().cpu().numpy()
+        err_u = np.abs(got_u - ref_u).max()
+        assert err_u <= ATTN_TOL[wl.kv_dtype], ((l, b, g), err_u)

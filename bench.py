@@ -271,7 +271,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
     draft_attn = run_draft_attention(eg, lib, wl, ws, stream, dev)
     static = run_static_tree(eg, lib, wl, ws, stream, dev)
     sampled_build = run_sampled_build(eg, lib, wl, ws, stream, dev)
-    attn_workloads = run_attention_workloads(eg, lib, ws, stream, dev, args.attn_launches)
+    attn_workloads = run_attention_workloads(eg, lib, ws, stream, dev, args.attn_launches) if args.attn_launches > 0 else {}
 
     bytes_ = datagen.bytes_of(wl, ctx_total=float(sets[0].attn["ctx_len"].sum().item()))
     peaks = _peaks()
@@ -881,7 +881,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--attn-launches", type=int, default=100,
-                    help="launches per workload in the attention-only sweep")
+                    help="launches per workload in the attention-only sweep (0: no sweep)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -5,10 +5,13 @@ Tolerances (GPU vs fp64 oracle):
   * tree indices, masks, committed tokens/paths: bit-exact.  A build difference is excused only
     when the oracle's smallest relative key gap at a selection boundary is < 1e-6; a verify
     difference only when the oracle's smallest |u - decision value| on its walk is < 1e-5.
-  * node_logv: 1e-5 relative.  out_ratio: 1e-5 relative to max(1, ratio).  The ratio is compared
-    with a uniform, so its natural error scale is absolute below 1 (the same 1e-5 that excuses a
-    decision); after j rejections it is (p0 - c_j q)/(S_j q), and the fp32 error of c_j (~1e-7) is
-    amplified by the cancellation p0 - c_j q on small ratios.
+  * node_logv: 1e-5 relative.  out_ratio of a node's first child (p0/q0): 2e-6 relative.  Later
+    children ((p0/q0 - c_j)/S_j after j rejected siblings): 1e-4 relative plus 1e-4 absolute.
+    c_j and S_j are exact sums, but of single-precision probabilities (each within about 2^-22
+    relative of its exact value), and the residual's mass S_j and the numerator p0/q0 - c_j are
+    differences of nearly equal quantities when the target resembles the draft, so the error grows
+    as 1/S_j along a chain: measured up to 5e-5 absolute on the full-size workloads, against under
+    1e-6 relative for the first child.
   * attention: max-abs 2e-2 (bf16 K/V) or 1e-4 (fp32).
 """
 from __future__ import annotations
@@ -63,7 +66,26 @@ def oracle_tree_tensors(o: dict, device) -> dict:
     return t
 
 
-def compare_verify(g: dict, o: dict, log: list | None = None, ratio_rtol=1e-5, ratio_atol=1e-5):
+RATIO_FIRST_RTOL = 2e-6
+RATIO_LATER_TOL = 1e-4
+
+
+def sibling_index(parents) -> np.ndarray:
+    """int [B, n]: the number of earlier siblings of each node (0 for a first child and the root)."""
+    parents = np.asarray(parents)
+    j = np.zeros(parents.shape, np.int64)
+    for b in range(parents.shape[0]):
+        seen: dict = {}
+        for i in range(1, parents.shape[1]):
+            p = int(parents[b, i])
+            j[b, i] = seen.get(p, 0)
+            seen[p] = j[b, i] + 1
+    return j
+
+
+def compare_verify(g: dict, o: dict, log: list | None = None):
+    """o: the oracle's verify outputs, with the tree's "parents" added (the ratio tolerance
+    depends on a child's place among its siblings)."""
     excused = []
     B = o["out_len"].shape[0]
     for b in range(B):
@@ -82,7 +104,9 @@ def compare_verify(g: dict, o: dict, log: list | None = None, ratio_rtol=1e-5, r
         orr = o["out_ratio"]
         fin = np.isfinite(orr)
         assert np.array_equal(np.isnan(gr), np.isnan(orr)), "ratio defined on different nodes"
-        np.testing.assert_allclose(gr[fin], orr[fin], rtol=ratio_rtol, atol=ratio_atol)
+        first = sibling_index(o["parents"]) == 0
+        np.testing.assert_allclose(gr[fin & first], orr[fin & first], rtol=RATIO_FIRST_RTOL, atol=0)
+        np.testing.assert_allclose(gr[fin & ~first], orr[fin & ~first], rtol=RATIO_LATER_TOL, atol=RATIO_LATER_TOL)
         inf = np.isinf(orr)
         assert np.array_equal(np.isinf(gr), inf)
     return excused

@@ -175,6 +175,7 @@ def _verify_case(wl, seed, T, with_ratio=True):
     g = {k: np_(v) for k, v in g.items() if v is not None}
     o = oracle.tree_verify(np_(target), np_(draft), o_tree["tokens"], o_tree["parents"], o_tree["node_row"], np_(u),
                            T, wl.depth + 1)
+    o["parents"] = o_tree["parents"]
     return g, o
 
 

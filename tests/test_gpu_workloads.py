@@ -43,6 +43,7 @@ def test_workload_round(name):
     for T in ([wl.temperature, 0.0] if name == "llama31_8b" else [wl.temperature]):
         ov = oracle.tree_verify(target_np, draft_np, o_tree["tokens"], o_tree["parents"], o_tree["node_row"], u_np,
                                 T, wl.depth + 1)
+        ov["parents"] = o_tree["parents"]
         for with_ratio in (True, False):
             gv = eg.tree_verify(target, draft, tree, u, temperature=T, depth=wl.depth, topk=wl.topk, ws=ws,
                                 with_ratio=with_ratio)

@@ -90,6 +90,7 @@ _SIGS = {
     "eagle_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "eagle_last_launch_count": (ctypes.c_int32, []),
     "eagle_selftest_wait_timeout": (ctypes.c_int32, [_P, _P, _P]),
+    "eagle_selftest_exp2_error": (ctypes.c_int32, [_P, _P]),
     "eagle_kv_commit_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(AttnCfg)]),
     "eagle_build_static_tree_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(StaticTreeCfg)]),
     "eagle_build_static_tree": (ctypes.c_int32, [ctypes.POINTER(StaticTreeCfg)] + [_P] * 9 + [ctypes.c_size_t, _P]),
@@ -135,6 +136,13 @@ def _status_string(s: int) -> str:
 def last_launch_count() -> int:
     """Kernel launches issued by the most recent entry-point call on this thread."""
     return int(load().eagle_last_launch_count())
+
+
+def selftest_exp2_error(device="cuda", stream=None) -> float:
+    """eagle_selftest_exp2_error: the largest relative error of the SFU's 2^f over |f| <= 1/2."""
+    out = torch.zeros(1, dtype=torch.float32, device=device)
+    _check(load().eagle_selftest_exp2_error(_ptr(out), _stream(stream)), "eagle_selftest_exp2_error")
+    return float(out.cpu()[0])
 
 
 def selftest_wait_timeout(ws: "Workspace", stream=None) -> tuple[int, list[int]]:

@@ -18,6 +18,7 @@ eagle_status build_finalize_launch(const eagle_tree_cfg &c, const int32_t *root,
                                    int32_t *depths, int32_t *node_row, uint64_t *mask, float *node_logv, void *ws,
                                    cudaStream_t stream);
 size_t row_sample_max_vocab();
+eagle_status exp2_error_launch(float *out, cudaStream_t stream);
 size_t tree_attention_workspace_bytes(const eagle_attn_cfg &c);
 eagle_status tree_attention_launch(const eagle_attn_cfg &c, const void *q, const void *k_cache, const void *v_cache,
                                    const int32_t *ctx_len, const void *k_tree, const void *v_tree,
@@ -358,6 +359,12 @@ eagle_status eagle_selftest_wait_timeout(void *ws, uint64_t *elapsed_ns, cudaStr
     if (cudaPeekAtLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();
     return EAGLE_OK;
+}
+
+eagle_status eagle_selftest_exp2_error(float *max_rel_err, cudaStream_t stream) {
+    if (!max_rel_err) return EAGLE_ERR_INVALID_ARG;
+    reset_launches();
+    return exp2_error_launch(max_rel_err, stream);
 }
 
 }  // extern "C"

@@ -11,15 +11,21 @@
 // One thread-block cluster per row; its CTAs split the row into contiguous slices.
 //   pass 1 (HBM)  slice maximum; the cluster reads its CTAs' maxima through distributed shared
 //                 memory, so every CTA holds the row maximum M.
-//   pass 2 (L2)   weights w = 2^((x - M) c) with c = log2(e) / T, summed per 4-token chunk in float
-//                 and then as integers in units of 2^-40: per (chunk column, warp) totals stay in
-//                 shared memory, slice totals go to the cluster.  Integer sums are exact, so the
-//                 slices' totals, their prefix sums and every CTA's view of the row total agree.
+//   pass 2 (L2)   weights w = 2^((x - M) c) with c = log2(e) / T, each as an integer in units of
+//                 2^-S (S = 62 - ceil(log2 V), so the row total stays below 2^62) and summed per
+//                 4-token chunk, per (chunk column, warp) in shared memory and per slice for the
+//                 cluster.  Integer sums are exact, so the slices' totals, their prefix sums and
+//                 every CTA's view of the row total agree.
 //   draw j        warp j of each CTA: target = floor(u_j * total) in fixed point; the CTA whose
 //                 slice range holds it walks column -> warp -> lane -> token, re-deriving the one
 //                 chunk's weights from the row with the same arithmetic (hence the same values).
-// The row's log normaliser is M / T + ln(total 2^-40).  Chunks start at multiples of 4 tokens and
-// every sum above a chunk is exact, so draws and log-confidences do not depend on the slicing.
+// A weight's exponent is formed without rounding error: x - M by an error-free sum (Knuth's
+// TwoSum) and its product with c = c_hi + c_lo by an error-free FMA product, split into an integer
+// n and a fraction f in [-1/2, 1/2] rounded once; w = 2^n 2^f with 2^f from the SFU (ex2.approx,
+// whose relative error on [-1/2, 1/2] eagle_selftest_exp2_error measures).  A step of the row's
+// CDF is then off by at most half the weights' relative error plus V 2^-S.
+// The row's log normaliser is M / T + ln(total 2^-S).  Chunks start at multiples of 4 tokens and
+// every sum above a weight is exact, so draws and log-confidences do not depend on the slicing.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -40,16 +46,84 @@ constexpr int kSmpWarps = kSmpThreads / 32;
 constexpr int kSmpMaxCols = 128;                           // chunk columns per slice
 constexpr int kSmpMaxSlice = kSmpMaxCols * kSmpThreads * 4;  // 262144 tokens
 constexpr int kSmpMaxSplits = 8;
-constexpr float kFx40 = 1099511627776.0f;  // 2^40
-constexpr double kLn2_40 = 40.0 * 0.69314718055994530942;
+constexpr double kLn2 = 0.69314718055994530942;
 
-// floor(x 2^40) for x in [0, 4] (NaN and non-positive give 0; larger values are clamped).
-__device__ __forceinline__ uint64_t fx40(float x) {
-    if (!(x > 0.f)) return 0ull;
-    const uint32_t bits = __float_as_uint(fminf(x, 4.f));
-    const int ex = int(bits >> 23);  // x = m 2^(ex - 150), so x 2^40 = m 2^(ex - 110)
+// Warp-wide exact sum of 64-bit values whose total is below 2^64 (the result in every lane):
+// three 32-bit reductions of 22-bit parts.
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+    const uint32_t p0 = __reduce_add_sync(0xffffffffu, uint32_t(v) & 0x3fffffu);
+    const uint32_t p1 = __reduce_add_sync(0xffffffffu, uint32_t(v >> 22) & 0x3fffffu);
+    const uint32_t p2 = __reduce_add_sync(0xffffffffu, uint32_t(v >> 44));
+    return (uint64_t(p2) << 44) + (uint64_t(p1) << 22) + p0;
+}
+
+// Two floats in one 64-bit register pair, for the paired f32x2 arithmetic of sm_100-class SMs
+// (each operation rounds each lane exactly as its scalar form would).
+__device__ __forceinline__ uint64_t x2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void x2_split(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t x2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t x2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// b - a, rounded once (a times -1 is exact)
+__device__ __forceinline__ uint64_t x2_sub(uint64_t b, uint64_t a) { return x2_fma(a, x2(-1.f, -1.f), b); }
+
+// floor(p 2^e) for a normal p (the SFU's 2^f, in [0.70, 1.42]) and e <= S, exactly, on the
+// integer pipe: p = m 2^(ex - 150) with a 24-bit m, so p 2^e = m 2^(ex - 150 + e).
+__device__ __forceinline__ uint64_t scaled_floor(float p, int e) {
+    const uint32_t bits = __float_as_uint(p);
     const uint32_t m = (bits & 0x7fffffu) | 0x800000u;
-    return ex >= 110 ? (uint64_t(m) << (ex - 110)) : (ex > 86 ? uint64_t(m >> (110 - ex)) : 0ull);
+    const int sh = int(bits >> 23) - 150 + e;
+    return sh >= 0 ? (uint64_t(m) << sh) : (sh > -24 ? uint64_t(m >> (-sh)) : 0ull);
+}
+
+// The fixed-point weights floor(2^((x - M) c) 2^S) of two logits x <= M (0 for -inf or past
+// 2^-S): x - M by TwoSum, times c = c_hi + c_lo by an FMA product, r = n + f with n = rint(r_hi)
+// and f rounded once; 2^f in [0.70, 1.42] from the SFU (its only instruction there), then
+// 2^(n + S) applied exactly.
+__device__ __forceinline__ void weight_fx2(float xa, float xb, float M, float c_hi, float c_lo, int S, uint64_t &wa,
+                                           uint64_t &wb) {
+    const uint64_t X = x2(xa, xb), Mn = x2(-M, -M), C = x2(c_hi, c_hi);
+    const uint64_t D = x2_add(X, Mn);  // TwoSum(x, -M): D + E = x - M exactly
+    const uint64_t BB = x2_sub(D, X);
+    const uint64_t E = x2_add(x2_sub(X, x2_sub(D, BB)), x2_sub(Mn, BB));
+    const uint64_t RH = x2_mul(D, C);  // RH + RL = (D + E)(c_hi + c_lo) to ~2^-48
+    const uint64_t RL = x2_add(x2_fma(D, C, x2_mul(RH, x2(-1.f, -1.f))),  // the product's rounding error
+                               x2_fma(D, x2(c_lo, c_lo), x2_mul(E, C)));
+    // n = rint(RH) by adding 1.5 2^23 (whose ulp is 1) on the FMA pipe; the sum's bits give n as
+    // an integer (|RH| < 2^22 wherever the weight is kept)
+    const float kMagic = 12582912.0f;
+    const uint64_t TN = x2_add(RH, x2(kMagic, kMagic));
+    const uint64_t N = x2_sub(TN, x2(kMagic, kMagic));
+    float rha, rhb, ta, tb;
+    x2_split(RH, rha, rhb);
+    x2_split(TN, ta, tb);
+    const int na = __float_as_int(ta) - __float_as_int(kMagic), nb = __float_as_int(tb) - __float_as_int(kMagic);
+    float fa, fb;
+    x2_split(x2_add(x2_sub(RH, N), RL), fa, fb);  // RH - n is exact
+    float da, db;
+    x2_split(D, da, db);
+    // an infinite logit has no weight (its difference is NaN); one more than S + 2 octaves below
+    // the maximum adds less than 2^-S
+    wa = (xa == -INFINITY || !(da <= 0.f) || rha < -float(S + 2)) ? 0ull : scaled_floor(fast_exp2(fa), S + na);
+    wb = (xb == -INFINITY || !(db <= 0.f) || rhb < -float(S + 2)) ? 0ull : scaled_floor(fast_exp2(fb), S + nb);
 }
 
 struct SampleArgs {
@@ -59,8 +133,9 @@ struct SampleArgs {
     double *row_lc;        // [B][out_R][k]
     int32_t *status;
     int V, R, k, chunk, out_R, out_r0;
-    float c;       // log2(e) / T
-    double inv_t;  // 1 / T
+    int S;               // weights in units of 2^-S
+    float c, c_lo;       // log2(e) / T as a float pair
+    double inv_t;        // 1 / T
 };
 
 // Chunk q of a slice: the four values at lo + 4q .. lo + 4q + 3 (-inf past hi).
@@ -75,14 +150,12 @@ __device__ __forceinline__ float4 load_chunk(const float *row, int lo, int hi, i
     return v;
 }
 
-// The chunk's weights against the row maximum (0 for -inf) and its fixed-point total; the pass
-// and the draw both call this, so they derive identical values.
-__device__ __forceinline__ uint64_t chunk_w(float4 x, float c, float mc, float (&w)[4]) {
-    w[0] = x.x == -INFINITY ? 0.f : fast_exp2(fmaf(x.x, c, -mc));
-    w[1] = x.y == -INFINITY ? 0.f : fast_exp2(fmaf(x.y, c, -mc));
-    w[2] = x.z == -INFINITY ? 0.f : fast_exp2(fmaf(x.z, c, -mc));
-    w[3] = x.w == -INFINITY ? 0.f : fast_exp2(fmaf(x.w, c, -mc));
-    return fx40(((w[0] + w[1]) + w[2]) + w[3]);
+// The chunk's fixed-point weights against the row maximum and their total; the pass and the draw
+// both call this, so they derive identical values.
+__device__ __forceinline__ uint64_t chunk_w(float4 x, float M, const SampleArgs &a, uint64_t (&w)[4]) {
+    weight_fx2(x.x, x.y, M, a.c, a.c_lo, a.S, w[0], w[1]);
+    weight_fx2(x.z, x.w, M, a.c, a.c_lo, a.S, w[2], w[3]);
+    return (w[0] + w[1]) + (w[2] + w[3]);
 }
 
 // Inclusive warp scan of 64-bit values.
@@ -125,7 +198,6 @@ __global__ void __launch_bounds__(kSmpThreads) row_sample_kernel(SampleArgs a) {
     const int nch = (cnt + 3) >> 2;
     const int ncol = (nch + kSmpThreads - 1) / kSmpThreads;
     const bool vec = ((a.V & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.x) & 15) == 0);
-    const float c = a.c;
 
     // pass 1: the slice maximum
     float m = -INFINITY;
@@ -146,7 +218,6 @@ __global__ void __launch_bounds__(kSmpThreads) row_sample_kernel(SampleArgs a) {
     cluster.sync();
     float M = -INFINITY;
     for (int s = 0; s < splits; ++s) M = fmaxf(M, *cluster.map_shared_rank(&s_max, s));
-    const float mc = M == -INFINITY ? 0.f : M * c;
 
     // pass 2: fixed-point totals per (column, warp), then the slice total
     // (four columns' loads in flight at a time; the trip counts are CTA-uniform, so every lane
@@ -162,8 +233,8 @@ __global__ void __launch_bounds__(kSmpThreads) row_sample_kernel(SampleArgs a) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             if (e0 + i >= ncol) break;
-            float w[4];
-            const uint64_t t = warp_sum_fx(chunk_w(v[i], c, mc, w));
+            uint64_t w[4];
+            const uint64_t t = warp_sum_u64(M == -INFINITY ? 0ull : chunk_w(v[i], M, a, w));
             if (lane == 0) s_col[e0 + i][warp] = t;
         }
     }
@@ -171,7 +242,7 @@ __global__ void __launch_bounds__(kSmpThreads) row_sample_kernel(SampleArgs a) {
     if (warp == 0) {
         uint64_t t = 0;
         for (int i = lane; i < ncol * kSmpWarps; i += 32) t += s_col[i / kSmpWarps][i % kSmpWarps];
-        t = warp_sum_fx(t);
+        t = warp_sum_u64(t);
         if (lane == 0) s_tot = t;
     }
     cluster.sync();
@@ -232,27 +303,26 @@ __global__ void __launch_bounds__(kSmpThreads) row_sample_kernel(SampleArgs a) {
                     base += __shfl_sync(0xffffffffu, incl - v, l);
                     // lane within the warp: chunk q of the slice
                     const int q = col * kSmpThreads + l * 32 + lane;
-                    float w[4] = {0.f, 0.f, 0.f, 0.f};
-                    const uint64_t cv = q < nch ? chunk_w(load_chunk(row, lo, hi, q, vec), c, mc, w) : 0ull;
+                    uint64_t w[4] = {0ull, 0ull, 0ull, 0ull};
+                    const uint64_t cv = q < nch ? chunk_w(load_chunk(row, lo, hi, q, vec), M, a, w) : 0ull;
                     const uint64_t cincl = warp_incl_scan(cv);
                     int cl = claim_lane(cv, cincl, base, local, q < nch);
                     if (cl < 0) cl = 0;
                     if (lane == cl) {
-                        // inside the chunk: the float partial sums its total was formed from
+                        // inside the chunk: the exact prefix sums of its fixed-point weights
                         const uint64_t rem = local >= base + cincl - cv ? local - (base + cincl - cv) : 0ull;
-                        const float rr = float(rem) * (1.f / kFx40);
-                        const float a1 = w[0] + w[1], a2 = a1 + w[2], a3 = a2 + w[3];
+                        const uint64_t a1 = w[0] + w[1], a2 = a1 + w[2], a3 = a2 + w[3];
                         int lastp = 0;
-                        if (w[1] > 0.f) lastp = 1;
-                        if (w[2] > 0.f) lastp = 2;
-                        if (w[3] > 0.f) lastp = 3;
-                        const int i = (w[0] > 0.f && w[0] > rr)   ? 0
-                                      : (w[1] > 0.f && a1 > rr) ? 1
-                                      : (w[2] > 0.f && a2 > rr) ? 2
-                                      : (w[3] > 0.f && a3 > rr) ? 3
-                                                                : lastp;
+                        if (w[1] > 0) lastp = 1;
+                        if (w[2] > 0) lastp = 2;
+                        if (w[3] > 0) lastp = 3;
+                        const int i = (w[0] > 0 && w[0] > rem)   ? 0
+                                      : (w[1] > 0 && a1 > rem) ? 1
+                                      : (w[2] > 0 && a2 > rem) ? 2
+                                      : (w[3] > 0 && a3 > rem) ? 3
+                                                               : lastp;
                         const int tok = min(lo + 4 * q + i, hi - 1);  // in range even on a fallback
-                        const double lse = double(M) * a.inv_t + (ln_pos(double(total)) - kLn2_40);
+                        const double lse = double(M) * a.inv_t + (ln_pos(double(total)) - a.S * kLn2);
                         a.row_tok[o] = tok;
                         a.row_lc[o] = double(__ldg(row + tok)) * a.inv_t - lse;
                     }
@@ -263,7 +333,34 @@ __global__ void __launch_bounds__(kSmpThreads) row_sample_kernel(SampleArgs a) {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Self-test of the SFU exponential the draws use: the largest relative error of ex2.approx over
+// every float f with |f| <= 1/2 (the fractions weight_fx passes it), against the double-precision
+// exp2, as the bits of a non-negative float (atomicMax on them orders like the floats).
+__global__ void __launch_bounds__(256) exp2_error_kernel(uint32_t *out) {
+    float worst = 0.f;
+    const uint32_t top = 0x3f000000u;  // 0.5
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i <= 2ull * top + 1;
+         i += uint64_t(gridDim.x) * blockDim.x) {
+        const uint32_t mag = uint32_t(i >> 1);
+        const float f = __uint_as_float(mag | ((i & 1) ? 0x80000000u : 0u));
+        const double ref = exp2(double(f));
+        const double got = double(fast_exp2(f));
+        worst = fmaxf(worst, float(fabs(got - ref) / ref));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) worst = fmaxf(worst, __shfl_xor_sync(0xffffffffu, worst, off));
+    if ((threadIdx.x & 31) == 0) atomicMax(out, __float_as_uint(worst));
+}
+
 }  // namespace
+
+eagle_status exp2_error_launch(float *out, cudaStream_t stream) {
+    if (cudaMemsetAsync(out, 0, sizeof(float), stream) != cudaSuccess) return EAGLE_ERR_CUDA;
+    exp2_error_kernel<<<device_sm_count() * 8, 256, 0, stream>>>(reinterpret_cast<uint32_t *>(out));
+    if (cudaPeekAtLastError() != cudaSuccess) return EAGLE_ERR_CUDA;
+    note_launch();
+    return EAGLE_OK;
+}
 
 size_t row_sample_max_vocab() { return size_t(kSmpMaxSlice) * kSmpMaxSplits; }
 
@@ -291,7 +388,12 @@ eagle_status row_sample_launch(const float *draft, const float *u, int B, int R,
     sa.chunk = chunk;
     sa.out_R = out_R;
     sa.out_r0 = out_r0;
-    sa.c = kLog2e / tree_temp;
+    const double cd = 1.4426950408889634074 / double(tree_temp);
+    sa.c = float(cd);
+    sa.c_lo = float(cd - double(sa.c));
+    int lv = 0;  // ceil(log2 V)
+    while ((1l << lv) < long(V)) ++lv;
+    sa.S = 62 - lv;
     sa.inv_t = 1.0 / double(tree_temp);
     if (launch_pdl(row_sample_kernel, dim3(splits, R, B), dim3(kSmpThreads), 0, stream, unsigned(splits), sa) !=
         cudaSuccess)

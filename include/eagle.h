@@ -159,8 +159,10 @@ eagle_status eagle_build_tree(const eagle_tree_cfg *cfg, const float *draft_logi
  * child_u[b][r][j]; the children keep draw order, so creation order, frontier slots, the rerank
  * and every output are then as in eagle_build_tree.  Draft confidences (node_logv) are q at the
  * drawn tokens.  The draw is decided on exact fixed-point sums of the row's weights against its
- * maximum (units of 2^-40 of the maximum's weight); the fp64 definition can differ only where a
- * uniform lies within about 1e-6 of a CDF step.
+ * maximum (units of 2^-S of the maximum's weight, S = 62 - ceil(log2 vocab)), each weight's
+ * exponent formed without rounding error; the fp64 definition can differ only where a uniform
+ * lies within about 1e-7 of a CDF step (eagle_selftest_exp2_error bounds the one approximate
+ * factor).
  * Losslessness: with tree_temp equal to the verify temperature, verification of a tree whose
  * every expanded node keeps all k children (keep = topk + (depth-1) topk^2, or a static tree)
  * commits exactly the target distribution.  A rerank that keeps fewer nodes drops children by
@@ -380,6 +382,13 @@ int32_t eagle_last_launch_count(void);
  * eagle_get_device_status) and store the nanoseconds they waited into elapsed_ns[0] (the warp)
  * and elapsed_ns[1] (the thread), a DEVICE buffer of two uint64.  The context stays usable. */
 eagle_status eagle_selftest_wait_timeout(void *ws, uint64_t *elapsed_ns, cudaStream_t stream);
+
+/* Self-test of the exponential behind the sampled children (eagle_build_tree_sampled and the
+ * sampled static tree): the largest relative error of the SFU's 2^f over every float f with
+ * |f| <= 1/2, against the double-precision exp2, stored into max_rel_err[0] (a DEVICE float).
+ * The draws' CDF steps are off by at most half the weights' relative error plus V 2^-S (S =
+ * 62 - ceil(log2 V)); a test bounds the former with this.  One launch, tens of milliseconds. */
+eagle_status eagle_selftest_exp2_error(float *max_rel_err, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -379,10 +379,27 @@ def run_e2e(eg, lib, wl, rd: Round, outs, ws, stream, dev, steps, world) -> dict
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    # the host -> device ceiling: one copy of a round's input bytes from pinned memory, alone
+    hb = torch.empty(h2d // 4, dtype=torch.float32).pin_memory()
+    db = torch.empty(h2d // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        db.copy_(hb, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for _ in range(10):
+        db.copy_(hb, non_blocking=True)
+    c1.record()
+    torch.cuda.synchronize(dev)
+    peak = hb.numel() * 4 / (c0.elapsed_time(c1) / 10) / 1e6
+    achieved = h2d * steps / ms / 1e6
+    del hb, db
     return {"value": job_rate(steps, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "pipeline": "inputs copied on a second stream in the order the calls need them; two device "
-                        "input sets alternate between rounds"}
+                        "input sets alternate between rounds",
+            "roofline": {"bound": "h2d", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_source": "one pinned host -> device copy of a round's input bytes, timed alone"}}
 
 
 def run_kv_commit(eg, lib, wl, rd: Round, outs, ws, stream, dev, calls: int = 200) -> dict:

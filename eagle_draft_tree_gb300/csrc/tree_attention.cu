@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(32 * kWarps) tree_attn_bf16_kernel(AttnArgs a)
 }
 
 // fp32: a CTA per (unit, block of kF32Rows query rows), 256 threads.  The unit's keys (its
-// context, then the n tree keys) stream through shared memory in tiles of kF32Keys; thread t owns
+// context, then the n tree keys) stream through shared memory in tiles of kF32Keys, the next
+// tile's loads in flight (in registers) while the current one is used; thread t owns
 // query row t / 16 of the block: two of the tile's scores (keys t % 16 and t % 16 + 16, full dot
 // products from shared memory) and HD / 16 output columns (t % 16 + 16 c).  The 16 threads of a
 // row are one half-warp, so the row's online softmax (running max, rescale, running sum) meets by
@@ -378,35 +379,54 @@ __global__ void __launch_bounds__(kF32Threads) tree_attn_f32_kernel(AttnArgs a) 
     for (int c = 0; c < NO; ++c) o[c] = 0.f;
     float m = -INFINITY, lsum = 0.f;
     const int nk = ctx + a.n;  // the context's keys, then the tree's
+    // this thread's share of a tile: NL float4 of K and of V (zero past the unit's keys)
+    constexpr int NL = kF32Keys * (HD / 4) / kF32Threads;
+    float4 kr[NL], vr[NL];
+    auto load_tile = [&](int j0) {
+#pragma unroll
+        for (int u = 0; u < NL; ++u) {
+            const int i = tid + u * kF32Threads;
+            const int jj = i / (HD / 4), c4 = i % (HD / 4), j = j0 + jj;
+            kr[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            vr[u] = kr[u];
+            if (j < ctx) {
+                kr[u] = reinterpret_cast<const float4 *>(kc + size_t(j) * stride)[c4];
+                vr[u] = reinterpret_cast<const float4 *>(vc + size_t(j) * stride)[c4];
+            } else if (j < nk) {
+                kr[u] = reinterpret_cast<const float4 *>(kt + size_t(j - ctx) * stride)[c4];
+                vr[u] = reinterpret_cast<const float4 *>(vt + size_t(j - ctx) * stride)[c4];
+            }
+        }
+    };
+    load_tile(0);
     for (int j0 = 0; j0 < nk; j0 += kF32Keys) {
         __syncthreads();  // the previous tile is consumed (and, the first time, sQ is written)
-        for (int i = tid; i < kF32Keys * (HD / 4); i += kF32Threads) {
-            const int jj = i / (HD / 4), c4 = i % (HD / 4), j = j0 + jj;
-            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-            if (j < ctx) {
-                kv = reinterpret_cast<const float4 *>(kc + size_t(j) * stride)[c4];
-                vv = reinterpret_cast<const float4 *>(vc + size_t(j) * stride)[c4];
-            } else if (j < nk) {
-                kv = reinterpret_cast<const float4 *>(kt + size_t(j - ctx) * stride)[c4];
-                vv = reinterpret_cast<const float4 *>(vt + size_t(j - ctx) * stride)[c4];
-            }
-            sK[jj][4 * c4] = kv.x;
-            sK[jj][4 * c4 + 1] = kv.y;
-            sK[jj][4 * c4 + 2] = kv.z;
-            sK[jj][4 * c4 + 3] = kv.w;
-            *reinterpret_cast<float4 *>(&sV[jj][4 * c4]) = vv;
+#pragma unroll
+        for (int u = 0; u < NL; ++u) {
+            const int i = tid + u * kF32Threads;
+            const int jj = i / (HD / 4), c4 = i % (HD / 4);
+            sK[jj][4 * c4] = kr[u].x;
+            sK[jj][4 * c4 + 1] = kr[u].y;
+            sK[jj][4 * c4 + 2] = kr[u].z;
+            sK[jj][4 * c4 + 3] = kr[u].w;
+            *reinterpret_cast<float4 *>(&sV[jj][4 * c4]) = vr[u];
         }
         __syncthreads();
-        // two scores of this thread's row: keys sub and sub + 16 of the tile
+        if (j0 + kF32Keys < nk) load_tile(j0 + kF32Keys);  // in flight while this tile is used
+        // two scores of this thread's row: keys sub and sub + 16 of the tile (four partial sums
+        // a dot product, so its chain is a quarter as long)
         float s2[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int jj = sub + 16 * h, j = j0 + jj;
             const bool vis = rvalid && (j < ctx || (j < nk && ((tmask >> (j - ctx)) & 1ull)));
-            float acc = 0.f;
-#pragma unroll 16
-            for (int d = 0; d < HD; ++d) acc = fmaf(sQ[orow][d], sK[jj][d], acc);
-            s2[h] = vis ? acc : -INFINITY;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int d = 0; d < HD; d += 4) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = fmaf(sQ[orow][d + e], sK[jj][d + e], acc[e]);
+            }
+            s2[h] = vis ? (acc[0] + acc[1]) + (acc[2] + acc[3]) : -INFINITY;
         }
         // online softmax over the row's half-warp
         float tmx = fmaxf(s2[0], s2[1]);

@@ -27,7 +27,7 @@ import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
-ATTN_EVERY = 16  # timed steps per attention launch bracketed by CUDA events
+ATTN_EVERY = 16  # timed steps per attention launch bracketed by CUDA events (at most)
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
@@ -241,12 +241,13 @@ def run_ours(args, rank, world, dev) -> dict | None:
     torch.cuda.synchronize(dev)
     launches[0] = 0
     e0.record(stream)
-    # The attention launch is bracketed by events on every ATTN_EVERY-th step only: an event
-    # recorded between two launches ends the programmatic overlap of the round's kernels, which
-    # costs about 7 us on every bracketed round.
-    sampled = [i for i in range(K) if i % ATTN_EVERY == 0]
+    # The attention launch is bracketed by events on every `every`-th step only: an event recorded
+    # between two launches ends the programmatic overlap of the round's kernels, which costs about
+    # 7 us on every bracketed round.  Short runs bracket every 4th step (5 launches at K = 20).
+    every = max(4, min(ATTN_EVERY, K // 8))
+    sampled = [i for i in range(K) if i % every == 0]
     for i in range(K):
-        step(sets[i % len(sets)], attn_ev[i] if i % ATTN_EVERY == 0 else None)
+        step(sets[i % len(sets)], attn_ev[i] if i % every == 0 else None)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -297,7 +298,7 @@ def run_ours(args, rank, world, dev) -> dict | None:
                      "traffic": _traffic(attn_bytes) if wl.name == "llama31_8b" else None,
                      "kernel": "tree_attn_tc_kernel" if wl.kv_dtype == "bf16" else "tree_attn_f32_kernel",
                      "algorithmic_bytes": attn_bytes, "avg_launch_ms": attn_ms,
-                     "launch_samples": f"CUDA events around the attention launch of every {ATTN_EVERY}th timed "
+                     "launch_samples": f"CUDA events around the attention launch of every {every}th timed "
                                        f"step ({len(sampled)} launches)",
                      "frac_nominal": achieved / NOMINAL_HBM_GBS, "nominal_peak": NOMINAL_HBM_GBS,
                      "loop_check": _loop_check(attn_workloads, wl.name),

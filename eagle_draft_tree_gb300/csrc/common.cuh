@@ -93,6 +93,10 @@ __device__ __forceinline__ uint64_t warp_bitonic_merge32(uint64_t v) {
     return v;
 }
 
+// Query rows of one 128-row M-tile of the tensor-core tree attention: whole nodes only, so a tile
+// holds floor(128 / G) nodes of G query heads each (all 128 rows when G divides 128).
+__host__ __device__ __forceinline__ int attn_tc_rows_per_mtile(int G) { return (128 / G) * G; }
+
 // Orderable 64-bit image of a double (integer order = numeric order; -0 folded onto +0 by an
 // integer test, which keeps the narrow FP64 pipe out of it).
 __device__ __forceinline__ uint64_t double_order_key(double d) {

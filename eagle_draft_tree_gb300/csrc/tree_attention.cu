@@ -496,9 +496,12 @@ eagle_status launch_f32(const AttnArgs &a, cudaStream_t stream) {
 // context tiles are shared among several CTAs whose partial results a merge kernel combines
 // exactly; the workspace then holds the partials.
 int attn_tc_splits(const eagle_attn_cfg &c) {
-    if (c.dtype != EAGLE_DTYPE_BF16 || c.head_dim != 128 || c.heads_kv < 1 || c.heads_q % c.heads_kv) return 1;
+    if (c.dtype != EAGLE_DTYPE_BF16 || c.head_dim != 128 || c.heads_kv < 1 || c.heads_q % c.heads_kv ||
+        c.heads_q / c.heads_kv > 128)
+        return 1;
     const long rows = long(c.heads_q / c.heads_kv) * c.nodes;
-    const long units = long(c.layers) * c.batch * c.heads_kv * ((rows + 255) / 256);
+    const long cta_rows = 2L * attn_tc_rows_per_mtile(c.heads_q / c.heads_kv);
+    const long units = long(c.layers) * c.batch * c.heads_kv * ((rows + cta_rows - 1) / cta_rows);
     const long sms = device_sm_count();
     if (units * 2 > sms) return 1;
     const long nctx = (long(c.max_seq) + 127) / 128;
@@ -510,7 +513,8 @@ int attn_tc_splits(const eagle_attn_cfg &c) {
 
 size_t attn_tc_partial_rows(const eagle_attn_cfg &c, int splits) {
     const long rows = long(c.heads_q / c.heads_kv) * c.nodes;
-    return size_t(c.layers) * c.batch * c.heads_kv * ((rows + 255) / 256) * splits * 256;
+    const long cta_rows = 2L * attn_tc_rows_per_mtile(c.heads_q / c.heads_kv);
+    return size_t(c.layers) * c.batch * c.heads_kv * ((rows + cta_rows - 1) / cta_rows) * splits * 256;
 }
 
 size_t tree_attention_workspace_bytes(const eagle_attn_cfg &c) {
@@ -559,7 +563,7 @@ eagle_status tree_attention_launch(const eagle_attn_cfg &c, const void *q, const
             tp.G = a.G;
             tp.S_max = a.S_max;
             tp.rows = a.rows;
-            tp.mgroups = (a.rows + 255) / 256;
+            tp.mgroups = (a.rows + 2 * attn_tc_rows_per_mtile(a.G) - 1) / (2 * attn_tc_rows_per_mtile(a.G));
             tp.scale_log2 = a.scale_log2;
             tp.splits = attn_tc_splits(c);
             tp.part_ml = nullptr;

@@ -4,9 +4,11 @@
 // scored in one target pass and every candidate sees only its ancestors and the context; and
 // "(EAGLE 2) EAGLE-2 ..." section "Tree Attention Mask".
 //
-// One CTA = one (layer, sequence, KV head) unit and up to two 128-row M-tiles of its query block
-// (row r = node * G + head-in-group).  The context streams through in 128-key tiles; the n <= 64
-// tree keys form one last tile whose visibility is the node's ancestor bit mask.
+// One CTA = one (layer, sequence, KV head) unit and up to two M-tiles of its query block (row
+// r = node * G + head-in-group); an M-tile holds floor(128 / G) whole nodes, all 128 TMEM lanes
+// when G divides 128, else G floor(128 / G) of them and a few padding lanes that nothing reads.
+// The context streams through in 128-key tiles; the n <= 64 tree keys form one last tile whose
+// visibility is the node's ancestor bit mask.
 //
 //   warp 0     TMA producer: Q once (two 64-column halves per M-tile), then K and V tiles (one
 //              4-D box per tile: 128 keys x both 64-dim halves, 128B-swizzled) through a 2-stage K
@@ -262,8 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && mg == 0 && g == 0) set_status(p.status, EAGLE_ERR_DEVICE_INPUT);
         return;  // uniform for the CTA: nothing allocated yet
     }
-    const int row0 = mg * 256;                          // first query row of this CTA
-    const int tm = min(2, (p.rows - row0 + 127) / 128);  // M-tiles in this CTA (1 or 2)
+    const int npt = 128 / p.G, rpt = npt * p.G;            // nodes and query rows of an M-tile
+    const int row0 = mg * 2 * rpt;                         // first query row of this CTA
+    const int tm = min(2, (p.rows - row0 + rpt - 1) / rpt);  // M-tiles in this CTA (1 or 2)
     const int nctx = (ctx + kNkv - 1) / kNkv;            // context tiles
     const int jtail = (ctx % kNkv) ? nctx - 1 : -1;      // the ragged context tile, if any
     // This CTA's share of the unit's tiles: context tiles [c0, c1), and the tree tile in the last
@@ -319,10 +322,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- TMA producer: two rings, issued whenever a stage is free ----------------
         if (lane == 0) {
             const int zq = (l * p.B + b) * p.n + row0 / p.G;  // first node of this CTA's rows
-            mbar_expect_tx(&bars.q_full, uint32_t(tm) * kQTile);
+            // an M-tile's box is rpt rows high (rows rpt .. 127 of its buffer are padding whose
+            // scores and outputs no row reads)
+            mbar_expect_tx(&bars.q_full, uint32_t(tm) * 2u * uint32_t(rpt) * 128u);
             for (int t = 0; t < tm; ++t)
                 for (int h = 0; h < 2; ++h)
-                    tma_3d(&qmap, sm + t * kQTile + h * kQHalf, &bars.q_full, 64 * h, g * p.G, zq + t * (128 / p.G));
+                    tma_3d(&qmap, sm + t * kQTile + h * kQHalf, &bars.q_full, 64 * h, g * p.G, zq + t * npt);
             const int zc = (l * p.B + b) * p.S_max;
             const int zt = (l * p.B + b) * p.n;
             const uint64_t pol = l2_evict_first_policy();
@@ -412,8 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = (warp - 4) >> 2;
         const int wq = warp & 3;  // TMEM lane quarter of this warp
         const int rho = wq * 32 + lane;
-        const int r = row0 + t * 128 + rho;
-        const bool valid = r < p.rows;
+        const int r = row0 + t * rpt + rho;
+        const bool valid = rho < rpt && r < p.rows;
         const int node = valid ? r / p.G : 0;
         const int gh = valid ? r % p.G : 0;
         const uint64_t tmask = valid ? p.mask[size_t(b) * p.n + node] : 0ull;
@@ -638,8 +643,10 @@ __global__ void __launch_bounds__(256) tree_attn_merge_kernel(AttnTcParams p) {
     const int g = int(unit % p.Hkv), b = int((unit / p.Hkv) % p.B), l = int(unit / (long(p.Hkv) * p.B));
     const int ctx = p.ctx_len[b];
     if (ctx < 0 || ctx > p.S_max) return;  // flagged by the main kernel; the rows stay unwritten
-    const int mg = r / 256, rin = r % 256;
-    auto prow = [&](int s) { return ((size_t(unit) * p.splits + s) * p.mgroups + mg) * 256 + rin; };
+    const int rpt = attn_tc_rows_per_mtile(p.G);
+    const int mg = r / (2 * rpt), rin = r % (2 * rpt);
+    const int pin = (rin / rpt) * 128 + rin % rpt;  // M-tile and lane of the row in its CTA's partial
+    auto prow = [&](int s) { return ((size_t(unit) * p.splits + s) * p.mgroups + mg) * 256 + pin; };
     // lane s < splits: split s's (max, sum), all loaded at once; the weights by warp reduction
     float ms = -INFINITY, ls = 0.f;
     if (lane < p.splits) {
@@ -726,7 +733,7 @@ bool make_kv_map(CUtensorMap *map, const void *base, uint64_t heads, uint64_t ro
 
 // True when the tensor-core kernel handles this configuration.
 bool tree_attention_tc_supported(int head_dim, int dtype, int G, int S_max) {
-    return dtype == EAGLE_DTYPE_BF16 && head_dim == 128 && G >= 1 && 128 % G == 0 && S_max >= 1 &&
+    return dtype == EAGLE_DTYPE_BF16 && head_dim == 128 && G >= 1 && G <= 128 && S_max >= 1 &&
            encode_fn() != nullptr;
 }
 

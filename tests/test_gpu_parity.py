@@ -79,6 +79,11 @@ ATTN_CASES = [
     (1, 2, 49, 16, 2, 128, [300, 5], "bf16"),
     (2, 2, 20, 6, 6, 64, [77, 128], "bf16"),
     (1, 1, 51, 2, 2, 128, [1000], "bf16"),
+    # query-head groups that do not divide 128: an M-tile holds floor(128 / G) whole nodes
+    (2, 2, 61, 40, 8, 128, [300, 129], "bf16"),  # G = 5: 125-row tiles, a CTA's second tile partial
+    (1, 2, 64, 21, 3, 128, [257, 0], "bf16"),    # G = 7: 126-row tiles, two CTAs a unit
+    (1, 1, 30, 24, 8, 128, [130], "bf16"),       # G = 3: one 90-row tile
+    (1, 1, 61, 40, 8, 128, [2048], "bf16"),      # G = 5 with the context split and its merge
 ]
 
 

@@ -492,14 +492,15 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     };
     const bool bulkA = bulk_ok(rowA), bulkB = bulk_ok(rowB);
     // The first child is the one most often accepted; when it is a leaf the walk may end there
-    // and need its bonus draw, so its target row's slice follows the node's own two rows in
-    // (used only if that child is accepted; the CTA waits for it before leaving either way).
+    // and need its bonus draw, so its target row's slice follows the node's own two rows in,
+    // issued once those have landed so that it does not share their bandwidth (used only if that
+    // child is accepted; the CTA waits for it before leaving either way).
+    const float *rowP = nullptr;
     if (tid == 0) {
         const int pre = (!a.greedy && !a.bonus_mode && !a.full_chain && has_q && ((s_leaves >> s_kid[0]) & 1ull))
                             ? s_kid[0] : -1;
-        const float *rowP = pre >= 0 ? a.target + (size_t(b) * n + pre) * V + lo : nullptr;
-        const bool bulkP = bulk_ok(rowP);
-        s_pre = bulkP ? pre : -1;
+        rowP = pre >= 0 ? a.target + (size_t(b) * n + pre) * V + lo : nullptr;
+        s_pre = bulk_ok(rowP) ? pre : -1;
         if (bulkA) {
             mbar_expect_tx(&s_lbar[0], uint32_t(cnt) * 4u);
             bulk_g2s(s_rows, rowA, uint32_t(cnt) * 4u, &s_lbar[0]);
@@ -507,10 +508,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         if (bulkB) {
             mbar_expect_tx(&s_lbar[1], uint32_t(cnt) * 4u);
             bulk_g2s(s_rows + kSliceMax, rowB, uint32_t(cnt) * 4u, &s_lbar[1]);
-        }
-        if (bulkP) {
-            mbar_expect_tx(&s_lbar[2], uint32_t(cnt) * 4u);
-            bulk_g2s(s_rows + 2 * kSliceMax, rowP, uint32_t(cnt) * 4u, &s_lbar[2]);
         }
     }
     // every final draw uses the sequence's first uniform (the root's, which no accept test uses)
@@ -535,6 +532,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     if (bulkB) {
         wait_slice(1);
         read_chunks(xq, s_rows + kSliceMax, cnt);
+    }
+    if (tid == 0 && s_pre >= 0) {  // the first child's slice, now that the node's own have landed
+        mbar_expect_tx(&s_lbar[2], uint32_t(cnt) * 4u);
+        bulk_g2s(s_rows + 2 * kSliceMax, rowP, uint32_t(cnt) * 4u, &s_lbar[2]);
     }
 
     // One pass = one exchange.  Every warp leaves its partial in s_wp[warp] and arrives on s_pbar;

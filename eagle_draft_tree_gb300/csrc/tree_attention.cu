@@ -32,6 +32,7 @@ struct AttnTcParams {
     __nv_bfloat16 *out;
     int32_t *status;
     int L, B, n, Hq, Hkv, G, S_max, rows, mgroups;
+    int HD;
     float scale_log2;
     int splits;
     float *part_o;
@@ -496,7 +497,7 @@ eagle_status launch_f32(const AttnArgs &a, cudaStream_t stream) {
 // context tiles are shared among several CTAs whose partial results a merge kernel combines
 // exactly; the workspace then holds the partials.
 int attn_tc_splits(const eagle_attn_cfg &c) {
-    if (c.dtype != EAGLE_DTYPE_BF16 || c.head_dim != 128 || c.heads_kv < 1 || c.heads_q % c.heads_kv ||
+    if (c.dtype != EAGLE_DTYPE_BF16 || (c.head_dim != 128 && c.head_dim != 64) || c.heads_kv < 1 || c.heads_q % c.heads_kv ||
         c.heads_q / c.heads_kv > 128)
         return 1;
     const long rows = long(c.heads_q / c.heads_kv) * c.nodes;
@@ -563,6 +564,7 @@ eagle_status tree_attention_launch(const eagle_attn_cfg &c, const void *q, const
             tp.G = a.G;
             tp.S_max = a.S_max;
             tp.rows = a.rows;
+            tp.HD = c.head_dim;
             tp.mgroups = (a.rows + 2 * attn_tc_rows_per_mtile(a.G) - 1) / (2 * attn_tc_rows_per_mtile(a.G));
             tp.scale_log2 = a.scale_log2;
             tp.splits = attn_tc_splits(c);

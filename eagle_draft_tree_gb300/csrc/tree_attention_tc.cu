@@ -48,6 +48,7 @@ struct AttnTcParams {  // same layout as the declaration in tree_attention.cu
     __nv_bfloat16 *out;
     int32_t *status;
     int L, B, n, Hq, Hkv, G, S_max, rows, mgroups;
+    int HD;         // head dimension: 128, or 64 (run as 128 with a zero upper half)
     float scale_log2;
     int splits;     // context splits per unit (1: each CTA writes its rows' output itself)
     float *part_o;  // splits > 1: [unit][split][mgroup][256 rows][128] unnormalised partial O
@@ -573,6 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float4 *po = reinterpret_cast<float4 *>(p.part_o + pr * 128);
 #pragma unroll
             for (int cc = 0; cc < 128; cc += 16) {
+                if (cc >= p.HD) break;
                 uint32_t o[16];
                 tld16(tO + cc, o);
                 tld_wait();
@@ -589,9 +591,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (!kSplit && ok && warp_wait(&bars.o_done[t], 0, abort_flag, p.status)) {
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-            __nv_bfloat16 *orow = p.out + ((((size_t)l * p.B + b) * p.n + node) * p.Hq + g * p.G + gh) * 128;
+            __nv_bfloat16 *orow = p.out + ((((size_t)l * p.B + b) * p.n + node) * p.Hq + g * p.G + gh) * p.HD;
 #pragma unroll
             for (int cc = 0; cc < 128; cc += 16) {
+                if (cc >= p.HD) break;  // d = 64: the upper half of O is the zero padding's
                 uint32_t o[16];
                 tld16(tO + cc, o);
                 tld_wait();
@@ -680,7 +683,8 @@ __global__ void __launch_bounds__(256) tree_attn_merge_kernel(AttnTcParams p) {
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
     const int node = r / p.G, gh = r % p.G;
-    __nv_bfloat16 *orow = p.out + ((((size_t)l * p.B + b) * p.n + node) * p.Hq + g * p.G + gh) * 128;
+    __nv_bfloat16 *orow = p.out + ((((size_t)l * p.B + b) * p.n + node) * p.Hq + g * p.G + gh) * p.HD;
+    if (4 * lane >= p.HD) return;  // d = 64: lanes 16 .. 31 hold the zero padding
     const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
     const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     reinterpret_cast<uint2 *>(orow)[lane] =
@@ -700,13 +704,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 3-D map over a [outer][mid][128] bf16 tensor with a {64, box_mid, box_outer} 128B-swizzled box
-bool make_map(CUtensorMap *map, const void *base, uint64_t mid, uint64_t outer, uint32_t box_mid,
+// 3-D map over a [outer][mid][hd] bf16 tensor with a {64, box_mid, box_outer} 128B-swizzled box
+// (hd = 64: a box at x = 64 lies past the tensor and lands as zeros)
+bool make_map(CUtensorMap *map, const void *base, uint64_t hd, uint64_t mid, uint64_t outer, uint32_t box_mid,
               uint32_t box_outer) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {128, mid, outer};
-    cuuint64_t strides[2] = {128 * 2, mid * 128 * 2};
+    cuuint64_t dims[3] = {hd, mid, outer};
+    cuuint64_t strides[2] = {hd * 2, mid * hd * 2};
     cuuint32_t box[3] = {64, box_mid, box_outer};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
@@ -714,14 +719,15 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t mid, uint64_t outer, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 4-D map over a [rows][heads][128] bf16 tensor seen as {64 elems, rows, 2 halves, heads} (strides
-// out of order) with a {64, box_rows, box_halves, 1} 128B-swizzled box.
-bool make_kv_map(CUtensorMap *map, const void *base, uint64_t heads, uint64_t rows, uint32_t box_rows,
+// 4-D map over a [rows][heads][hd] bf16 tensor seen as {64 elems, rows, hd / 64 halves, heads}
+// (strides out of order) with a {64, box_rows, box_halves, 1} 128B-swizzled box (hd = 64: the
+// second half of a two-half box lies past the tensor and lands as zeros).
+bool make_kv_map(CUtensorMap *map, const void *base, uint64_t hd, uint64_t heads, uint64_t rows, uint32_t box_rows,
                  uint32_t box_halves) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[4] = {64, rows, 2, heads};
-    cuuint64_t strides[3] = {heads * 128 * 2, 128, 128 * 2};
+    cuuint64_t dims[4] = {64, rows, hd / 64, heads};
+    cuuint64_t strides[3] = {heads * hd * 2, 128, hd * 2};
     cuuint32_t box[4] = {64, box_rows, box_halves, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, es,
@@ -733,7 +739,7 @@ bool make_kv_map(CUtensorMap *map, const void *base, uint64_t heads, uint64_t ro
 
 // True when the tensor-core kernel handles this configuration.
 bool tree_attention_tc_supported(int head_dim, int dtype, int G, int S_max) {
-    return dtype == EAGLE_DTYPE_BF16 && head_dim == 128 && G >= 1 && G <= 128 && S_max >= 1 &&
+    return dtype == EAGLE_DTYPE_BF16 && (head_dim == 128 || head_dim == 64) && G >= 1 && G <= 128 && S_max >= 1 &&
            encode_fn() != nullptr;
 }
 
@@ -741,9 +747,11 @@ eagle_status tree_attention_tc_launch(const AttnTcParams &p, const void *q, cons
                                       const void *k_tree, const void *v_tree, cudaStream_t stream) {
     CUtensorMap qm, km, vm, ktm, vtm;
     const uint64_t LB = uint64_t(p.L) * p.B;
-    if (!make_map(&qm, q, p.Hq, LB * p.n, p.G, 128 / p.G) || !make_kv_map(&km, k_cache, p.Hkv, LB * p.S_max, kNkv, 2) ||
-        !make_kv_map(&vm, v_cache, p.Hkv, LB * p.S_max, kNkv, 2) || !make_kv_map(&ktm, k_tree, p.Hkv, LB * p.n, kNkv, 2) ||
-        !make_kv_map(&vtm, v_tree, p.Hkv, LB * p.n, kNkv, 2))
+    const uint64_t hd = uint64_t(p.HD);
+    if (!make_map(&qm, q, hd, p.Hq, LB * p.n, p.G, 128 / p.G) ||
+        !make_kv_map(&km, k_cache, hd, p.Hkv, LB * p.S_max, kNkv, 2) ||
+        !make_kv_map(&vm, v_cache, hd, p.Hkv, LB * p.S_max, kNkv, 2) ||
+        !make_kv_map(&ktm, k_tree, hd, p.Hkv, LB * p.n, kNkv, 2) || !make_kv_map(&vtm, v_tree, hd, p.Hkv, LB * p.n, kNkv, 2))
         return EAGLE_ERR_UNSUPPORTED;  // the caller falls back to the mma.sync kernel
     static std::atomic<uint64_t> ready{0};
     const size_t smem = kSmemBytes + 1024;

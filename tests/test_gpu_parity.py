@@ -84,6 +84,9 @@ ATTN_CASES = [
     (1, 2, 64, 21, 3, 128, [257, 0], "bf16"),    # G = 7: 126-row tiles, two CTAs a unit
     (1, 1, 30, 24, 8, 128, [130], "bf16"),       # G = 3: one 90-row tile
     (1, 1, 61, 40, 8, 128, [2048], "bf16"),      # G = 5 with the context split and its merge
+    # d = 64 on the tensor cores (a zero upper half through the tensor maps' out-of-range fill)
+    (2, 2, 61, 32, 8, 64, [300, 129], "bf16"),
+    (1, 1, 40, 16, 4, 64, [2048], "bf16"),        # with the context split
 ]
 
 
@@ -120,6 +123,17 @@ def test_tree_attention_matches_oracle(case):
     got = out.float().cpu().numpy().astype(np.float64)
     err = np.abs(got - ref).max()
     assert err <= ATTN_TOL[dtype], err
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bf16_attention_takes_the_tensor_core_path(d):
+    """Few units: the tensor-core kernel splits the context and merges (two launches); the
+    mma.sync kernel it would otherwise fall back to is one launch."""
+    wl, inp, mask = _attn_inputs(1, 1, 40, 16, 4, d, [2048], "bf16", seed=5)
+    mask_t = torch.from_numpy(mask.reshape(1, 40).view(np.int64).copy()).to(DEV)
+    eg.tree_attention(inp["q"], inp["k_cache"], inp["v_cache"], inp["ctx_len"], inp["k_tree"], inp["v_tree"], mask_t)
+    torch.cuda.synchronize()
+    assert eg.last_launch_count() == 2
 
 
 @pytest.mark.parametrize("case", [c for c in ATTN_CASES if min(c[6]) < max(c[6])],

@@ -28,6 +28,9 @@ BUILD_SHAPES = [
     (1, 1000, 3, 4, 10), (3, 1000, 3, 4, 10), (2, 32000, 6, 10, 50), (2, 128256, 8, 10, 60),
     (4, 16, 2, 3, 12), (2, 500, 1, 5, 5), (2, 300, 5, 1, 5), (2, 4096, 4, 16, 63), (5, 777, 3, 7, 30),
     (2, 2048, 2, 2, 1), (2, 300, 64, 1, 63), (1, 2000, 11, 10, 63),
+    # the full vocabulary over 101 rows (the largest pool at k = 10) and a depth-64 chain, and
+    # 304 rows in all
+    (1, 128256, 11, 10, 63), (1, 128256, 64, 1, 63), (4, 2000, 16, 5, 60),
 ]
 
 

@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     __shared__ float s_uk[kMaxNodes];            // each child's uniform
     __shared__ int s_dec[2];                     // the accept test of the current child, by parity
     __shared__ __align__(8) uint64_t s_decbar;   // s_dec written
-    __shared__ int s_nk, s_fail, s_second;
+    __shared__ int s_nk, s_fail, s_second, s_y;
     __shared__ uint64_t s_leaves;  // the tree's leaves (nodes without children), one bit each
     __shared__ int s_acc;          // the child at which the chain stopped (accepted)
     __shared__ int s_pre;          // the child whose target row slice was prefetched, or -1
@@ -400,20 +400,20 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = int(cluster.block_rank());
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = a.n, V = a.V, b = blockIdx.z;
+    const int n = a.n, V = a.V, b = blockIdx.y;
     const int lo = rank * a.slice;
     const int hi = min(V, lo + a.slice);
     const int cnt = hi > lo ? hi - lo : 0;
     const int32_t *par = a.parents + size_t(b) * n;
 
-    // ---- work of this cluster.  Greedy: nodes 2y and 2y + 1 (argmax of two target rows).
-    // Sampling: node y when it has children (a leaf's cluster exits).  Bonus mode: the leaf the
-    // walk ended at, if any (written by the walk, the launch before this one).
-    const int breq = a.bonus_mode ? __ldg(a.bonus + blockIdx.z) : -1;
+    // ---- work of this cluster (cluster index s = blockIdx.z, sequence b = blockIdx.y).  Greedy:
+    // nodes 2s and 2s + 1 (argmax of two target rows).  Sampling: the s-th working node in index
+    // order, a node with children or the root (found by the tree scan below; clusters past the
+    // last working node exit), so that the clusters with work are the first ones the GPU places.
+    // Bonus mode: the leaf the walk ended at, if any (written by the walk, the launch before this).
+    const int breq = a.bonus_mode ? __ldg(a.bonus + blockIdx.y) : -1;
     if (a.bonus_mode && breq < 0) return;  // uniform for the cluster: nothing has started
-    const int y = a.bonus_mode ? (breq & 255) : int(blockIdx.y);
-    const int nodeA = a.greedy ? 2 * y : y;
-    const int nrow = a.greedy ? -1 : __ldg(a.node_row + size_t(b) * n + nodeA);
+    const int cs = int(blockIdx.z);
     // The barriers exist before anything else, and the cluster barrier that publishes them to the
     // peers is arrived at now and waited on only before the first exchange, so its latency hides
     // behind the tree scan, the slice copies and the first register pass.
@@ -434,9 +434,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
             s_second = -1;
             s_fail = 0;
             s_own[0] = -1;
+            s_y = breq & 255;
         }
     } else if (warp == 0) {
-        // every node's "has children" bit, and the children of node y, from the <= 64 parents
+        // every node's "has children" bit, this cluster's node y, and its children, from the <= 64
+        // parents
         const int p0 = lane < n ? __ldg(par + lane) : -1;
         const int p1 = lane + 32 < n ? __ldg(par + lane + 32) : -1;
         uint64_t mine = 0;
@@ -447,17 +449,26 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
         const uint64_t internal = (uint64_t(mh) << 32) | ml;
         const uint64_t all = n >= 64 ? ~0ull : ((1ull << n) - 1ull);
         const uint64_t leaves = all & ~internal;
-        const bool k0 = lane > 0 && p0 == y, k1 = p1 == y;
+        int y = a.greedy ? cs : -1;
+        if (!a.greedy) {
+            // working nodes: those with children, and the root unless every ratio is wanted (it
+            // then has its own draw only when it has children)
+            uint64_t work = internal | (a.full_chain ? 0ull : 1ull);
+            if (cs < __popcll(work)) {
+                for (int i = 0; i < cs; ++i) work &= work - 1ull;  // drop the cs lowest working nodes
+                y = __ffsll(static_cast<long long>(work)) - 1;
+            }
+        }
+        const bool k0 = y >= 0 && lane > 0 && p0 == y, k1 = y >= 0 && p1 == y;
         const unsigned b0 = __ballot_sync(0xffffffffu, k0), b1 = __ballot_sync(0xffffffffu, k1);
         if (k0) s_kid[__popc(b0 & ((1u << lane) - 1u))] = lane;
         if (k1) s_kid[__popc(b0) + __popc(b1 & ((1u << lane) - 1u))] = lane + 32;
         if (lane == 0) {
             s_nk = __popc(b0) + __popc(b1);
             int second = -1;  // greedy: the paired node (-2: this cluster has no work)
-            // a leaf's cluster has no work, except the root's when the root has no children and
-            // the prep makes the leaves' draws (its final token is drawn from its target row)
-            if (!a.greedy && ((leaves >> y) & 1ull) && !(y == 0 && !a.full_chain)) second = -2;
+            if (!a.greedy && y < 0) second = -2;  // past the last working node
             s_leaves = leaves;
+            s_y = y < 0 ? 0 : y;
             if (a.greedy) second = 2 * y + 1 < n ? 2 * y + 1 : -1;
             s_second = second;
             s_fail = 0;
@@ -467,6 +478,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1) verify_prep_kernel(VerifyArgs
     __syncthreads();
     const int second = s_second;
     if (second == -2) return;  // uniform for the cluster: no exchange or copy has started
+    const int nodeA = a.greedy ? 2 * cs : s_y;
+    const int nrow = a.greedy ? -1 : __ldg(a.node_row + size_t(b) * n + nodeA);
     const int J = a.greedy ? 0 : s_nk;
     const int nodeB = a.greedy ? second : -1;  // greedy: the paired node
     const int rowq = J > 0 ? nrow : -1;
@@ -1035,7 +1048,7 @@ cudaError_t launch_prep(const VerifyArgs &a, int clusters, int batch, cudaStream
         return r;
     });
     if (e != cudaSuccess) return e;
-    return launch_pdl(verify_prep_kernel<CL>, dim3(CL, clusters, batch), dim3(kPrepThreads), kPrepSmem, stream,
+    return launch_pdl(verify_prep_kernel<CL>, dim3(CL, batch, clusters), dim3(kPrepThreads), kPrepSmem, stream,
                       unsigned(CL), a);
 }
 }  // namespace
@@ -1083,7 +1096,9 @@ eagle_status tree_verify_launch(const eagle_verify_cfg &c, const float *target, 
     int slice = (c.vocab + cl - 1) / cl;
     slice = (slice + 3) & ~3;
     a.slice = slice;
-    const int clusters = a.greedy ? (n + 1) / 2 : n;  // sampling: one per node, leaves' clusters idle
+    // sampling: one per node at most (the working nodes take the first clusters, the rest exit);
+    // grid (CL, B, clusters), so that every sequence's working clusters come before idle ones
+    const int clusters = a.greedy ? (n + 1) / 2 : n;
     cudaError_t e = cl == 8 ? launch_prep<8>(a, clusters, c.batch, stream) : launch_prep<16>(a, clusters, c.batch, stream);
     if (e != cudaSuccess) return EAGLE_ERR_CUDA;
     note_launch();

@@ -251,6 +251,40 @@ def test_tree_verify_bonus_token_at_a_leaf(shape, T, with_ratio):
         assert int(g["out_tokens"][b][L - 1]) >= 0
 
 
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_tree_verify_repeated_calls_on_a_stale_workspace(T):
+    """Repeated calls on one workspace, and calls on a workspace whose body holds stale bytes
+    (another call's scratch), commit the same tokens; launches: the prep and the walk, plus the
+    bonus launch when sampling with every ratio wanted."""
+    wl = datagen.WORKLOADS["tiny_f32"].with_(batch=3, vocab=32000, depth=6, topk=10, keep=50)
+    seed = 5
+    draft, root = _draft(wl, seed)
+    o_tree = oracle.build_tree(np_(draft), np_(root), wl.depth, wl.topk, wl.keep)
+    target = datagen.target_logits(draft, torch.from_numpy(o_tree["node_row"]).to(DEV),
+                                   datagen.noise_sigmas(wl, seed), seed)
+    u = datagen.uniforms(wl.batch, wl.nodes, seed, DEV)
+    tree = oracle_tree_tensors(o_tree, DEV)
+    ws = eg.Workspace()
+    args = (target, draft, tree, u)
+    kw = dict(temperature=T, depth=wl.depth, topk=wl.topk, ws=ws)
+    ref = eg.tree_verify(*args, with_ratio=True, **kw)
+    assert eg.last_launch_count() == (2 if T == 0.0 else 3)
+    ref = {k: v.clone() for k, v in ref.items() if v is not None}
+    o = oracle.tree_verify(np_(target), np_(draft), o_tree["tokens"], o_tree["parents"], o_tree["node_row"], np_(u),
+                           T, wl.depth + 1)
+    o["parents"] = o_tree["parents"]
+    compare_verify({k: np_(v) for k, v in ref.items()}, o)
+    for fill in (None, None, 0xFF, 0x00, 0x5A):
+        if fill is not None:  # everything past the status header
+            off = ws.ptr.value - ws.buf.data_ptr()
+            ws.buf[off + 256:].fill_(fill)
+        g = eg.tree_verify(*args, with_ratio=False, **kw)
+        assert eg.last_launch_count() == 2
+        for key in ("out_tokens", "out_len", "out_path"):
+            assert torch.equal(g[key], ref[key]), (fill, key)
+    assert ws.status() == eg.EAGLE_OK
+
+
 def test_tree_verify_bad_tree_sets_status():
     wl = datagen.WORKLOADS["tiny_f32"].with_(batch=2)
     draft, root = _draft(wl, 1)

@@ -19,7 +19,8 @@
 // the tree reduces to comparisons of uniforms with precomputed ratios.
 //
 //   verify_prep_kernel  one cluster of CL CTAs (8, or 16 for vocabularies above 131072) per node
-//                       with children (sampling; greedy: per pair of nodes).  Each CTA bulk-copies
+//                       with children (sampling, working nodes first; greedy: per pair of nodes).
+//                       Each CTA bulk-copies
 //                       its slices of the node's target and draft rows into shared memory; thread
 //                       t takes 8 chunks of 4 tokens, chunk e at token 4 (t + 512 e) of the slice,
 //                       into registers.  Log-sum-exp, the S_j passes and the inverse-CDF scan are

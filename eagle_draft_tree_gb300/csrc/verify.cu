@@ -21,9 +21,8 @@
 //   verify_prep_kernel  one cluster of CL CTAs (8, or 16 for vocabularies above 131072) per node
 //                       with children (sampling, working nodes first; greedy: per pair of nodes).
 //                       Each CTA bulk-copies its slices of the node's target and draft rows into
-//                       shared memory; thread
-//                       t takes 8 chunks of 4 tokens, chunk e at token 4 (t + 512 e) of the slice,
-//                       into registers.  Log-sum-exp, the S_j passes and the inverse-CDF scan are
+//                       shared memory; thread t takes 8 chunks of 4 tokens, chunk e at token
+//                       4 (t + 512 e) of the slice, into registers.  Log-sum-exp, the S_j passes and the inverse-CDF scan are
 //                       register loops; each CTA reduces a pass to one record and pushes it to
 //                       every peer (st.async completing on the receiver's mbarrier), so a pass
 //                       costs one point-to-point exchange, not a cluster-wide barrier.  A chain

@@ -21,18 +21,18 @@
 //   verify_prep_kernel  one cluster of CL CTAs (8, or 16 for vocabularies above 131072) per node
 //                       with children (sampling, working nodes first; greedy: per pair of nodes).
 //                       Each CTA bulk-copies its slices of the node's target and draft rows into
-//                       shared memory; thread t takes 8 chunks of 4 tokens, chunk e at token
-//                       4 (t + 512 e) of the slice, into registers.  Log-sum-exp, the S_j passes and the inverse-CDF scan are
-//                       register loops; each CTA reduces a pass to one record and pushes it to
-//                       every peer (st.async completing on the receiver's mbarrier), so a pass
-//                       costs one point-to-point exchange, not a cluster-wide barrier.  A chain
-//                       stops at its first accepted child.  When that child is a leaf the walk may
-//                       end there, so the cluster also draws the leaf's bonus token from the
-//                       leaf's target row (the first child's row slice is prefetched with the
-//                       node's own rows, as it is the one usually accepted); the root without
-//                       children draws its own final token.  Per-node statistics (row maxima, log
-//                       normalisers, each child's c_j and S_j with the prep's verdict) and the
-//                       draws go to the workspace.
+//                       shared memory; thread t takes 8 chunks of 4 tokens, chunk e at token 4 (t +
+//                       512 e) of the slice, into registers.  Log-sum-exp, the S_j passes and the
+//                       inverse-CDF scan are register loops; each CTA reduces a pass to one record
+//                       and pushes it to every peer (st.async completing on the receiver's
+//                       mbarrier), so a pass costs one point-to-point exchange, not a cluster-wide
+//                       barrier.  A chain stops at its first accepted child.  When that child is a
+//                       leaf the walk may end there, so the cluster also draws the leaf's bonus
+//                       token from the leaf's target row (the first child's row slice is prefetched
+//                       with the node's own rows, as it is the one usually accepted); the root
+//                       without children draws its own final token.  Per-node statistics (row
+//                       maxima, log normalisers, each child's c_j and S_j with the prep's verdict)
+//                       and the draws go to the workspace.
 //   verify_walk_kernel  one CTA per sequence: validates the tree and walks it over the prep's
 //                       verdicts, committing the draft tokens of the accepted path and the final
 //                       or bonus token the prep drew where the walk stops.  With every child's

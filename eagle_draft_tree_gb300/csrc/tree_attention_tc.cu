@@ -85,6 +85,8 @@ constexpr uint32_t idesc(int M, int N, int b_mn) {
            (uint32_t(M >> 4) << 24);
 }
 constexpr uint32_t kIdescQK = idesc(128, kNkv, 0);  // N = 128 keys
+constexpr uint32_t kIdescQK64 = idesc(128, 64, 0);  // the tree tile: N = 64 keys (a tree has <= 64 nodes)
+constexpr int kTreeKeys = 64;
 constexpr uint32_t kIdescPV = idesc(128, 128, 1);  // A = P from TMEM, B = V MN-major
 
 // The MMA issuer is a whole converged warp; one lane, picked by elect.sync, issues each operation
@@ -354,26 +356,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer for both M-tiles, in a fixed order ----------------------------
         bool ok = warp_wait(&bars.q_full, 0, abort_flag, p.status);
         tc_fence_after();
-        // S_t(j) = Q_t K(j)^T into S_t (N = 128 keys)
+        // S_t(j) = Q_t K(j)^T into S_t (N = 128 keys; the tree tile's 64 first keys only, as a
+        // tree has at most 64 nodes)
         auto issue_s = [&](int t, int j) {
             const uint32_t qbase = sa(sm + t * kQTile);
             const uint32_t kbase = sa(sm + kOffK + (j % kKStages) * kTileBytes);
             const uint32_t dS = tmem + kColS + t * 128;
+            const uint32_t id = gtile(j) == nctx ? kIdescQK64 : kIdescQK;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * kQHalf + (kk & 3) * 32;
                 const uint32_t offk = (kk >> 2) * kHalf + (kk & 3) * 32;
-                umma(dS, sdesc(qbase + off, 16, 1024), sdesc(kbase + offk, 16, 1024), kIdescQK, kk > 0);
+                umma(dS, sdesc(qbase + off, 16, 1024), sdesc(kbase + offk, 16, 1024), id, kk > 0);
             }
             umma_commit(&bars.s_full[t]);
         };
-        // O_t += P_t(j) V(j), P_t read from the first 64 columns of S_t
+        // O_t += P_t(j) V(j), P_t read from the first 64 columns of S_t (the tree tile: its first
+        // 64 keys, P over the first 32 columns)
         auto issue_pv = [&](int t, int j) {
             const uint32_t vbase = sa(sm + kOffV + (j % kVStages) * kTileBytes);
             const uint32_t aP = tmem + kColS + t * 128, dO = tmem + t * 128;
+            const int nk = (gtile(j) == nctx ? kTreeKeys : kNkv) / 16;
 #pragma unroll
             for (int kk = 0; kk < kNkv / 16; ++kk)
-                umma_ts(dO, aP + kk * 8, sdesc(vbase + kk * 2048, kHalf, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                if (kk < nk)
+                    umma_ts(dO, aP + kk * 8, sdesc(vbase + kk * 2048, kHalf, 1024), kIdescPV,
+                            (j > 0 || kk > 0) ? 1u : 0u);
         };
         if (ok && (ok = warp_wait(&bars.k_full[0], 0, abort_flag, p.status))) {
             tc_fence_after();
@@ -444,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kvalid = tree ? p.n : min(kNkv, ctx - jg * kNkv);
             float tile_sum = 0.f;
 #pragma unroll 1
-            for (int q = 0; q < 2; ++q) {  // 64-key chunks
+            for (int q = 0; q < (tree ? 1 : 2); ++q) {  // 64-key chunks (the tree tile has one)
                 {
                     uint32_t raw[64];
                     uint32_t (&r0)[16] = *reinterpret_cast<uint32_t(*)[16]>(raw);
@@ -556,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 unsigned char *st = sm + kOffV + (j % kVStages) * kTileBytes;
                 // a row is 128 contiguous bytes in each half (the swizzle permutes within the row)
-                for (int i = kvalid * 8 + rho; i < kNkv * 8; i += 128) {
+                for (int i = kvalid * 8 + rho; i < (jg == nctx ? kTreeKeys : kNkv) * 8; i += 128) {
                     const int rr = i >> 3, c16 = i & 7;
                     *reinterpret_cast<uint4 *>(st + rr * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4 *>(st + kHalf + rr * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);

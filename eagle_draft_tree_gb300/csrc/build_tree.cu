@@ -313,19 +313,20 @@ struct SelSmem {
         double lc[kMaxPool];        // [R*k] the rows' child log-confidences (R*k = P <= 1024)
         uint64_t sorted[kMaxPool];  // after the depth loop: each depth's best keys, descending
     } u;
-    union {
+    struct {
         int ctok[kMaxPool];  // [R*k] the rows' child tokens
-        int kept[kMaxPool];  // after the depth loop: kept flags
     } v;
-    double logv[kMaxPool];   // pool: log V
-    uint64_t key[kMaxPool];  // pool: composite key
-    int par[kMaxPool];       // pool: parent pool index (-1: the root)
-    int row[kMaxPool];       // pool: draft row that expanded it, or -1
-    int flat[kMaxPool];      // pool: rank within its depth, then flattened index or -1
-    int ptok[kMaxPool];      // pool: token
-    int lent[kMaxPool];      // the rerank table: pool index of each sorted-list entry
+    double logv[kMaxPool];    // pool: log V
+    uint64_t key[kMaxPool];   // pool: composite key
+    int par[kMaxPool];        // pool: parent pool index (-1: the root)
+    int row[kMaxPool];        // pool: draft row that expanded it, or -1
+    int flat[kMaxPool];       // pool: rank within its depth; for a kept entry, then its flattened index
+    int ptok[kMaxPool];       // pool: token
+    int lent[kMaxPool];       // the rerank table: pool index of each sorted-list entry
     int fslot[kMaxSelDepth][16];  // frontier of each depth: pool index of slot s
-    int wsum[kMaxPool / 32];
+    unsigned kbits[kMaxPool / 32];  // kept entries, one bit each
+    int klist[64];                  // kept entries (m <= 63), in no particular order
+    int nkept;
 };
 
 // Ranks of a depth's candidates within the depth (cnt <= 256 unique keys; rank = the number of
@@ -383,9 +384,10 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     SelSmem &S = *reinterpret_cast<SelSmem *>(sel_smem_raw);
 
     const int b = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int k = a.k, R = a.R, D = a.D, m = a.m;
     const int np = k + (D - 1) * k * k;  // pool size
+    const int32_t rt = tid == 0 ? a.root_token[b] : 0;  // loaded now: only the outputs use it
 
     // the rows' children (written by the row kernel): every load in flight before the first store
     const int nload = R * k;
@@ -411,6 +413,8 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
             if (i < np) S.row[i] = -1;
         }
     }
+    if (tid < kMaxPool / 32) S.kbits[tid] = 0u;
+    if (tid == 0) S.nkept = 0;
     __syncthreads();
     // depth 1: the root's children (row 0)
     for (int i = tid; i < k; i += kSelThreads) {
@@ -476,7 +480,6 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
             S.u.sorted[idx] = S.key[e];
             S.lent[idx] = e;
         }
-        S.v.kept[e] = 0;
     }
     __syncthreads();
     for (int t = tid; t < nlist; t += kSelThreads) {
@@ -504,35 +507,23 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
                 }
             g += (pos[0] + pos[1]) + (pos[2] + pos[3]);
         }
-        if (g < m) S.v.kept[S.lent[t]] = 1;
+        if (g < m) {
+            const int e = S.lent[t];
+            atomicOr(&S.kbits[e >> 5], 1u << (e & 31));
+            const int slot = atomicAdd(&S.nkept, 1);
+            if (slot < 64) S.klist[slot] = e;
+        }
     }
     __syncthreads();
 
-    // flatten: flat index = 1 + number of kept entries created earlier (ballots over creation order)
-    const int nchunks = (np + 31) / 32;
-    for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
-        const int e = ch * 32 + lane;
-        const bool kept = e < np && S.v.kept[e];
-        const unsigned bal = __ballot_sync(0xffffffffu, kept);
-        if (lane == 0) S.wsum[ch] = __popc(bal);
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int v = lane < nchunks ? S.wsum[lane] : 0;
-        int incl = v;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            int o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        if (lane < nchunks) S.wsum[lane] = incl - v;
-    }
-    __syncthreads();
-    for (int ch = warp; ch < nchunks; ch += kSelThreads / 32) {
-        const int e = ch * 32 + lane;
-        const bool kept = e < np && S.v.kept[e];
-        const unsigned bal = __ballot_sync(0xffffffffu, kept);
-        if (e < np) S.flat[e] = kept ? 1 + S.wsum[ch] + __popc(bal & ((1u << lane) - 1u)) : -1;
+    // flatten: flat index = 1 + number of kept entries created earlier (popcounts of the kept bits)
+    const int nk = min(S.nkept, 64);
+    auto kept_bit = [&](int e) { return (S.kbits[e >> 5] >> (e & 31)) & 1u; };
+    for (int q = tid; q < nk; q += kSelThreads) {
+        const int e = S.klist[q];
+        int before = __popc(S.kbits[e >> 5] & ((1u << (e & 31)) - 1u));
+        for (int w = 0; w < (e >> 5); ++w) before += __popc(S.kbits[w]);
+        S.flat[e] = 1 + before;
     }
     __syncthreads();
 
@@ -544,7 +535,6 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
     int32_t *node_row = a.node_row + size_t(b) * n;
     uint64_t *mask = a.mask + size_t(b) * n;
     if (tid == 0) {
-        const int32_t rt = a.root_token[b];
         if (rt < 0 || rt >= a.V) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
         tokens[0] = rt;
         parents[0] = -1;
@@ -553,23 +543,22 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(SelectArgs a) 
         mask[0] = 1ull;
         if (a.node_logv) a.node_logv[size_t(b) * n] = 0.f;
     }
-    for (int e = tid; e < np; e += kSelThreads) {
+    if (tid == 0 && S.nkept != m) set_status(a.status, EAGLE_ERR_DEVICE_INPUT);  // cannot happen: m distinct keys
+    for (int q = tid; q < nk; q += kSelThreads) {
+        const int e = S.klist[q];
         const int i = S.flat[e];
-        if (i < 0) continue;
         const int pe = S.par[e];
         int pi = 0;
         if (pe >= 0) {
-            pi = S.flat[pe];
+            pi = kept_bit(pe) ? S.flat[pe] : -1;
             if (pi < 0) {  // cannot happen for a consistent pool: the kept set is ancestor-closed
                 set_status(a.status, EAGLE_ERR_DEVICE_INPUT);
                 pi = 0;
             }
         }
         uint64_t bits = 1ull | (1ull << i);
-        for (int anc = pe; anc >= 0; anc = S.par[anc]) {
-            const int fi = S.flat[anc];
-            if (fi > 0) bits |= 1ull << fi;
-        }
+        for (int anc = pe; anc >= 0; anc = S.par[anc])
+            if (kept_bit(anc)) bits |= 1ull << S.flat[anc];
         tokens[i] = S.ptok[e];
         parents[i] = pi;
         depths[i] = depth_of(e, k);

@@ -600,22 +600,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
             __nv_bfloat16 *orow = p.out + ((((size_t)l * p.B + b) * p.n + node) * p.Hq + g * p.G + gh) * p.HD;
+            // 64 columns of O per TMEM round trip (four loads, one wait)
 #pragma unroll
-            for (int cc = 0; cc < 128; cc += 16) {
-                if (cc >= p.HD) break;  // d = 64: the upper half of O is the zero padding's
-                uint32_t o[16];
-                tld16(tO + cc, o);
+            for (int c0 = 0; c0 < 128; c0 += 64) {
+                if (c0 >= p.HD) break;  // d = 64: the upper half of O is the zero padding's
+                uint32_t o[64];
+                tld16(tO + c0, *reinterpret_cast<uint32_t(*)[16]>(o));
+                tld16(tO + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(o + 16));
+                tld16(tO + c0 + 32, *reinterpret_cast<uint32_t(*)[16]>(o + 32));
+                tld16(tO + c0 + 48, *reinterpret_cast<uint32_t(*)[16]>(o + 48));
                 tld_wait();
-                uint32_t w[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(o[2 * e]) * inv,
-                                                              __uint_as_float(o[2 * e + 1]) * inv);
-                    w[e] = *reinterpret_cast<uint32_t *>(&hh);
-                }
-                if (valid) {
-                    reinterpret_cast<uint4 *>(orow + cc)[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    reinterpret_cast<uint4 *>(orow + cc)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                for (int cc = 0; cc < 64; cc += 16) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        __nv_bfloat162 hh = __floats2bfloat162_rn(__uint_as_float(o[cc + 2 * e]) * inv,
+                                                                  __uint_as_float(o[cc + 2 * e + 1]) * inv);
+                        w[e] = *reinterpret_cast<uint32_t *>(&hh);
+                    }
+                    if (valid) {
+                        reinterpret_cast<uint4 *>(orow + c0 + cc)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                        reinterpret_cast<uint4 *>(orow + c0 + cc)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    }
                 }
             }
         }

@@ -262,33 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = unit % p.Hkv;
     const int b = (unit / p.Hkv) % p.B;
     const int l = unit / (p.Hkv * p.B);
-    const int ctx = p.ctx_len[b];
-    if (ctx < 0 || ctx > p.S_max) {
-        if (tid == 0 && mg == 0 && g == 0) set_status(p.status, EAGLE_ERR_DEVICE_INPUT);
-        return;  // uniform for the CTA: nothing allocated yet
-    }
-    const int npt = 128 / p.G, rpt = npt * p.G;            // nodes and query rows of an M-tile
-    const int row0 = mg * 2 * rpt;                         // first query row of this CTA
-    const int tm = min(2, (p.rows - row0 + rpt - 1) / rpt);  // M-tiles in this CTA (1 or 2)
-    const int nctx = (ctx + kNkv - 1) / kNkv;            // context tiles
-    const int jtail = (ctx % kNkv) ? nctx - 1 : -1;      // the ragged context tile, if any
-    // This CTA's share of the unit's tiles: context tiles [c0, c1), and the tree tile in the last
-    // split.  Stages, phases and the first-tile test count local tiles j = 0 .. ntiles - 1; the
-    // coordinates and the masking use the global tile gtile(j).
-    const int tps = kSplit ? (nctx + splits - 1) / splits : nctx;
-    const int c0 = kSplit ? min(split * tps, nctx) : 0, c1 = kSplit ? min(c0 + tps, nctx) : nctx;
-    const bool has_tree = !kSplit || split == splits - 1;
-    const int ntiles = (c1 - c0) + (has_tree ? 1 : 0);
-    auto gtile = [&](int j) { return kSplit ? (j < c1 - c0 ? c0 + j : nctx) : j; };
-    const size_t pbase = (size_t(unit * splits + split) * p.mgroups + mg) * 256;  // partial rows
-    if (kSplit && ntiles == 0) {  // a split with no tile (short context): an empty partial, uniform for the CTA
-        for (int i = tid; i < 256; i += kThreads) {
-            p.part_ml[(pbase + i) * 2] = -INFINITY;
-            p.part_ml[(pbase + i) * 2 + 1] = 0.f;
-        }
-        return;
-    }
-
+    const int ctx = p.ctx_len[b];  // in flight during the set-up below, which does not depend on it
     if (tid == 0) {
         s_abort = 0;
         mbar_init(&bars.q_full, 1);
@@ -319,6 +293,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     volatile int *abort_flag = &s_abort;
+    // A context length outside [0, S_max], or (context split) a split with no tile: uniform exits
+    // for the CTA, which give back its TMEM.
+    const bool bad_ctx = ctx < 0 || ctx > p.S_max;
+    const int ctxv = bad_ctx ? 0 : ctx;
+    const int npt = 128 / p.G, rpt = npt * p.G;            // nodes and query rows of an M-tile
+    const int row0 = mg * 2 * rpt;                         // first query row of this CTA
+    const int tm = min(2, (p.rows - row0 + rpt - 1) / rpt);  // M-tiles in this CTA (1 or 2)
+    const int nctx = (ctxv + kNkv - 1) / kNkv;           // context tiles
+    const int jtail = (ctxv % kNkv) ? nctx - 1 : -1;     // the ragged context tile, if any
+    // This CTA's share of the unit's tiles: context tiles [c0, c1), and the tree tile in the last
+    // split.  Stages, phases and the first-tile test count local tiles j = 0 .. ntiles - 1; the
+    // coordinates and the masking use the global tile gtile(j).
+    const int tps = kSplit ? (nctx + splits - 1) / splits : nctx;
+    const int c0 = kSplit ? min(split * tps, nctx) : 0, c1 = kSplit ? min(c0 + tps, nctx) : nctx;
+    const bool has_tree = !kSplit || split == splits - 1;
+    const int ntiles = (c1 - c0) + (has_tree ? 1 : 0);
+    auto gtile = [&](int j) { return kSplit ? (j < c1 - c0 ? c0 + j : nctx) : j; };
+    const size_t pbase = (size_t(unit * splits + split) * p.mgroups + mg) * 256;  // partial rows
+    if (bad_ctx || (kSplit && ntiles == 0)) {
+        if (bad_ctx) {
+            if (tid == 0 && mg == 0 && g == 0) set_status(p.status, EAGLE_ERR_DEVICE_INPUT);
+        } else {  // an empty partial
+            for (int i = tid; i < 256; i += kThreads) {
+                p.part_ml[(pbase + i) * 2] = -INFINITY;
+                p.part_ml[(pbase + i) * 2 + 1] = 0.f;
+            }
+        }
+        if (warp == 1)
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+        return;
+    }
 
     int k_issued = 0, v_issued = 0;  // producer: K / V tiles whose copies were issued
     if (warp == 0) {
